@@ -1,0 +1,226 @@
+/*
+ * qmoe.h -- C ABI of the GB300 (sm_103a) weight-only block-quantised
+ * Mixture-of-Experts layer forward (QMoE).
+ *
+ * The layer computes, for T tokens x[T,H] and router logits[T,E]:
+ *
+ *   1. routing: per token, the top_k experts by fp32 logit under a total
+ *      order (-0.0 < +0.0), ties to the lower expert index, in rank order;
+ *      weights exp(l - max_all) / (sum over all E, or over the k chosen when
+ *      renormalising).  [onnx-runtime-ep-cuda src/kernels/qmoe.rs, CUDA_SRC:
+ *      total_order_key, route_value_is_better, qmoe_route]
+ *   2. grouping: per-expert counts, exclusive offsets and a stable route
+ *      permutation, then a tile work-list (experts ascending).  [qmoe.rs
+ *      launch_grouping; metrale gemm_quant_moe.rs moe_build_tile_worklist]
+ *   3. fc1: a[r,n] = sum_d x[t,d] * W1[e,n,d] with W = R_D((q - zp) * s) per
+ *      block of B along d.  [qmoe.rs decode_affine_weight; onnxruntime PR
+ *      "fused int2 mixed-input GEMM + GeGLU + fractional zero-point"
+ *      (zero_point_offset); PR "fast INT3 QMoE kernels" review item "Round
+ *      dequantized weights before accumulation"]
+ *   4. gated activation h = act(gate) * up, gate = a[:, :I], up = a[:, I:],
+ *      act = SiLU (SwiGLU) or tanh-GELU (GeGLU).  [qmoe.rs qmoe_activate,
+ *      swiglu_value; PR "fused int2 ..." GeGLU]
+ *   5. fc2: y[r,m] = sum_n h[r,n] * W2[e,m,n].
+ *   6. combine: out[t,m] = R_D(sum_j w[t,j] * y[t*k+j, m]) in slot order j.
+ *      [qmoe.rs qmoe_combine_impl]
+ *
+ * Canonical (input) tensor layouts, all contiguous row-major:
+ *   x        [T, H]   dtype D (QMOE_F32 / QMOE_F16 / QMOE_BF16)
+ *   logits   [T, E]   float32
+ *   out      [T, H]   dtype D
+ *   codes    uint8 [E, N, K*bits/8]: each row an LSB-first bit stream of K
+ *            codes (code d occupies bits [d*bits, d*bits+bits) of the row).
+ *            fc1: N = 2*inter rows [gate | up], K = hidden.
+ *            fc2: N = hidden rows, K = inter.
+ *   scales   dtype D [E, N, K/B]
+ *   zero_points uint8 [E, N, ceil((K/B)*bits/8)]: LSB-first bit stream of the
+ *            K/B per-block zero points at the weight bit width
+ *            (QMOE_ZP_UINT8 only).
+ *
+ * Conventions.
+ *   - Pointers named *_dev are device pointers; *_host are host pointers.
+ *     "stream" is a cudaStream_t passed as void* (NULL = legacy default).
+ *   - Ownership: the caller owns every pointer it passes.  The layer owns its
+ *     prepacked weights and workspace until qmoe_destroy.  Inputs to
+ *     qmoe_prepack may be freed once the stream has been synchronised.
+ *   - Errors: every call returns a qmoe_status; argument and shape checks are
+ *     synchronous.  qmoe_last_error() gives a message for the last failure on
+ *     that layer.  Device-side conditions (bounded waits that ran out) are
+ *     reported by qmoe_poll_device_status().
+ *   - Concurrency: one layer serves one stream at a time.
+ *   - Graph capture: qmoe_forward allocates nothing when num_tokens <= the
+ *     reserved count (qmoe_reserve); it may then be captured into a CUDA
+ *     graph.  Exceeding the reservation while capturing returns
+ *     QMOE_ERR_STATE.
+ */
+#ifndef QMOE_H_
+#define QMOE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct qmoe_layer qmoe_layer;
+
+typedef enum {
+  QMOE_OK = 0,
+  QMOE_ERR_INVALID_ARG = 1,   /* bad pointer, shape or value */
+  QMOE_ERR_UNSUPPORTED = 2,   /* valid QMoE, but not a supported variant */
+  QMOE_ERR_CUDA = 3,          /* a CUDA runtime call or launch failed */
+  QMOE_ERR_OOM = 4,           /* device allocation failed */
+  QMOE_ERR_STATE = 5,         /* call out of order (e.g. forward before prepack) */
+  QMOE_ERR_TIMEOUT = 6        /* a bounded device-side wait ran out */
+} qmoe_status;
+
+enum { QMOE_ZP_SYMMETRIC = 0, QMOE_ZP_UINT8 = 1, QMOE_ZP_OFFSET = 2 };
+enum { QMOE_ACT_SWIGLU = 0, QMOE_ACT_GEGLU_TANH = 1 };
+enum { QMOE_F32 = 0, QMOE_F16 = 1, QMOE_BF16 = 2 };
+
+/* Stage boundaries recorded by qmoe_set_trace_events (see there). */
+enum {
+  QMOE_TRACE_BEGIN = 0,
+  QMOE_TRACE_ROUTED = 1,     /* after routing + grouping + work-lists */
+  QMOE_TRACE_FC1 = 2,        /* after fc1 (+ fused activation) */
+  QMOE_TRACE_FC2 = 3,        /* after fc2 */
+  QMOE_TRACE_END = 4,        /* after the combine */
+  QMOE_TRACE_NUM_EVENTS = 5
+};
+
+/*
+ * Create a layer description.  Host-only: allocates no device memory.
+ *   hidden, inter   H and I (fc1 has 2*inter rows, gate then up)
+ *   experts, top_k  E (1..1024) and k (1 <= k <= E)  [qmoe.rs requires
+ *                   0 < k <= num_experts]
+ *   bits_fc1/fc2    code widths, each in {2, 3, 4}
+ *   block_size      B in {32, 64, 128}; hidden and inter must be multiples
+ *                   of B  [qmoe.rs: power of two >= 16 dividing K]
+ *   zp_mode         QMOE_ZP_SYMMETRIC (zp = 2^(bits-1)), QMOE_ZP_UINT8
+ *                   (packed zero-point tensors), QMOE_ZP_OFFSET (one
+ *                   fractional centre, set by qmoe_set_zero_point_offset)
+ *   activation      QMOE_ACT_SWIGLU or QMOE_ACT_GEGLU_TANH
+ *   dtype           activation / scale / output type
+ * Routing renormalisation defaults to on (qmoe_set_routing).
+ * Returns INVALID_ARG for out-of-range values, UNSUPPORTED (with a
+ * "requantize" hint) for widths / block sizes outside the supported set.
+ */
+qmoe_status qmoe_create(int hidden, int inter, int experts, int top_k, int bits_fc1,
+                        int bits_fc2, int block_size, int zp_mode, int activation,
+                        int dtype, qmoe_layer** out);
+
+/* Renormalise the k routing weights (1, default) or divide by the softmax
+ * sum over all E experts (0).  [qmoe.rs qmoe_route, `normalize`] */
+qmoe_status qmoe_set_routing(qmoe_layer* layer, int normalize);
+
+/* Fractional zero point for QMOE_ZP_OFFSET: w = (code - offset) * scale.
+ * [PR "fused int2 ...", zero_point_offset]  Every (code - offset) must be
+ * exactly representable in the activation type (e.g. offsets that are
+ * multiples of 1/8 for 4-bit codes); other values return UNSUPPORTED.
+ * Must be called before qmoe_prepack in that mode. */
+qmoe_status qmoe_set_zero_point_offset(qmoe_layer* layer, float offset);
+
+/* Experts with more than `min_rows` routed rows take the tensor-core grouped
+ * GEMM; the others the weight-streaming decode kernel.  Any value gives the
+ * same result within tolerance.  Default 32.  [qmoe.rs prefill_min_tokens;
+ * PR "fast INT3" kMaxProfiledExpandedRows] */
+qmoe_status qmoe_set_gemm_min_rows(qmoe_layer* layer, int min_rows);
+
+/* Size the device workspace for up to max_tokens tokens.  Required before
+ * capturing qmoe_forward into a CUDA graph.  Allocates device memory. */
+qmoe_status qmoe_reserve(qmoe_layer* layer, int64_t max_tokens);
+
+/*
+ * Copy one projection's weights (fc = 1 or 2) from the canonical layout into
+ * the layer's own GB300 layouts, on `stream`.
+ *   codes_dev        uint8 [E, N, K*bits/8]
+ *   scales_dev       D     [E, N, K/B]
+ *   zero_points_dev  uint8 [E, N, ceil((K/B)*bits/8)], non-NULL iff
+ *                    zp_mode == QMOE_ZP_UINT8 (else must be NULL)
+ * May be called again to replace the weights.  Allocates device memory.
+ */
+qmoe_status qmoe_prepack(qmoe_layer* layer, int fc, const uint8_t* codes_dev,
+                         const void* scales_dev, const uint8_t* zero_points_dev,
+                         void* stream);
+
+/*
+ * The layer forward on device buffers, asynchronous on `stream`.
+ *   x_dev       D [num_tokens, H]
+ *   logits_dev  float32 [num_tokens, E]
+ *   out_dev     D [num_tokens, H] (written)
+ * num_tokens == 0 returns QMOE_OK without launching anything.  Both fcs
+ * must have been prepacked.  No host synchronisation.
+ */
+qmoe_status qmoe_forward(qmoe_layer* layer, const void* x_dev, const float* logits_dev,
+                         void* out_dev, int64_t num_tokens, void* stream);
+
+/*
+ * The same forward on HOST buffers: copies x and logits to the device,
+ * runs qmoe_forward, copies out back and synchronises `stream`.  Pinned host
+ * memory makes the copies asynchronous DMA; pageable memory also works.
+ *   x_host D [num_tokens, H], logits_host float32 [num_tokens, E],
+ *   out_host D [num_tokens, H].
+ */
+qmoe_status qmoe_forward_host(qmoe_layer* layer, const void* x_host, const float* logits_host,
+                              void* out_host, int64_t num_tokens, void* stream);
+
+/*
+ * Routing of the last forward (device pointers, any may be NULL), enqueued
+ * on `stream`:
+ *   ids_dev     int32 [T*k]  selected experts, slot order (rank)
+ *   weights_dev float32 [T*k]
+ *   perm_dev    int32 [T*k]  routes grouped by expert, ascending r inside
+ *   offsets_dev int32 [E+1]  exclusive offsets into perm
+ */
+qmoe_status qmoe_get_routing(qmoe_layer* layer, int32_t* ids_dev, float* weights_dev,
+                             int32_t* perm_dev, int32_t* offsets_dev, void* stream);
+
+/*
+ * Tile work-list of the last forward for one kernel class (which = 0: the
+ * decode kernel, 1: the tensor-core grouped GEMM), enqueued on `stream`.
+ *   items_dev  int32 [capacity][4]: (expert, row_start, rows, 0), experts
+ *              ascending, then row_start; row_start indexes the grouped
+ *              (permuted) route order.  Each item covers at most
+ *              *m_tile_host rows.
+ *   count_dev  int32 [1]: the number of items.
+ *   m_tile_host (host, may be NULL): rows per item of that class.
+ * Returns INVALID_ARG if capacity is below the worst-case item count
+ * (qmoe_worklist_capacity).
+ */
+qmoe_status qmoe_get_worklist(qmoe_layer* layer, int which, int32_t* items_dev,
+                              int32_t* count_dev, int64_t capacity, int* m_tile_host,
+                              void* stream);
+
+/* Worst-case item count of work-list `which` for num_tokens tokens. */
+int64_t qmoe_worklist_capacity(const qmoe_layer* layer, int which, int64_t num_tokens);
+
+/*
+ * Record cudaEvent_t events[QMOE_TRACE_NUM_EVENTS] (passed as void*) on the
+ * forward's stream at the stage boundaries QMOE_TRACE_*.  NULL disables.
+ * The events are owned by the caller and must outlive their use.
+ */
+qmoe_status qmoe_set_trace_events(qmoe_layer* layer, void* const* events, int n);
+
+/* Read (and clear) the device status word: QMOE_OK, or QMOE_ERR_TIMEOUT if
+ * a bounded wait inside a kernel ran out.  Synchronises the device. */
+qmoe_status qmoe_poll_device_status(qmoe_layer* layer);
+
+/* Test hook: the iteration limit of bounded device-side waits (0 = the
+ * default).  A tiny limit makes waits run out, to exercise the error path. */
+qmoe_status qmoe_set_wait_limit(qmoe_layer* layer, int64_t iterations);
+
+/* Message of the last failed call on `layer` ("" if none); static strings
+ * for NULL layers. */
+const char* qmoe_last_error(const qmoe_layer* layer);
+
+/* Human-readable name of a status code. */
+const char* qmoe_status_string(qmoe_status status);
+
+/* Free every device buffer of the layer (synchronises the device). */
+void qmoe_destroy(qmoe_layer* layer);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* QMOE_H_ */

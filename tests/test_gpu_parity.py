@@ -1,0 +1,240 @@
+"""Parity of the CUDA path (through the C ABI) with the CPU oracle.
+
+Routing (selected experts, permutation, offsets, work-lists) must match
+bit-exactly; outputs within max|err| <= 2e-3*max|ref| + 1e-3 (f32/f16) or
+8e-3*max|ref| + 4e-3 (bf16)."""
+import numpy as np
+import pytest
+import torch
+
+from oracle import qmoe_oracle as O
+from qmoe_inputs import CONFIGS, make_inputs
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def qm():
+    from weight_only_quantized_qmoe_gb300 import build
+    build.build()
+    import weight_only_quantized_qmoe_gb300 as q
+    return q
+
+
+def run_layer(qm, inp, reserve=None, min_rows=None):
+    cfg = inp["cfg"]
+    layer = qm.QMoELayer.from_config(cfg)
+    if min_rows is not None:
+        layer.set_gemm_min_rows(min_rows)
+    if reserve:
+        layer.reserve(reserve)
+    x, logits = qm.load_inputs(layer, inp)
+    out = layer.forward(x, logits)
+    torch.cuda.synchronize()
+    assert layer.poll() == 0
+    return layer, out
+
+
+def check_routing(layer, inp):
+    cfg = inp["cfg"]
+    ids, w, perm, offs = layer.routing(cfg.T)
+    torch.cuda.synchronize()
+    rt = O.routing(inp)
+    np.testing.assert_array_equal(ids.cpu().numpy().reshape(cfg.T, cfg.k), rt["ids"])
+    np.testing.assert_array_equal(perm.cpu().numpy(), rt["perm"])
+    np.testing.assert_array_equal(offs.cpu().numpy(), rt["offsets"])
+    np.testing.assert_allclose(w.cpu().numpy().reshape(cfg.T, cfg.k), rt["weights"],
+                               rtol=2e-6, atol=1e-7)
+    # work-list of the decode kernel: the oracle's order at the same item height
+    items, m_tile = layer.worklist(0, cfg.T)
+    ref = O.build_worklist(rt["offsets"], m_tile)
+    got = [tuple(int(v) for v in row[:3]) for row in items.numpy()]
+    assert got == [(e, s, r) for e, s, r, _ in ref]
+    return rt
+
+
+def check_out(out, ref, dtype, tokens=None):
+    got = out.float().cpu().numpy().astype(np.float64)
+    if tokens is not None:
+        got = got[tokens]
+    err = np.abs(got - ref).max()
+    tol = O.tolerance(dtype, np.abs(ref).max())
+    assert err <= tol, f"max|err| {err:.3e} > tol {tol:.3e} (max|ref| {np.abs(ref).max():.3e})"
+    return err, tol
+
+
+@pytest.mark.parametrize("name", ["tiny", "decode_int2", "decode_many_expert_int4", "mixed_int3_int4"])
+def test_config_parity(qm, name):
+    inp = make_inputs(CONFIGS[name])
+    layer, out = run_layer(qm, inp)
+    check_routing(layer, inp)
+    check_out(out, O.forward(inp), inp["cfg"].dtype)
+
+
+def test_prefill_config_sampled(qm):
+    cfg = CONFIGS["prefill_int4"]
+    inp = make_inputs(cfg)
+    layer, out = run_layer(qm, inp)
+    check_routing(layer, inp)
+    rng = np.random.default_rng(11)
+    tokens = np.sort(rng.choice(cfg.T, size=12, replace=False))
+    ref = O.forward(inp, tokens=tokens)
+    check_out(out, ref, cfg.dtype, tokens)
+
+
+# ---------------------------------------------------------------------------
+# Edge cases and the variant matrix (small shapes, full oracle comparison)
+# ---------------------------------------------------------------------------
+BASE = CONFIGS["tiny"].with_(H=256, I=128, E=8, k=2, dtype="bf16", B=32)
+
+VARIANTS = {
+    "T1": dict(T=1),
+    "ragged_T37": dict(T=37),
+    "k_equals_E": dict(E=4, k=4, T=9),
+    "k1_no_renorm": dict(k=1, normalize=False, T=20),
+    "int2_f16_offset_geglu": dict(bits1=2, bits2=2, zp_mode="offset", zp_offset=1.5, dtype="f16",
+                                  act="geglu", B=128, T=6),
+    "int2_K_much_larger_than_64": dict(bits1=2, bits2=2, H=1024, I=512, B=64, T=5),
+    "int3_sym_B32": dict(bits1=3, bits2=3, B=32, T=11),
+    "int3_uint8_B64": dict(bits1=3, bits2=4, zp_mode="uint8", zp_lo=0, zp_hi=7, B=64, T=7),
+    "int4_uint8_f16_B128": dict(zp_mode="uint8", zp_lo=5, zp_hi=11, dtype="f16", B=128, T=13),
+    "int2_uint8_B32": dict(bits1=2, bits2=2, zp_mode="uint8", zp_lo=0, zp_hi=3, B=32, T=10),
+    "mixed_4_2_geglu_bf16": dict(bits1=4, bits2=2, act="geglu", T=16),
+    "K_not_multiple_of_64": dict(H=96, I=96, B=32, T=6),
+    "f32_int3_offset": dict(dtype="f32", bits1=3, bits2=2, zp_mode="offset", zp_offset=2.5, T=5),
+    "f32_uint8": dict(dtype="f32", zp_mode="uint8", zp_lo=3, zp_hi=12, T=9),
+    "many_tokens_one_group": dict(T=300, E=4, k=2),
+    "wide_E_256": dict(E=256, k=6, T=40),
+}
+
+
+@pytest.mark.parametrize("name", list(VARIANTS))
+def test_variant_parity(qm, name):
+    cfg = BASE.with_(**VARIANTS[name])
+    inp = make_inputs(cfg)
+    layer, out = run_layer(qm, inp)
+    check_routing(layer, inp)
+    check_out(out, O.forward(inp), cfg.dtype)
+
+
+def test_all_tokens_on_one_expert_and_empty_experts(qm):
+    cfg = BASE.with_(T=40, k=2, E=8)
+    inp = make_inputs(cfg)
+    logits = inp["logits"].clone()
+    logits[:, 3] += 50.0          # every token picks expert 3 first
+    logits[:, 5] += 40.0          # ... and expert 5 second; the others stay empty
+    inp["logits"] = logits
+    layer, out = run_layer(qm, inp)
+    rt = check_routing(layer, inp)
+    assert rt["counts"][3] == 40 and rt["counts"][5] == 40 and rt["counts"].sum() == 80
+    check_out(out, O.forward(inp), cfg.dtype)
+
+
+def test_tied_logits_lowest_index_wins(qm):
+    cfg = BASE.with_(T=16, E=8, k=3)
+    inp = make_inputs(cfg)
+    lg = np.zeros((16, 8), np.float32)
+    lg[:, ::2] = -0.0            # -0.0 ranks below +0.0
+    lg[3] = 1.0
+    inp["logits"] = torch.from_numpy(lg)
+    layer, out = run_layer(qm, inp)
+    rt = check_routing(layer, inp)
+    assert list(rt["ids"][0]) == [1, 3, 5]
+    check_out(out, O.forward(inp), cfg.dtype)
+
+
+def test_zero_tokens_and_growth(qm):
+    cfg = BASE.with_(T=6)
+    inp = make_inputs(cfg)
+    layer = qm.QMoELayer.from_config(cfg)
+    layer.reserve(2)
+    x, logits = qm.load_inputs(layer, inp)
+    empty = torch.empty((0, cfg.H), dtype=x.dtype, device="cuda")
+    layer.forward(empty, logits[:0])                 # no work, no error
+    out = layer.forward(x, logits)                   # grows past the reservation
+    torch.cuda.synchronize()
+    check_out(out, O.forward(inp), cfg.dtype)
+
+
+def test_graph_capture_replay_matches_eager(qm):
+    cfg = CONFIGS["decode_int2"]
+    inp = make_inputs(cfg)
+    layer = qm.QMoELayer.from_config(cfg)
+    layer.reserve(cfg.T)
+    x, logits = qm.load_inputs(layer, inp)
+    eager = layer.forward(x, logits).clone()
+    out = torch.empty_like(x)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        layer.forward(x, logits, out, stream=s)      # warm on the capture stream
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        layer.forward(x, logits, out, stream=s)
+    out.zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(out, eager)                   # deterministic
+    check_out(out, O.forward(inp), cfg.dtype)
+
+
+def test_capture_beyond_reservation_is_refused(qm):
+    cfg = BASE.with_(T=8)
+    inp = make_inputs(cfg)
+    layer = qm.QMoELayer.from_config(cfg)
+    layer.reserve(4)
+    x, logits = qm.load_inputs(layer, inp)
+    s = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    with pytest.raises(qm.QMoEError) as ei:
+        with torch.cuda.graph(g, stream=s):
+            layer.forward(x, logits, stream=s)
+    assert ei.value.status == qm.QMOE_ERR_STATE
+
+
+def test_forward_host_matches_device(qm):
+    cfg = CONFIGS["decode_many_expert_int4"]
+    inp = make_inputs(cfg)
+    layer = qm.QMoELayer.from_config(cfg)
+    layer.reserve(cfg.T)
+    x, logits = qm.load_inputs(layer, inp)
+    dev = layer.forward(x, logits)
+    xh = inp["x"].pin_memory()
+    lh = inp["logits"].pin_memory()
+    oh = torch.empty_like(xh).pin_memory()
+    layer.forward_host(xh, lh, oh)
+    torch.cuda.synchronize()
+    assert torch.equal(oh, dev.cpu())
+
+
+def test_bounded_wait_reports_timeout_and_context_survives(qm):
+    # A wait limit of one poll makes the first stage wait run out; the kernel
+    # records QMOE_ERR_TIMEOUT, drains its own copies and returns.
+    cfg = BASE.with_(T=4)
+    inp = make_inputs(cfg)
+    layer = qm.QMoELayer.from_config(cfg)
+    x, logits = qm.load_inputs(layer, inp)
+    layer.set_wait_limit(1)
+    layer.forward(x, logits)
+    torch.cuda.synchronize()
+    assert layer.poll() == qm.QMOE_ERR_TIMEOUT
+    layer.set_wait_limit(0)                          # back to the default
+    out = layer.forward(x, logits)
+    torch.cuda.synchronize()
+    assert layer.poll() == 0
+    check_out(out, O.forward(inp), cfg.dtype)
+
+
+def test_trace_events_bracket_stages(qm):
+    cfg = CONFIGS["decode_int2"]
+    inp = make_inputs(cfg)
+    layer = qm.QMoELayer.from_config(cfg)
+    x, logits = qm.load_inputs(layer, inp)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(qm.QMOE_TRACE_NUM_EVENTS)]
+    layer.set_trace_events(ev)
+    layer.forward(x, logits)
+    torch.cuda.synchronize()
+    times = [ev[i].elapsed_time(ev[i + 1]) for i in range(len(ev) - 1)]
+    assert all(t >= 0 for t in times)
+    layer.set_trace_events(None)

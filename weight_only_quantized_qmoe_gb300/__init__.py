@@ -1,0 +1,150 @@
+"""GB300 (sm_103a) weight-only block-quantised MoE layer forward (QMoE).
+
+The compute lives in ``libqmoe.so`` (C ABI, ``include/qmoe.h``); this package
+holds its ctypes binding (:mod:`.binding`, the C names) and :class:`QMoELayer`,
+a convenience owner of one layer handle that takes torch CUDA tensors.
+PyTorch is used only for device memory and streams.
+"""
+from __future__ import annotations
+
+from . import binding
+from .binding import *  # noqa: F401,F403  (the C-ABI names)
+
+_DT = {"f32": binding.QMOE_F32, "f16": binding.QMOE_F16, "bf16": binding.QMOE_BF16}
+_ZP = {"sym": binding.QMOE_ZP_SYMMETRIC, "uint8": binding.QMOE_ZP_UINT8,
+       "offset": binding.QMOE_ZP_OFFSET}
+_ACT = {"swiglu": binding.QMOE_ACT_SWIGLU, "geglu": binding.QMOE_ACT_GEGLU_TANH}
+
+
+class QMoEError(RuntimeError):
+    def __init__(self, status, msg):
+        super().__init__(f"{binding.qmoe_status_string(status)}: {msg}")
+        self.status = status
+
+
+def _ptr(t):
+    return 0 if t is None else t.data_ptr()
+
+
+def _stream(stream):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream
+
+
+class QMoELayer:
+    """One QMoE layer on the current CUDA device.
+
+    Parameters mirror ``qmoe_create``; string forms are accepted for
+    ``zp_mode`` ("sym" | "uint8" | "offset"), ``activation`` ("swiglu" |
+    "geglu") and ``dtype`` ("f32" | "f16" | "bf16").
+    """
+
+    def __init__(self, hidden, inter, experts, top_k, bits_fc1, bits_fc2, block_size,
+                 zp_mode="sym", activation="swiglu", dtype="bf16", normalize=True,
+                 zp_offset=None):
+        zp = _ZP.get(zp_mode, zp_mode)
+        act = _ACT.get(activation, activation)
+        dt = _DT.get(dtype, dtype)
+        st, h = binding.qmoe_create(hidden, inter, experts, top_k, bits_fc1, bits_fc2,
+                                    block_size, zp, act, dt)
+        if st != binding.QMOE_OK:
+            raise QMoEError(st, "qmoe_create rejected the configuration")
+        self.handle = h
+        self.hidden, self.inter, self.experts, self.top_k = hidden, inter, experts, top_k
+        self._check(binding.qmoe_set_routing(h, normalize))
+        if zp_offset is not None:
+            self._check(binding.qmoe_set_zero_point_offset(h, zp_offset))
+
+    @classmethod
+    def from_config(cls, cfg):
+        return cls(cfg.H, cfg.I, cfg.E, cfg.k, cfg.bits1, cfg.bits2, cfg.B, cfg.zp_mode,
+                   cfg.act, cfg.dtype, cfg.normalize,
+                   cfg.zp_offset if cfg.zp_mode == "offset" else None)
+
+    def _check(self, st):
+        if st != binding.QMOE_OK:
+            raise QMoEError(st, binding.qmoe_last_error(self.handle))
+
+    def reserve(self, max_tokens):
+        self._check(binding.qmoe_reserve(self.handle, max_tokens))
+
+    def set_gemm_min_rows(self, n):
+        self._check(binding.qmoe_set_gemm_min_rows(self.handle, n))
+
+    def prepack(self, fc, codes, scales, zp=None, stream=None):
+        self._check(binding.qmoe_prepack(self.handle, fc, _ptr(codes), _ptr(scales), _ptr(zp),
+                                         _stream(stream)))
+
+    def forward(self, x, logits, out=None, stream=None):
+        import torch
+        if out is None:
+            out = torch.empty_like(x)
+        self._check(binding.qmoe_forward(self.handle, _ptr(x), _ptr(logits), _ptr(out),
+                                         x.shape[0], _stream(stream)))
+        return out
+
+    def forward_host(self, x_host, logits_host, out_host, stream=None):
+        self._check(binding.qmoe_forward_host(self.handle, _ptr(x_host), _ptr(logits_host),
+                                              _ptr(out_host), x_host.shape[0], _stream(stream)))
+        return out_host
+
+    def routing(self, T, stream=None):
+        import torch
+        R = T * self.top_k
+        dev = torch.device("cuda")
+        ids = torch.empty(R, dtype=torch.int32, device=dev)
+        w = torch.empty(R, dtype=torch.float32, device=dev)
+        perm = torch.empty(R, dtype=torch.int32, device=dev)
+        offs = torch.empty(self.experts + 1, dtype=torch.int32, device=dev)
+        self._check(binding.qmoe_get_routing(self.handle, _ptr(ids), _ptr(w), _ptr(perm),
+                                             _ptr(offs), _stream(stream)))
+        return ids, w, perm, offs
+
+    def worklist(self, which, T, stream=None):
+        import torch
+        cap = binding.qmoe_worklist_capacity(self.handle, which, T)
+        items = torch.empty((cap, 4), dtype=torch.int32, device="cuda")
+        cnt = torch.empty(1, dtype=torch.int32, device="cuda")
+        st, m_tile = binding.qmoe_get_worklist(self.handle, which, _ptr(items), _ptr(cnt), cap,
+                                               _stream(stream))
+        self._check(st)
+        torch.cuda.synchronize()
+        return items[: int(cnt.item())].cpu(), m_tile
+
+    def set_trace_events(self, events):
+        self._check(binding.qmoe_set_trace_events(
+            self.handle, None if events is None else [e.cuda_event for e in events]))
+
+    def poll(self):
+        return binding.qmoe_poll_device_status(self.handle)
+
+    def set_wait_limit(self, n):
+        self._check(binding.qmoe_set_wait_limit(self.handle, n))
+
+    def close(self):
+        if getattr(self, "handle", None):
+            binding.qmoe_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def load_inputs(layer: QMoELayer, inp: dict, device="cuda"):
+    """Move one workload (qmoe_inputs.make_inputs) to the device and prepack
+    it.  Returns (x, logits) device tensors."""
+    for fc in (1, 2):
+        pre = f"fc{fc}_"
+        codes = inp[pre + "codes"].to(device)
+        scales = inp[pre + "scales"].to(device)
+        zp = inp[pre + "zp"]
+        zp = zp.to(device) if zp is not None else None
+        layer.prepack(fc, codes, scales, zp)
+    import torch
+    torch.cuda.synchronize()
+    return inp["x"].to(device), inp["logits"].to(device)

@@ -1,0 +1,575 @@
+// C ABI of the QMoE layer (include/qmoe.h): validation, device memory
+// ownership, prepack and the forward's launch sequence on one stream.
+//
+// Launch sequence of qmoe_forward (all on the caller's stream, no host sync,
+// no allocation once reserved -> capturable into a CUDA graph):
+//   route + group + work-lists    (1 CTA for small T; route grid + 1 CTA else)
+//   fc1 (+ fused GLU)             decode mma kernel   | SIMT kernel for f32
+//   fc2                           decode mma kernel   | SIMT kernel for f32
+//   combine                       slot-ordered weighted sum, round into D
+// Consecutive kernels use programmatic dependent launch.
+#include <climits>
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+
+#include "qmoe_internal.cuh"
+
+using namespace qmoe;
+
+namespace {
+
+struct Proj {
+  uint8_t* codes = nullptr;
+  void* scales = nullptr;
+  uint8_t* zp = nullptr;
+  uint8_t* dec = nullptr;
+  size_t codes_bytes = 0, scales_bytes = 0, zp_bytes = 0, dec_bytes = 0;
+  int N = 0, K = 0, bits = 0, zp_row = 0;
+  DecodeLayout L{};
+  bool ready = false;
+};
+
+const char* kStatusNames[] = {"QMOE_OK",          "QMOE_ERR_INVALID_ARG", "QMOE_ERR_UNSUPPORTED",
+                              "QMOE_ERR_CUDA",    "QMOE_ERR_OOM",         "QMOE_ERR_STATE",
+                              "QMOE_ERR_TIMEOUT"};
+
+constexpr long long kDefaultWaitLimit = 1LL << 24;
+
+}  // namespace
+
+struct qmoe_layer {
+  int H, I, E, k, B, zp_mode, act, dtype, dsize;
+  int bits[2];
+  int normalize = 1;
+  float zp_offset = NAN;
+  bool offset_set = false;
+  int gemm_min_rows = 32;
+  int device = -1;
+  long long wait_limit = kDefaultWaitLimit;
+  Proj proj[2];
+
+  // workspace for up to cap_T tokens
+  int64_t cap_T = 0;
+  int* ids = nullptr;
+  float* w = nullptr;
+  int* counts = nullptr;
+  int* offsets = nullptr;
+  int* perm = nullptr;
+  int* pos = nullptr;
+  int* n_items = nullptr;
+  Item* items[2] = {nullptr, nullptr};
+  int cap_items[2] = {0, 0};
+  void* hbuf = nullptr;
+  float* ybuf = nullptr;
+  int* status = nullptr;
+  void* x_stage = nullptr;
+  float* logits_stage = nullptr;
+  void* out_stage = nullptr;
+
+  int64_t last_T = 0;
+  int last_tb[2] = {0, 0};
+  cudaEvent_t trace[QMOE_TRACE_NUM_EVENTS] = {};
+  bool trace_on = false;
+  std::string err;
+};
+
+namespace {
+
+qmoe_status fail(qmoe_layer* l, qmoe_status st, const std::string& msg) {
+  if (l) l->err = msg;
+  return st;
+}
+
+qmoe_status cuda_fail(qmoe_layer* l, cudaError_t e, const char* what) {
+  cudaGetLastError();  // clear a sticky launch error if any
+  const qmoe_status st = e == cudaErrorMemoryAllocation ? QMOE_ERR_OOM : QMOE_ERR_CUDA;
+  return fail(l, st, std::string(what) + ": " + cudaGetErrorString(e));
+}
+
+#define QMOE_CUDA(layer, call, what)                 \
+  do {                                               \
+    cudaError_t e_ = (call);                         \
+    if (e_ != cudaSuccess) return cuda_fail(layer, e_, what); \
+  } while (0)
+
+bool exact_in(double v, int dtype) {
+  // Is v exactly representable (finite, normal or zero) in dtype?
+  if (v == 0.0) return true;
+  if (!std::isfinite(v)) return false;
+  const int p = dtype == QMOE_F32 ? 24 : dtype == QMOE_F16 ? 11 : 8;
+  const int emin = dtype == QMOE_F16 ? -14 : -126;
+  const int emax = dtype == QMOE_F16 ? 15 : 127;
+  int e;
+  const double m = std::frexp(v, &e);  // v = m * 2^e, 0.5 <= |m| < 1
+  if (e - 1 < emin || e - 1 > emax) return false;
+  const double scaled = std::ldexp(m, p);
+  return scaled == std::floor(scaled);
+}
+
+template <typename T>
+cudaError_t dalloc(T** p, size_t bytes) {
+  *p = nullptr;
+  if (bytes == 0) bytes = 16;
+  return cudaMalloc(reinterpret_cast<void**>(p), bytes);
+}
+
+void free_workspace(qmoe_layer* l) {
+  void* bufs[] = {l->ids, l->w, l->counts, l->offsets, l->perm, l->pos, l->n_items, l->items[0],
+                  l->items[1], l->hbuf, l->ybuf, l->status, l->x_stage, l->logits_stage,
+                  l->out_stage};
+  for (void* b : bufs)
+    if (b) cudaFree(b);
+  l->ids = nullptr;
+  l->w = nullptr;
+  l->counts = l->offsets = l->perm = l->pos = l->n_items = nullptr;
+  l->items[0] = l->items[1] = nullptr;
+  l->hbuf = nullptr;
+  l->ybuf = nullptr;
+  l->status = nullptr;
+  l->x_stage = nullptr;
+  l->logits_stage = nullptr;
+  l->out_stage = nullptr;
+  l->cap_T = 0;
+}
+
+// Rows per work item of each class for a forward of T tokens.
+void item_heights(const qmoe_layer* l, int64_t T, int* tb0, int* tb1) {
+  if (l->dtype == QMOE_F32) {
+    *tb0 = 4;  // SIMT kernel
+  } else {
+    const int64_t R = T * l->k;
+    const int64_t active = R < l->E ? R : l->E;
+    const double per = active > 0 ? (double)R / (double)active : 1.0;
+    int ng = per <= 8.0 ? 1 : per <= 12.0 ? 2 : 4;
+    // The staged rows (ng * 8 tokens x K, 16-bit) must fit in shared memory
+    // next to the weight ring: cap ng by the longer K of the two projections.
+    const int kmax = l->H > l->I ? l->H : l->I;
+    const int ktiles = (kmax + 127) / 128 * 8;
+    while (ng > 1 && ng * ktiles * 256 > 160 * 1024) ng /= 2;
+    *tb0 = 8 * ng;
+  }
+  *tb1 = 128;
+}
+
+int64_t items_cap(const qmoe_layer* l, int which, int64_t T, int tb) {
+  const int64_t R = T * l->k;
+  const int64_t active = R < l->E ? R : l->E;
+  return active + R / (tb > 0 ? tb : 1) + 1;
+}
+
+qmoe_status ensure_workspace(qmoe_layer* l, int64_t T) {
+  if (T <= l->cap_T) return QMOE_OK;
+  free_workspace(l);
+  const int64_t R = T * l->k;
+  const size_t ds = (size_t)l->dsize;
+  QMOE_CUDA(l, dalloc(&l->ids, R * sizeof(int)), "allocate workspace");
+  QMOE_CUDA(l, dalloc(&l->w, R * sizeof(float)), "allocate workspace");
+  QMOE_CUDA(l, dalloc(&l->counts, l->E * sizeof(int)), "allocate workspace");
+  QMOE_CUDA(l, dalloc(&l->offsets, (l->E + 1) * sizeof(int)), "allocate workspace");
+  QMOE_CUDA(l, dalloc(&l->perm, R * sizeof(int)), "allocate workspace");
+  QMOE_CUDA(l, dalloc(&l->pos, R * sizeof(int)), "allocate workspace");
+  QMOE_CUDA(l, dalloc(&l->n_items, 2 * sizeof(int)), "allocate workspace");
+  for (int c = 0; c < 2; ++c) {
+    const int64_t cap = items_cap(l, c, T, 4);
+    if (cap > INT_MAX / 2) return fail(l, QMOE_ERR_INVALID_ARG, "token count too large");
+    l->cap_items[c] = (int)cap;
+    QMOE_CUDA(l, dalloc(&l->items[c], cap * sizeof(Item)), "allocate workspace");
+  }
+  QMOE_CUDA(l, dalloc(&l->hbuf, (size_t)R * l->I * ds), "allocate workspace");
+  QMOE_CUDA(l, dalloc(&l->ybuf, (size_t)R * l->H * sizeof(float)), "allocate workspace");
+  QMOE_CUDA(l, dalloc(&l->status, sizeof(int)), "allocate workspace");
+  QMOE_CUDA(l, cudaMemset(l->status, 0, sizeof(int)), "clear status");
+  QMOE_CUDA(l, dalloc(&l->x_stage, (size_t)T * l->H * ds), "allocate workspace");
+  QMOE_CUDA(l, dalloc(&l->logits_stage, (size_t)T * l->E * sizeof(float)), "allocate workspace");
+  QMOE_CUDA(l, dalloc(&l->out_stage, (size_t)T * l->H * ds), "allocate workspace");
+  l->cap_T = T;
+  return QMOE_OK;
+}
+
+bool capturing(cudaStream_t s) {
+  cudaStreamCaptureStatus st = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(s, &st) != cudaSuccess) return false;
+  return st != cudaStreamCaptureStatusNone;
+}
+
+void trace(qmoe_layer* l, int i, cudaStream_t s) {
+  // Under stream capture the record becomes an event-record node of the graph.
+  if (l->trace_on && l->trace[i])
+    cudaEventRecordWithFlags(l->trace[i], s, capturing(s) ? cudaEventRecordExternal : cudaEventRecordDefault);
+}
+
+}  // namespace
+
+extern "C" {
+
+qmoe_status qmoe_create(int hidden, int inter, int experts, int top_k, int bits_fc1, int bits_fc2,
+                        int block_size, int zp_mode, int activation, int dtype, qmoe_layer** out) {
+  if (!out) return QMOE_ERR_INVALID_ARG;
+  *out = nullptr;
+  if (hidden <= 0 || inter <= 0 || experts <= 0 || top_k <= 0) return QMOE_ERR_INVALID_ARG;
+  if (experts > 1024) return QMOE_ERR_UNSUPPORTED;
+  if (top_k > experts) return QMOE_ERR_INVALID_ARG;
+  for (int b : {bits_fc1, bits_fc2})
+    if (b != 2 && b != 3 && b != 4) return QMOE_ERR_UNSUPPORTED;
+  if (block_size != 32 && block_size != 64 && block_size != 128) return QMOE_ERR_UNSUPPORTED;
+  if (hidden % block_size || inter % block_size) return QMOE_ERR_INVALID_ARG;
+  if (zp_mode < QMOE_ZP_SYMMETRIC || zp_mode > QMOE_ZP_OFFSET) return QMOE_ERR_INVALID_ARG;
+  if (activation != QMOE_ACT_SWIGLU && activation != QMOE_ACT_GEGLU_TANH) return QMOE_ERR_INVALID_ARG;
+  if (dtype < QMOE_F32 || dtype > QMOE_BF16) return QMOE_ERR_INVALID_ARG;
+  if ((long long)hidden * inter > (1LL << 31)) return QMOE_ERR_UNSUPPORTED;
+  qmoe_layer* l = new qmoe_layer();
+  l->H = hidden;
+  l->I = inter;
+  l->E = experts;
+  l->k = top_k;
+  l->bits[0] = bits_fc1;
+  l->bits[1] = bits_fc2;
+  l->B = block_size;
+  l->zp_mode = zp_mode;
+  l->act = activation;
+  l->dtype = dtype;
+  l->dsize = dtype == QMOE_F32 ? 4 : 2;
+  *out = l;
+  return QMOE_OK;
+}
+
+qmoe_status qmoe_set_routing(qmoe_layer* l, int normalize) {
+  if (!l) return QMOE_ERR_INVALID_ARG;
+  l->normalize = normalize ? 1 : 0;
+  return QMOE_OK;
+}
+
+qmoe_status qmoe_set_zero_point_offset(qmoe_layer* l, float offset) {
+  if (!l) return QMOE_ERR_INVALID_ARG;
+  if (l->zp_mode != QMOE_ZP_OFFSET)
+    return fail(l, QMOE_ERR_STATE, "zero_point_offset needs zp_mode == QMOE_ZP_OFFSET");
+  if (!std::isfinite(offset)) return fail(l, QMOE_ERR_INVALID_ARG, "zero_point_offset must be finite");
+  for (int f = 0; f < 2; ++f)
+    for (int c = 0; c < (1 << l->bits[f]); ++c)
+      if (!exact_in((double)c - (double)offset, l->dtype) || !exact_in((double)offset, l->dtype))
+        return fail(l, QMOE_ERR_UNSUPPORTED,
+                    "zero_point_offset: (code - offset) is not exact in the activation type; "
+                    "requantize with a coarser fractional centre");
+  l->zp_offset = offset;
+  l->offset_set = true;
+  return QMOE_OK;
+}
+
+qmoe_status qmoe_set_gemm_min_rows(qmoe_layer* l, int min_rows) {
+  if (!l || min_rows < 0) return QMOE_ERR_INVALID_ARG;
+  l->gemm_min_rows = min_rows;
+  return QMOE_OK;
+}
+
+qmoe_status qmoe_set_wait_limit(qmoe_layer* l, int64_t iterations) {
+  if (!l || iterations < 0) return QMOE_ERR_INVALID_ARG;
+  l->wait_limit = iterations == 0 ? kDefaultWaitLimit : iterations;
+  return QMOE_OK;
+}
+
+qmoe_status qmoe_reserve(qmoe_layer* l, int64_t max_tokens) {
+  if (!l || max_tokens < 0) return QMOE_ERR_INVALID_ARG;
+  if ((max_tokens * l->k) > INT_MAX / 8) return fail(l, QMOE_ERR_INVALID_ARG, "max_tokens too large");
+  if (max_tokens == 0) return QMOE_OK;
+  return ensure_workspace(l, max_tokens);
+}
+
+qmoe_status qmoe_prepack(qmoe_layer* l, int fc, const uint8_t* codes, const void* scales,
+                         const uint8_t* zero_points, void* stream) {
+  if (!l) return QMOE_ERR_INVALID_ARG;
+  if (fc != 1 && fc != 2) return fail(l, QMOE_ERR_INVALID_ARG, "fc must be 1 or 2");
+  if (!codes || !scales) return fail(l, QMOE_ERR_INVALID_ARG, "codes and scales are required");
+  if ((zero_points != nullptr) != (l->zp_mode == QMOE_ZP_UINT8))
+    return fail(l, QMOE_ERR_INVALID_ARG, "zero_points must be given iff zp_mode == QMOE_ZP_UINT8");
+  if (l->zp_mode == QMOE_ZP_OFFSET && !l->offset_set)
+    return fail(l, QMOE_ERR_STATE, "call qmoe_set_zero_point_offset before qmoe_prepack");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  Proj& p = l->proj[fc - 1];
+  p.bits = l->bits[fc - 1];
+  p.N = fc == 1 ? 2 * l->I : l->H;
+  p.K = fc == 1 ? l->H : l->I;
+  const size_t E = (size_t)l->E;
+  const size_t codes_bytes = E * p.N * ((size_t)p.K * p.bits / 8);
+  const size_t scales_bytes = E * p.N * (size_t)(p.K / l->B) * l->dsize;
+  p.zp_row = (p.K / l->B * p.bits + 7) / 8;
+  const size_t zp_bytes = zero_points ? E * p.N * (size_t)p.zp_row : 0;
+  int dev = -1;
+  QMOE_CUDA(l, cudaGetDevice(&dev), "cudaGetDevice");
+  if (l->device >= 0 && l->device != dev)
+    return fail(l, QMOE_ERR_STATE, "prepack on a different device than the layer's");
+  l->device = dev;
+  if (p.codes_bytes != codes_bytes) {
+    if (p.codes) cudaFree(p.codes);
+    QMOE_CUDA(l, dalloc(&p.codes, codes_bytes), "allocate codes");
+    p.codes_bytes = codes_bytes;
+  }
+  if (p.scales_bytes != scales_bytes) {
+    if (p.scales) cudaFree(p.scales);
+    QMOE_CUDA(l, dalloc(&p.scales, scales_bytes), "allocate scales");
+    p.scales_bytes = scales_bytes;
+  }
+  if (p.zp_bytes != zp_bytes) {
+    if (p.zp) cudaFree(p.zp);
+    p.zp = nullptr;
+    if (zp_bytes) QMOE_CUDA(l, dalloc(&p.zp, zp_bytes), "allocate zero points");
+    p.zp_bytes = zp_bytes;
+  }
+  QMOE_CUDA(l, cudaMemcpyAsync(p.codes, codes, codes_bytes, cudaMemcpyDeviceToDevice, s), "copy codes");
+  QMOE_CUDA(l, cudaMemcpyAsync(p.scales, scales, scales_bytes, cudaMemcpyDeviceToDevice, s), "copy scales");
+  if (zp_bytes)
+    QMOE_CUDA(l, cudaMemcpyAsync(p.zp, zero_points, zp_bytes, cudaMemcpyDeviceToDevice, s), "copy zp");
+  if (l->dtype != QMOE_F32) {
+    p.L = make_decode_layout(p.bits, l->B, fc == 1 ? l->I : l->H, p.K, fc == 1 ? 2 : 1, l->zp_mode,
+                             l->dsize);
+    const size_t dec_bytes = p.L.expert_bytes * E;
+    if (p.dec_bytes != dec_bytes) {
+      if (p.dec) cudaFree(p.dec);
+      QMOE_CUDA(l, dalloc(&p.dec, dec_bytes), "allocate decode layout");
+      p.dec_bytes = dec_bytes;
+    }
+    RepackArgs ra{};
+    ra.codes = p.codes;
+    ra.scales = p.scales;
+    ra.zp = p.zp;
+    ra.out = p.dec;
+    ra.E = l->E;
+    ra.N = p.N;
+    ra.K = p.K;
+    ra.I_or_0 = fc == 1 ? l->I : 0;
+    ra.dsize = l->dsize;
+    ra.L = p.L;
+    QMOE_CUDA(l, launch_repack_decode(ra, s), "repack weights");
+  }
+  p.ready = true;
+  return QMOE_OK;
+}
+
+qmoe_status qmoe_forward(qmoe_layer* l, const void* x, const float* logits, void* out,
+                         int64_t T, void* stream) {
+  if (!l) return QMOE_ERR_INVALID_ARG;
+  if (T < 0) return fail(l, QMOE_ERR_INVALID_ARG, "num_tokens < 0");
+  if (T == 0) return QMOE_OK;
+  if (!x || !logits || !out) return fail(l, QMOE_ERR_INVALID_ARG, "null x / logits / out");
+  if (!l->proj[0].ready || !l->proj[1].ready)
+    return fail(l, QMOE_ERR_STATE, "prepack fc1 and fc2 before qmoe_forward");
+  if (T * l->k > INT_MAX / 8) return fail(l, QMOE_ERR_INVALID_ARG, "num_tokens too large");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (T > l->cap_T) {
+    if (capturing(s))
+      return fail(l, QMOE_ERR_STATE, "num_tokens exceeds the reservation during graph capture");
+    const qmoe_status st = ensure_workspace(l, T);
+    if (st != QMOE_OK) return st;
+  }
+  int tb0, tb1;
+  item_heights(l, T, &tb0, &tb1);
+  l->last_T = T;
+  l->last_tb[0] = tb0;
+  l->last_tb[1] = tb1;
+  const int R = (int)(T * l->k);
+  const WaitCfg wait{l->status, l->wait_limit};
+
+  trace(l, QMOE_TRACE_BEGIN, s);
+  RouteArgs ra{};
+  ra.logits = logits;
+  ra.T = (int)T;
+  ra.E = l->E;
+  ra.k = l->k;
+  ra.normalize = l->normalize;
+  ra.ids = l->ids;
+  ra.w = l->w;
+  ra.counts = l->counts;
+  ra.offsets = l->offsets;
+  ra.perm = l->perm;
+  ra.pos = l->pos;
+  ra.items[0] = l->items[0];
+  ra.items[1] = l->items[1];
+  ra.n_items = l->n_items;
+  ra.tb[0] = tb0;
+  ra.tb[1] = tb1;
+  ra.threshold = INT_MAX;  // every expert takes the decode/SIMT kernel
+  ra.cap[0] = (int)items_cap(l, 0, T, tb0);
+  ra.cap[1] = (int)items_cap(l, 1, T, tb1);
+  QMOE_CUDA(l, launch_route_group(ra, T <= 64, s), "launch routing");
+  trace(l, QMOE_TRACE_ROUTED, s);
+
+  for (int f = 0; f < 2; ++f) {
+    const Proj& p = l->proj[f];
+    if (l->dtype == QMOE_F32) {
+      SimtArgs sa{};
+      sa.codes = p.codes;
+      sa.scales = p.scales;
+      sa.zp = p.zp;
+      sa.bits = p.bits;
+      sa.B = l->B;
+      sa.K = p.K;
+      sa.N_out = f == 0 ? l->I : l->H;
+      sa.I_or_0 = f == 0 ? l->I : 0;
+      sa.zp_bytes_row = p.zp_row;
+      sa.items = l->items[0];
+      sa.n_items = l->n_items;
+      sa.max_items = ra.cap[0];
+      sa.src = f == 0 ? x : l->hbuf;
+      sa.perm = l->perm;
+      sa.k = l->k;
+      sa.fc = f + 1;
+      sa.dtype = l->dtype;
+      sa.act = l->act;
+      sa.zp_mode = l->zp_mode;
+      sa.zp_offset = l->zp_offset;
+      sa.dst = f == 0 ? l->hbuf : (void*)l->ybuf;
+      sa.E = l->E;
+      QMOE_CUDA(l, launch_simt(sa, s), "launch SIMT projection");
+    } else {
+      DecodeArgs da{};
+      da.wpk = p.dec;
+      da.L = p.L;
+      da.K = p.K;
+      da.N_out = f == 0 ? l->I : l->H;
+      da.items = l->items[0];
+      da.n_items = l->n_items;
+      da.max_items = ra.cap[0];
+      da.src = f == 0 ? x : l->hbuf;
+      da.perm = l->perm;
+      da.k = l->k;
+      da.fc = f + 1;
+      da.ng = tb0 / 8;
+      da.dst = f == 0 ? l->hbuf : (void*)l->ybuf;
+      da.act = l->act;
+      da.zp_mode = l->zp_mode;
+      da.zp_offset = l->zp_offset;
+      da.bf16 = l->dtype == QMOE_BF16;
+      da.wait = wait;
+      da.pdl = 1;
+      QMOE_CUDA(l, launch_decode_mma(da, s), "launch decode projection");
+    }
+    trace(l, f == 0 ? QMOE_TRACE_FC1 : QMOE_TRACE_FC2, s);
+  }
+
+  FinalizeArgs fa{};
+  fa.y = l->ybuf;
+  fa.w = l->w;
+  fa.pos = l->pos;
+  fa.out = out;
+  fa.T = (int)T;
+  fa.H = l->H;
+  fa.k = l->k;
+  fa.dtype = l->dtype;
+  fa.pdl = 1;
+  QMOE_CUDA(l, launch_finalize(fa, s), "launch combine");
+  trace(l, QMOE_TRACE_END, s);
+  (void)R;
+  return QMOE_OK;
+}
+
+qmoe_status qmoe_forward_host(qmoe_layer* l, const void* x_host, const float* logits_host,
+                              void* out_host, int64_t T, void* stream) {
+  if (!l) return QMOE_ERR_INVALID_ARG;
+  if (T < 0) return fail(l, QMOE_ERR_INVALID_ARG, "num_tokens < 0");
+  if (T == 0) return QMOE_OK;
+  if (!x_host || !logits_host || !out_host) return fail(l, QMOE_ERR_INVALID_ARG, "null host buffer");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (T > l->cap_T) {
+    const qmoe_status st = ensure_workspace(l, T);
+    if (st != QMOE_OK) return st;
+  }
+  const size_t xb = (size_t)T * l->H * l->dsize;
+  QMOE_CUDA(l, cudaMemcpyAsync(l->x_stage, x_host, xb, cudaMemcpyHostToDevice, s), "copy x");
+  QMOE_CUDA(l, cudaMemcpyAsync(l->logits_stage, logits_host, (size_t)T * l->E * sizeof(float),
+                               cudaMemcpyHostToDevice, s),
+            "copy logits");
+  const qmoe_status st = qmoe_forward(l, l->x_stage, l->logits_stage, l->out_stage, T, stream);
+  if (st != QMOE_OK) return st;
+  QMOE_CUDA(l, cudaMemcpyAsync(out_host, l->out_stage, xb, cudaMemcpyDeviceToHost, s), "copy out");
+  QMOE_CUDA(l, cudaStreamSynchronize(s), "synchronise");
+  return QMOE_OK;
+}
+
+qmoe_status qmoe_get_routing(qmoe_layer* l, int32_t* ids, float* weights, int32_t* perm,
+                             int32_t* offsets, void* stream) {
+  if (!l) return QMOE_ERR_INVALID_ARG;
+  if (l->last_T == 0) return fail(l, QMOE_ERR_STATE, "no forward has run");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const size_t R = (size_t)l->last_T * l->k;
+  if (ids) QMOE_CUDA(l, cudaMemcpyAsync(ids, l->ids, R * 4, cudaMemcpyDeviceToDevice, s), "copy ids");
+  if (weights) QMOE_CUDA(l, cudaMemcpyAsync(weights, l->w, R * 4, cudaMemcpyDeviceToDevice, s), "copy w");
+  if (perm) QMOE_CUDA(l, cudaMemcpyAsync(perm, l->perm, R * 4, cudaMemcpyDeviceToDevice, s), "copy perm");
+  if (offsets)
+    QMOE_CUDA(l, cudaMemcpyAsync(offsets, l->offsets, (l->E + 1) * 4, cudaMemcpyDeviceToDevice, s),
+              "copy offsets");
+  return QMOE_OK;
+}
+
+int64_t qmoe_worklist_capacity(const qmoe_layer* l, int which, int64_t T) {
+  if (!l || (which != 0 && which != 1) || T < 0) return -1;
+  int tb0, tb1;
+  item_heights(l, T, &tb0, &tb1);
+  return items_cap(l, which, T, which == 0 ? tb0 : tb1);
+}
+
+qmoe_status qmoe_get_worklist(qmoe_layer* l, int which, int32_t* items, int32_t* count,
+                              int64_t capacity, int* m_tile_host, void* stream) {
+  if (!l || (which != 0 && which != 1)) return QMOE_ERR_INVALID_ARG;
+  if (l->last_T == 0) return fail(l, QMOE_ERR_STATE, "no forward has run");
+  const int64_t need = items_cap(l, which, l->last_T, l->last_tb[which]);
+  if (capacity < need) return fail(l, QMOE_ERR_INVALID_ARG, "work-list capacity too small");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (items)
+    QMOE_CUDA(l, cudaMemcpyAsync(items, l->items[which], need * sizeof(Item), cudaMemcpyDeviceToDevice, s),
+              "copy items");
+  if (count)
+    QMOE_CUDA(l, cudaMemcpyAsync(count, l->n_items + which, sizeof(int), cudaMemcpyDeviceToDevice, s),
+              "copy count");
+  if (m_tile_host) *m_tile_host = l->last_tb[which];
+  return QMOE_OK;
+}
+
+qmoe_status qmoe_set_trace_events(qmoe_layer* l, void* const* events, int n) {
+  if (!l) return QMOE_ERR_INVALID_ARG;
+  if (!events) {
+    l->trace_on = false;
+    return QMOE_OK;
+  }
+  if (n != QMOE_TRACE_NUM_EVENTS) return fail(l, QMOE_ERR_INVALID_ARG, "need QMOE_TRACE_NUM_EVENTS events");
+  for (int i = 0; i < n; ++i) l->trace[i] = static_cast<cudaEvent_t>(events[i]);
+  l->trace_on = true;
+  return QMOE_OK;
+}
+
+qmoe_status qmoe_poll_device_status(qmoe_layer* l) {
+  if (!l) return QMOE_ERR_INVALID_ARG;
+  if (!l->status) return QMOE_OK;
+  int h = 0;
+  QMOE_CUDA(l, cudaDeviceSynchronize(), "synchronise");
+  QMOE_CUDA(l, cudaMemcpy(&h, l->status, sizeof(int), cudaMemcpyDeviceToHost), "read status");
+  QMOE_CUDA(l, cudaMemset(l->status, 0, sizeof(int)), "clear status");
+  if (h == DEV_TIMEOUT) return fail(l, QMOE_ERR_TIMEOUT, "a bounded device-side wait ran out");
+  return QMOE_OK;
+}
+
+const char* qmoe_last_error(const qmoe_layer* l) {
+  if (!l) return "null layer";
+  return l->err.c_str();
+}
+
+const char* qmoe_status_string(qmoe_status st) {
+  if ((int)st < 0 || (int)st > 6) return "QMOE_ERR_UNKNOWN";
+  return kStatusNames[st];
+}
+
+void qmoe_destroy(qmoe_layer* l) {
+  if (!l) return;
+  if (l->device >= 0 || l->cap_T > 0) cudaDeviceSynchronize();
+  free_workspace(l);
+  for (Proj& p : l->proj) {
+    if (p.codes) cudaFree(p.codes);
+    if (p.scales) cudaFree(p.scales);
+    if (p.zp) cudaFree(p.zp);
+    if (p.dec) cudaFree(p.dec);
+  }
+  delete l;
+}
+
+}  // extern "C"

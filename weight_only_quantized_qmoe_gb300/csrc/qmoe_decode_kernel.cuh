@@ -1,0 +1,361 @@
+// The weight-streaming mma decode kernel (template), instantiated per code
+// width in qmoe_decode_b{2,3,4}.cu.  See qmoe_decode.cu for the design.
+#pragma once
+#include "qmoe_internal.cuh"
+
+namespace qmoe {
+
+// ----------------------------------------------------------------------------
+// The mma decode kernel
+// ----------------------------------------------------------------------------
+constexpr int kWarps = 8;
+
+struct DecodeSmem {
+  int bar_off, ring_off, stage_bytes, stages, g_chunks, bop_off, total;
+};
+
+__host__ __device__ inline DecodeSmem decode_smem(const DecodeLayout& L, int NG, int stages, int g_chunks,
+                                                  int ksplit) {
+  DecodeSmem m;
+  m.stages = stages;
+  m.g_chunks = g_chunks;
+  m.stage_bytes = g_chunks * L.scb;
+  m.bar_off = 0;
+  m.ring_off = 1024;
+  int ring = kWarps * stages * m.stage_bytes;
+  const int red = ksplit > 1 ? kWarps * 32 * (L.nsub * 4 * 4) * 4 : 0;
+  if (red > ring) ring = red;
+  m.bop_off = m.ring_off + ((ring + 127) / 128) * 128;
+  const int ktiles = L.nkc * L.SC / 16;
+  m.total = m.bop_off + ktiles * NG * 256;
+  return m;
+}
+
+template <bool BF16>
+struct Magic;
+template <>
+struct Magic<true> {
+  static constexpr uint32_t v = 0x43004300u;  // bf16 pair (128, 128), ulp 1
+};
+template <>
+struct Magic<false> {
+  static constexpr uint32_t v = 0x64006400u;  // f16 pair (1024, 1024), ulp 1
+};
+
+// Fragment pair r (0..3) of k-tile j of this lane's code words (pairs of
+// 16-bit fields, low element in bits 0.., high element in bits 16..).
+template <int BITS>
+__device__ __forceinline__ uint32_t code_pair(const uint32_t* cw, const uint32_t* hw, int j, int r) {
+  if (BITS == 4) {
+    return (cw[j] >> (4 * r)) & 0x000F000Fu;
+  } else if (BITS == 2) {
+    return (cw[j >> 1] >> (2 * ((j & 1) * 4 + r))) & 0x00030003u;
+  } else {
+    const uint32_t lo = (cw[j >> 1] >> (2 * ((j & 1) * 4 + r))) & 0x00030003u;
+    const uint32_t hi = (hw[j >> 2] >> ((j & 3) * 4 + r)) & 0x00010001u;
+    return lo | (hi << 2);
+  }
+}
+
+template <int BITS, int ZPM, bool BF16, bool GLU, int BLK>
+__global__ void __launch_bounds__(kWarps * 32, 1)
+    decode_mma_kernel(const DecodeArgs a, int tpc, int ksplit, int stages, int g_chunks) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  constexpr int NSUB = GLU ? 2 : 1;
+  constexpr int SC = BLK > 64 ? BLK : 64;  // super-chunk length along K
+  constexpr int KT = SC / 16;              // k-tiles per super-chunk
+  constexpr int NBK = SC / BLK;            // quantisation blocks per super-chunk
+  constexpr int KTB = BLK / 16;            // k-tiles per block
+  const DecodeLayout& L = a.L;
+  constexpr int NGM = 4;               // max token groups (accumulator size)
+  const int NG = a.ng;
+  const DecodeSmem sm = decode_smem(L, NG, stages, g_chunks, ksplit);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + sm.bar_off);
+  uint8_t* ring_base = smem + sm.ring_off;
+  uint32_t* bop = reinterpret_cast<uint32_t*>(smem + sm.bop_off);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = lane >> 2, t = lane & 3;
+
+  pdl_wait();
+  const int n_items = *a.n_items;
+  if ((int)blockIdx.y >= n_items) return;  // uniform across the CTA
+  const Item it = a.items[blockIdx.y];
+
+  const int tile = blockIdx.x * tpc + warp / ksplit;
+  const int ks = warp % ksplit;
+  const bool active = warp < tpc * ksplit && tile < L.ntiles;
+  const int kc0 = ks * L.nkc / ksplit, kc1 = (ks + 1) * L.nkc / ksplit;
+  const int nchunks = kc1 - kc0;
+  const int nst = active ? (nchunks + g_chunks - 1) / g_chunks : 0;
+  uint64_t* bar = bars + warp * stages;
+  uint8_t* ring = ring_base + (size_t)warp * stages * sm.stage_bytes;
+  const uint8_t* src = a.wpk + (size_t)it.e * L.expert_bytes + (size_t)(active ? tile : 0) * L.tile_bytes +
+                       (size_t)kc0 * L.scb;
+
+  auto issue = [&](int i) {
+    const int slot = i % stages;
+    const int nck = min(g_chunks, nchunks - i * g_chunks);
+    const uint32_t bytes = (uint32_t)(nck * L.scb);
+    mbar_arrive_expect_tx(&bar[slot], bytes);
+    bulk_g2s(ring + slot * sm.stage_bytes, src + (size_t)i * g_chunks * L.scb, bytes, &bar[slot]);
+  };
+  int issued = 0;
+  if (active && lane == 0) {
+    for (int s = 0; s < stages; ++s) mbar_init(&bar[s], 1);
+    fence_mbar_init();
+    for (; issued < min(stages, nst); ++issued) issue(issued);
+  }
+  issued = __shfl_sync(0xffffffffu, issued, 0);
+  __syncwarp();
+
+  // Stage the item's rows (B operand) in fragment order:
+  // bop[((kt * NG + ng) * 32 + g*4 + t) * 2 + hi] = (row ng*8+g, k = kt*16 + hi*8 + 2t, +1)
+  {
+    const int Kp2 = L.nkc * SC / 2;
+    const int K = a.K;
+    const uint16_t* src16 = static_cast<const uint16_t*>(a.src);
+    for (int idx = threadIdx.x; idx < NG * 8 * Kp2; idx += blockDim.x) {
+      const int n = idx / Kp2, q = idx % Kp2;
+      uint32_t v = 0;
+      if (n < it.rows && 2 * q < K) {
+        size_t row;
+        if (a.fc == 1) row = (size_t)(a.perm[it.start + n] / a.k);
+        else row = (size_t)(it.start + n);
+        v = *reinterpret_cast<const uint32_t*>(src16 + row * K + 2 * q);
+      }
+      const int kk = 2 * q, kt = kk >> 4, within = kk & 15;
+      const int tt = (within & 7) >> 1, hi = within >> 3;
+      bop[((kt * NG + (n >> 3)) * 32 + (n & 7) * 4 + tt) * 2 + hi] = v;
+    }
+  }
+  __syncthreads();
+
+  float acc[NSUB][NGM][4];
+#pragma unroll
+  for (int s = 0; s < NSUB; ++s)
+#pragma unroll
+    for (int n = 0; n < NGM; ++n)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) acc[s][n][i] = 0.f;
+
+  const int ng_act = (it.rows + 7) >> 3;
+  constexpr uint32_t MAGIC = Magic<BF16>::v;
+  uint32_t zoff2 = 0;
+  if (ZPM == QMOE_ZP_OFFSET) {
+    if (BF16) {
+      const __nv_bfloat16 z = __float2bfloat16_rn(a.zp_offset);
+      zoff2 = (uint32_t)__bfloat16_as_ushort(z) * 0x00010001u;
+    } else {
+      const __half z = __float2half_rn(a.zp_offset);
+      zoff2 = (uint32_t)__half_as_ushort(z) * 0x00010001u;
+    }
+  }
+  constexpr uint32_t ZSYM = MAGIC | ((1u << (BITS - 1)) * 0x00010001u);
+
+  bool ok = true;
+  int i = 0;
+  for (; i < nst; ++i) {
+    const int slot = i % stages;
+    if (!mbar_wait_bounded(&bar[slot], (uint32_t)((i / stages) & 1), a.wait)) {
+      ok = false;
+      break;
+    }
+    const uint8_t* st = ring + slot * sm.stage_bytes;
+    const int nck = min(g_chunks, nchunks - i * g_chunks);
+    for (int c = 0; c < nck; ++c) {
+      const uint8_t* ch = st + c * L.scb;
+      const int kc = kc0 + i * g_chunks + c;
+      // this lane's code words for each sub-tile
+      constexpr int WPL = BITS == 4 ? SC / 16 : SC / 32;   // (low-plane) words per lane
+      constexpr int WPH = BITS == 3 ? SC / 64 : 1;
+      uint32_t cw[NSUB][WPL];
+      uint32_t hw[NSUB][WPH];
+#pragma unroll
+      for (int s = 0; s < NSUB; ++s) {
+        const uint32_t* base = reinterpret_cast<const uint32_t*>(ch + s * L.code_bytes);
+#pragma unroll
+        for (int w = 0; w < WPL; ++w) cw[s][w] = base[lane * WPL + w];
+        if (BITS == 3) {
+#pragma unroll
+          for (int w = 0; w < WPH; ++w) hw[s][w] = base[32 * WPL + lane * WPH + w];
+        }
+      }
+#pragma unroll
+      for (int blk = 0; blk < NBK; ++blk) {
+        uint32_t ss[NSUB][2], zz[NSUB][2];
+#pragma unroll
+        for (int s = 0; s < NSUB; ++s) {
+          const uint32_t sp = *reinterpret_cast<const uint32_t*>(
+              ch + NSUB * L.code_bytes + s * L.scale_bytes + (blk * 8 + g) * 4);
+          ss[s][0] = __byte_perm(sp, 0, 0x1010);   // (s_g, s_g)
+          ss[s][1] = __byte_perm(sp, 0, 0x3232);   // (s_g8, s_g8)
+          if (ZPM == QMOE_ZP_UINT8) {
+            const uint32_t zb = ch[NSUB * (L.code_bytes + L.scale_bytes) + s * L.zp_bytes + blk * 8 + g];
+            zz[s][0] = MAGIC | ((zb & 15u) * 0x00010001u);
+            zz[s][1] = MAGIC | ((zb >> 4) * 0x00010001u);
+          } else {
+            zz[s][0] = zz[s][1] = ZSYM;
+          }
+        }
+#pragma unroll
+        for (int jj = 0; jj < KTB; ++jj) {
+          const int j = blk * KTB + jj;   // k-tile within the super-chunk
+          uint32_t afrag[NSUB][4];
+#pragma unroll
+          for (int s = 0; s < NSUB; ++s) {
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+              uint32_t v = code_pair<BITS>(cw[s], hw[s], j, r) | MAGIC;
+              if (ZPM == QMOE_ZP_OFFSET) {
+                v = sub2<BF16>(v, MAGIC);
+                v = sub2<BF16>(v, zoff2);
+              } else {
+                v = sub2<BF16>(v, zz[s][r & 1]);
+              }
+              afrag[s][r] = mul2<BF16>(v, ss[s][r & 1]);
+            }
+          }
+          const int ktg = kc * KT + j;
+#pragma unroll
+          for (int n = 0; n < NGM; ++n) {
+            if (n < ng_act) {
+              const uint2 b = *reinterpret_cast<const uint2*>(bop + ((ktg * NG + n) * 32 + lane) * 2);
+#pragma unroll
+              for (int s = 0; s < NSUB; ++s) mma16816<BF16>(acc[s][n], afrag[s], b.x, b.y);
+            }
+          }
+        }
+      }
+    }
+    __syncwarp();
+    if (lane == 0 && i + stages < nst) {
+      fence_proxy_async_smem();
+      issue(i + stages);
+    }
+    issued = min(nst, max(issued, i + stages + 1));
+  }
+  if (!ok) {
+    // Drain the copies still in flight into this warp's ring before the CTA
+    // can exit.  This uses the fixed default bound, not the (possibly tiny)
+    // configured one, so the copies have landed when the CTA leaves.
+    const WaitCfg drain{a.wait.status, kDrainWaitLimit};
+    for (int d = i; d < issued; ++d)
+      mbar_wait_bounded(&bar[d % stages], (uint32_t)((d / stages) & 1), drain);
+  }
+  pdl_launch_dependents();
+
+  // Split-K reduction over the ksplit warps of a tile (deterministic order).
+  if (ksplit > 1) {
+    __syncthreads();
+    float* red = reinterpret_cast<float*>(ring_base);
+    constexpr int NACC = NSUB * NGM * 4;
+    if (ks != 0) {
+      float* dst = red + (warp * 32 + lane) * NACC;
+#pragma unroll
+      for (int s = 0; s < NSUB; ++s)
+#pragma unroll
+        for (int n = 0; n < NGM; ++n)
+#pragma unroll
+          for (int q = 0; q < 4; ++q) dst[(s * NGM + n) * 4 + q] = acc[s][n][q];
+    }
+    __syncthreads();
+    if (ks == 0) {
+      for (int o = 1; o < ksplit; ++o) {
+        const float* srcr = red + ((warp + o) * 32 + lane) * NACC;
+#pragma unroll
+        for (int s = 0; s < NSUB; ++s)
+#pragma unroll
+          for (int n = 0; n < NGM; ++n)
+#pragma unroll
+            for (int q = 0; q < 4; ++q) acc[s][n][q] += srcr[(s * NGM + n) * 4 + q];
+      }
+    }
+  }
+  if (!active || ks != 0) return;
+
+  // Epilogue.  acc[s][n][q]: row g + 8*(q>>1), token n*8 + 2t + (q&1).
+#pragma unroll
+  for (int n = 0; n < NGM; ++n) {
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int tok = n * 8 + 2 * t + (q & 1);
+      const int row = tile * 16 + g + 8 * (q >> 1);
+      if (tok < it.rows) {
+        const size_t o = (size_t)(it.start + tok) * a.N_out + row;
+        if (GLU) {
+          const float h = glu(a.act, acc[0][n][q], acc[1][n][q]);
+          if (BF16) static_cast<__nv_bfloat16*>(a.dst)[o] = __float2bfloat16_rn(h);
+          else static_cast<__half*>(a.dst)[o] = __float2half_rn(h);
+        } else {
+          static_cast<float*>(a.dst)[o] = acc[0][n][q];
+        }
+      }
+    }
+  }
+}
+
+template <int BITS, int ZPM, bool BF16, bool GLU, int BLK>
+static cudaError_t launch_dm(const DecodeArgs& a, cudaStream_t s) {
+  const DecodeLayout& L = a.L;
+  // Split-K when the tiles alone would not fill the GPU.
+  const int sms = 152;
+  int ksplit = 1;
+  const long long est_items = a.max_items;
+  while (ksplit < 8 && est_items * ((L.ntiles + (kWarps / ksplit) - 1) / (kWarps / ksplit)) < 2LL * sms &&
+         L.nkc / (ksplit * 2) >= 2)
+    ksplit *= 2;
+  const int tpc = kWarps / ksplit;
+  // Stages of >= ~1 KB, ring of ~4 stages per warp within the smem budget.
+  int g_chunks = L.scb >= 1024 ? 1 : (1024 + L.scb - 1) / L.scb;
+  int stages = 4;
+  DecodeSmem sm = decode_smem(L, a.ng, stages, g_chunks, ksplit);
+  while (sm.total > 220 * 1024 && stages > 2) {
+    --stages;
+    sm = decode_smem(L, a.ng, stages, g_chunks, ksplit);
+  }
+  while (sm.total > 220 * 1024 && g_chunks > 1) {
+    --g_chunks;
+    sm = decode_smem(L, a.ng, stages, g_chunks, ksplit);
+  }
+  if (sm.total > 227 * 1024) return cudaErrorInvalidConfiguration;
+  auto kern = decode_mma_kernel<BITS, ZPM, BF16, GLU, BLK>;
+  cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, sm.total);
+  if (err != cudaSuccess) return err;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.gridDim = dim3((L.ntiles + tpc - 1) / tpc, a.max_items);
+  cfg.blockDim = dim3(kWarps * 32);
+  cfg.dynamicSmemBytes = sm.total;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = a.pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kern, a, tpc, ksplit, stages, g_chunks);
+}
+
+template <int BITS, int ZPM, bool BF16, bool GLU>
+static cudaError_t dispatch_blk(const DecodeArgs& a, cudaStream_t s) {
+  if (a.L.B == 32) return launch_dm<BITS, ZPM, BF16, GLU, 32>(a, s);
+  if (a.L.B == 64) return launch_dm<BITS, ZPM, BF16, GLU, 64>(a, s);
+  return launch_dm<BITS, ZPM, BF16, GLU, 128>(a, s);
+}
+template <int BITS, int ZPM, bool BF16>
+static cudaError_t dispatch_glu(const DecodeArgs& a, cudaStream_t s) {
+  if (a.fc == 1) return dispatch_blk<BITS, ZPM, BF16, true>(a, s);
+  return dispatch_blk<BITS, ZPM, BF16, false>(a, s);
+}
+template <int BITS, int ZPM>
+static cudaError_t dispatch_dt(const DecodeArgs& a, cudaStream_t s) {
+  if (a.bf16) return dispatch_glu<BITS, ZPM, true>(a, s);
+  return dispatch_glu<BITS, ZPM, false>(a, s);
+}
+template <int BITS>
+cudaError_t launch_decode_mma_bits(const DecodeArgs& a, cudaStream_t s) {
+  if (a.zp_mode == QMOE_ZP_UINT8) return dispatch_dt<BITS, QMOE_ZP_UINT8>(a, s);
+  if (a.zp_mode == QMOE_ZP_OFFSET) return dispatch_dt<BITS, QMOE_ZP_OFFSET>(a, s);
+  return dispatch_dt<BITS, QMOE_ZP_SYMMETRIC>(a, s);
+}
+
+}  // namespace qmoe

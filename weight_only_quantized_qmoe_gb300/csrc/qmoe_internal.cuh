@@ -1,0 +1,339 @@
+// Internal declarations shared by the QMoE CUDA translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_fp16.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "../../include/qmoe.h"
+
+namespace qmoe {
+
+// ----------------------------------------------------------------------------
+// Device status word (bounded waits report here instead of hanging/trapping)
+// ----------------------------------------------------------------------------
+enum : int { DEV_OK = 0, DEV_TIMEOUT = 1 };
+
+struct WaitCfg {
+  int* status;            // device int, 0 = ok
+  long long limit;        // iterations of a bounded wait before giving up
+};
+
+// Polls of the wait that drains a CTA's own in-flight copies after another
+// wait ran out (large: those copies always complete).
+constexpr long long kDrainWaitLimit = 1LL << 24;
+
+// ----------------------------------------------------------------------------
+// Work-list item: (expert, row_start in grouped order, rows, pad)
+// ----------------------------------------------------------------------------
+struct Item {
+  int e, start, rows, pad;
+};
+
+// ----------------------------------------------------------------------------
+// Decode (mma) prepacked layout of one projection.
+//
+// A "tile" is 16 output rows (fc2) or 16 gate rows + the matching 16 up rows
+// (fc1, so the GLU fuses).  Along K the tile is cut into super-chunks of SC
+// = max(64, B) values.  One super-chunk of one 16-row sub-tile holds
+//   codes : 32 lanes x (SC*bits/32/16) words in mma-fragment order
+//           (int3: a 2-bit plane then a 1-bit plane)
+//   scales: [SC/B blocks][8][2] of D: (s[row g], s[row g+8])
+//   zp    : [SC/B blocks][8] bytes: z[row g] | z[row g+8] << 4, padded to 16 B
+// A super-chunk of the tile is [sub0 codes][sub1 codes][sub0 scales]
+// [sub1 scales][sub0 zp][sub1 zp]; the tile is its super-chunks in K order;
+// the expert is its tiles in row order.  Every section is 16-byte aligned.
+// ----------------------------------------------------------------------------
+struct DecodeLayout {
+  int bits, B, SC, nkc, nsub, ntiles;
+  int code_bytes;    // per sub-tile per super-chunk
+  int scale_bytes;   // per sub-tile per super-chunk
+  int zp_bytes;      // per sub-tile per super-chunk (0 unless uint8 zp)
+  int scb;           // bytes of one super-chunk of a tile (all sub-tiles)
+  size_t tile_bytes; // nkc * scb
+  size_t expert_bytes;
+};
+
+DecodeLayout make_decode_layout(int bits, int B, int N_rows_per_sub, int K, int nsub,
+                                int zp_mode, int dsize);
+
+// ----------------------------------------------------------------------------
+// Launchers (host side, defined in the .cu files)
+// ----------------------------------------------------------------------------
+struct RouteArgs {
+  const float* logits;
+  int T, E, k, normalize;
+  int* ids;
+  float* w;
+  // grouping
+  int* counts;
+  int* offsets;
+  int* perm;
+  int* pos;
+  Item* items[2];
+  int* n_items;          // [2]
+  int tb[2];             // rows per item of each class
+  int threshold;         // experts with > threshold rows go to class 1
+  int cap[2];            // capacity of each item list
+};
+
+cudaError_t launch_route_group(const RouteArgs& a, bool fused, cudaStream_t s);
+
+struct RepackArgs {
+  const uint8_t* codes;     // canonical [E, N, K*bits/8]
+  const void* scales;       // canonical [E, N, K/B], D
+  const uint8_t* zp;        // canonical packed zp or null
+  uint8_t* out;             // decode layout
+  int E, N, K, I_or_0;      // I_or_0 = inter for fc1 (gate/up pairing), 0 for fc2
+  int dsize;
+  DecodeLayout L;
+};
+cudaError_t launch_repack_decode(const RepackArgs& a, cudaStream_t s);
+
+struct DecodeArgs {
+  const uint8_t* wpk;       // decode layout
+  DecodeLayout L;
+  int K;                    // real K (<= nkc*SC)
+  int N_out;                // output features of this fc (I for fc1, H for fc2)
+  const Item* items;
+  const int* n_items;
+  int max_items;
+  // B operand source: fc1 -> x rows by token (perm / k); fc2 -> rows of h
+  const void* src;
+  const int* perm;
+  int k;
+  int fc;                   // 1 or 2
+  int ng;                   // token groups of 8 per item (1, 2 or 4)
+  void* dst;                // fc1: h [R, I] D ; fc2: y [R, H] f32
+  int act;
+  int zp_mode;
+  float zp_offset;
+  int bf16;
+  WaitCfg wait;
+  int pdl;                  // launch with programmatic dependent launch
+};
+cudaError_t launch_decode_mma(const DecodeArgs& a, cudaStream_t s);
+
+struct SimtArgs {
+  const uint8_t* codes;     // canonical
+  const void* scales;
+  const uint8_t* zp;
+  int bits, B, K, N_out, I_or_0;
+  int zp_bytes_row;
+  const Item* items;
+  const int* n_items;
+  int max_items;
+  const void* src;
+  const int* perm;
+  int k, fc, dtype, act, zp_mode;
+  float zp_offset;
+  void* dst;                // fc1: h [R, I] f32 ; fc2: y [R, H] f32
+  int E;
+};
+cudaError_t launch_simt(const SimtArgs& a, cudaStream_t s);
+
+struct FinalizeArgs {
+  const float* y;           // [R, H] grouped order
+  const float* w;           // [T*k]
+  const int* pos;           // [T*k] grouped position of route r
+  void* out;                // [T, H] D
+  int T, H, k, dtype;
+  int pdl;
+};
+cudaError_t launch_finalize(const FinalizeArgs& a, cudaStream_t s);
+
+size_t group_smem_bytes(int E);
+
+}  // namespace qmoe
+
+// ----------------------------------------------------------------------------
+// Device helpers
+// ----------------------------------------------------------------------------
+#ifdef __CUDACC__
+namespace qmoe {
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
+               : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+               "r"(bytes)
+               : "memory");
+}
+
+// 1-D bulk copy global -> shared, completing on `bar` (complete_tx).  dst,
+// src and bytes must be multiples of 16.
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes,
+                                         uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded wait: returns false (and records DEV_TIMEOUT) if the phase did not
+// complete within `limit` polls.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity,
+                                                  const WaitCfg& w) {
+  for (long long i = 0; i < w.limit; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+  }
+  atomicExch(w.status, DEV_TIMEOUT);
+  return false;
+}
+
+__device__ __forceinline__ void pdl_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+__device__ __forceinline__ uint4 ld_nc_v4(const void* p) {
+  uint4 r;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "l"(p));
+  return r;
+}
+
+// Packed 16-bit pair arithmetic, round-to-nearest-even, no contraction.
+template <bool BF16>
+__device__ __forceinline__ uint32_t sub2(uint32_t a, uint32_t b);
+template <bool BF16>
+__device__ __forceinline__ uint32_t mul2(uint32_t a, uint32_t b);
+
+template <>
+__device__ __forceinline__ uint32_t sub2<true>(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+template <>
+__device__ __forceinline__ uint32_t sub2<false>(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+template <>
+__device__ __forceinline__ uint32_t mul2<true>(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+template <>
+__device__ __forceinline__ uint32_t mul2<false>(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
+// D = A(16x16, row) * B(16x8, col) + C, fp32 accumulate.
+template <bool BF16>
+__device__ __forceinline__ void mma16816(float* c, const uint32_t* a, uint32_t b0, uint32_t b1);
+
+template <>
+__device__ __forceinline__ void mma16816<true>(float* c, const uint32_t* a, uint32_t b0,
+                                               uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
+      "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+template <>
+__device__ __forceinline__ void mma16816<false>(float* c, const uint32_t* a, uint32_t b0,
+                                                uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
+      "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// Loads of one element of D as float.
+template <int DT>
+__device__ __forceinline__ float load_d(const void* p, size_t i);
+template <>
+__device__ __forceinline__ float load_d<QMOE_F32>(const void* p, size_t i) {
+  return static_cast<const float*>(p)[i];
+}
+template <>
+__device__ __forceinline__ float load_d<QMOE_F16>(const void* p, size_t i) {
+  return __half2float(static_cast<const __half*>(p)[i]);
+}
+template <>
+__device__ __forceinline__ float load_d<QMOE_BF16>(const void* p, size_t i) {
+  return __bfloat162float(static_cast<const __nv_bfloat16*>(p)[i]);
+}
+
+// Round-to-nearest-even into D, back to float.
+template <int DT>
+__device__ __forceinline__ float round_d(float v);
+template <>
+__device__ __forceinline__ float round_d<QMOE_F32>(float v) { return v; }
+template <>
+__device__ __forceinline__ float round_d<QMOE_F16>(float v) {
+  return __half2float(__float2half_rn(v));
+}
+template <>
+__device__ __forceinline__ float round_d<QMOE_BF16>(float v) {
+  return __bfloat162float(__float2bfloat16_rn(v));
+}
+
+template <int DT>
+__device__ __forceinline__ void store_d(void* p, size_t i, float v);
+template <>
+__device__ __forceinline__ void store_d<QMOE_F32>(void* p, size_t i, float v) {
+  static_cast<float*>(p)[i] = v;
+}
+template <>
+__device__ __forceinline__ void store_d<QMOE_F16>(void* p, size_t i, float v) {
+  static_cast<__half*>(p)[i] = __float2half_rn(v);
+}
+template <>
+__device__ __forceinline__ void store_d<QMOE_BF16>(void* p, size_t i, float v) {
+  static_cast<__nv_bfloat16*>(p)[i] = __float2bfloat16_rn(v);
+}
+
+// Gated activations in fp32 (CUDA's expf / tanhf).
+__device__ __forceinline__ float act_silu(float g) {
+  return g >= 0.f ? g / (1.f + expf(-g)) : g * expf(g) / (1.f + expf(g));
+}
+__device__ __forceinline__ float act_gelu_tanh(float g) {
+  return 0.5f * g * (1.f + tanhf(0.7978845608028654f * (g + 0.044715f * g * g * g)));
+}
+__device__ __forceinline__ float glu(int act, float g, float u) {
+  return (act == QMOE_ACT_SWIGLU ? act_silu(g) : act_gelu_tanh(g)) * u;
+}
+
+}  // namespace qmoe
+#endif

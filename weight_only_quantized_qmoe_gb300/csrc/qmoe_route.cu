@@ -1,0 +1,310 @@
+// Routing (top-k + softmax weights), expert grouping, tile work-lists and the
+// slot-ordered combine of the QMoE layer forward.
+//
+// Routing follows onnx-runtime-ep-cuda src/kernels/qmoe.rs (CUDA_SRC,
+// total_order_key / route_value_is_better / qmoe_route): experts are ranked
+// by a total-order key of the fp32 logit, ties to the lower index; the
+// weight of a selected expert is exp(l - max_all) divided by the sum over all
+// E experts, or over the k chosen when renormalising.  Here one warp ranks
+// one token (k warp-wide arg-max rounds) instead of one thread per token.
+//
+// Grouping replaces that page's count / 1-thread prefix / atomic-cursor
+// assignment with one CTA that builds a *stable* permutation (routes of an
+// expert in ascending route order), so the result is deterministic.  The
+// work-lists follow metrale gemm_quant_moe.rs moe_build_tile_worklist
+// (experts ascending, then m-tile); each item carries its row range.
+#include <climits>
+
+#include "qmoe_internal.cuh"
+
+namespace qmoe {
+
+__device__ __forceinline__ int total_order_key(float v) {
+  int b = __float_as_int(v);
+  return b ^ ((b >> 31) & 0x7fffffff);
+}
+
+// One warp ranks the E logits of one token and writes ids[0..k) and
+// w[0..k).  NPL = logits held per lane (E <= 32 * NPL).
+template <int NPL>
+__device__ void route_token(const float* __restrict__ lg, int E, int k, int normalize,
+                            int* __restrict__ ids, float* __restrict__ w) {
+  const int lane = threadIdx.x & 31;
+  int key[NPL];
+  uint32_t taken = 0;  // bit i: logit lane + 32 i is selected or absent
+  float mx = -INFINITY;
+#pragma unroll
+  for (int i = 0; i < NPL; ++i) {
+    const int e = lane + 32 * i;
+    if (e < E) {
+      const float v = lg[e];
+      key[i] = total_order_key(v);
+      mx = fmaxf(mx, v);
+    } else {
+      key[i] = INT_MIN;
+      taken |= 1u << i;
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  float sum_all = 0.f;
+#pragma unroll
+  for (int i = 0; i < NPL; ++i) {
+    const int e = lane + 32 * i;
+    if (e < E) sum_all += expf(lg[e] - mx);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) sum_all += __shfl_xor_sync(0xffffffffu, sum_all, o);
+
+  float sum_sel = 0.f;
+  for (int slot = 0; slot < k; ++slot) {
+    int bk = INT_MIN, bi = INT_MAX;
+#pragma unroll
+    for (int i = 0; i < NPL; ++i) {
+      const int e = lane + 32 * i;
+      if (!((taken >> i) & 1u) && (key[i] > bk || (key[i] == bk && e < bi))) {
+        bk = key[i];
+        bi = e;
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const int ok = __shfl_xor_sync(0xffffffffu, bk, o);
+      const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+      if (ok > bk || (ok == bk && oi < bi)) {
+        bk = ok;
+        bi = oi;
+      }
+    }
+    if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
+    if (lane == 0) ids[slot] = bi;
+    sum_sel += expf(lg[bi] - mx);
+  }
+  __syncwarp();
+  const float denom = normalize ? sum_sel : sum_all;
+  for (int slot = lane; slot < k; slot += 32) w[slot] = expf(lg[ids[slot]] - mx) / denom;
+}
+
+template <int NPL>
+__global__ void __launch_bounds__(256) route_kernel(const RouteArgs a) {
+  const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
+  if (t < a.T)
+    route_token<NPL>(a.logits + (size_t)t * a.E, a.E, a.k, a.normalize, a.ids + (size_t)t * a.k,
+                     a.w + (size_t)t * a.k);
+  pdl_launch_dependents();
+}
+
+// Exclusive scan of v over the 1024 threads of the block; returns the
+// exclusive prefix, *total gets the sum.  ws: 32 ints of shared memory.
+__device__ int block_exclusive_scan(int v, int* ws, int* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int incl = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int n = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += n;
+  }
+  if (lane == 31) ws[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    int s = ws[lane];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int n = __shfl_up_sync(0xffffffffu, s, o);
+      if (lane >= o) s += n;
+    }
+    ws[lane] = s;
+  }
+  __syncthreads();
+  const int excl = incl - v + (warp > 0 ? ws[warp - 1] : 0);
+  *total = ws[31];
+  __syncthreads();
+  return excl;
+}
+
+// One CTA of 1024 threads: optional routing of all tokens (small T), then
+// counts, offsets, the stable permutation, its inverse and both work-lists.
+// Shared memory: cnt[32][E] (per-warp, per-expert counts, later bases),
+// off[E], scan scratch.
+template <int NPL>
+__global__ void __launch_bounds__(1024) group_kernel(const RouteArgs a, int do_route) {
+  extern __shared__ int smem[];
+  const int E = a.E;
+  int* cnt = smem;             // [32][E]
+  int* off = smem + 32 * E;    // [E]
+  int* ws = off + E;           // [32]
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int R = a.T * a.k;
+
+  if (do_route) {
+    for (int t = warp; t < a.T; t += 32)
+      route_token<NPL>(a.logits + (size_t)t * E, E, a.k, a.normalize, a.ids + (size_t)t * a.k,
+                       a.w + (size_t)t * a.k);
+  } else {
+    pdl_wait();
+  }
+  for (int i = tid; i < 32 * E; i += blockDim.x) cnt[i] = 0;
+  __syncthreads();
+
+  // Pass 1: each warp counts its contiguous segment of routes per expert.
+  const int seg = (((R + 31) / 32) + 31) & ~31;
+  const int beg = warp * seg, end = min(R, beg + seg);
+  for (int base = beg; base < end; base += 32) {
+    const int r = base + lane;
+    const int e = r < end ? a.ids[r] : -1;
+    const unsigned peers = __match_any_sync(0xffffffffu, e);
+    if (e >= 0 && lane == __ffs(peers) - 1) cnt[warp * E + e] += __popc(peers);
+    __syncwarp();
+  }
+  __syncthreads();
+
+  // Column scan: cnt[w][e] <- routes of e in segments before w.
+  int count = 0;
+  if (tid < E) {
+    for (int w = 0; w < 32; ++w) {
+      const int c = cnt[w * E + tid];
+      cnt[w * E + tid] = count;
+      count += c;
+    }
+  }
+  int total;
+  const int excl = block_exclusive_scan(count, ws, &total);
+  if (tid < E) {
+    off[tid] = excl;
+    a.counts[tid] = count;
+    a.offsets[tid] = excl;
+  }
+  if (tid == 0) a.offsets[E] = total;
+  __syncthreads();
+  for (int i = tid; i < 32 * E; i += blockDim.x) cnt[i] += off[i % E];
+  __syncthreads();
+
+  // Pass 2: stable placement, walking each segment in route order.
+  const unsigned lt = (1u << lane) - 1u;
+  for (int base = beg; base < end; base += 32) {
+    const int r = base + lane;
+    const int e = r < end ? a.ids[r] : -1;
+    const unsigned peers = __match_any_sync(0xffffffffu, e);
+    if (e >= 0) {
+      const int p = cnt[warp * E + e] + __popc(peers & lt);
+      a.perm[p] = r;
+      a.pos[r] = p;
+    }
+    __syncwarp();
+    if (e >= 0 && lane == __ffs(peers) - 1) cnt[warp * E + e] += __popc(peers);
+    __syncwarp();
+  }
+
+  // Work-lists: class 0 (decode kernel) for experts with 1..threshold rows,
+  // class 1 (grouped GEMM) above; each cut into items of tb[cls] rows.
+  for (int cls = 0; cls < 2; ++cls) {
+    const int tb = a.tb[cls];
+    int nb = 0;
+    if (tid < E && count > 0 && ((count > a.threshold) == (cls == 1))) nb = (count + tb - 1) / tb;
+    int ntot;
+    const int ib = block_exclusive_scan(nb, ws, &ntot);
+    for (int i = 0; i < nb; ++i) {
+      if (ib + i < a.cap[cls]) {
+        Item it;
+        it.e = tid;
+        it.start = excl + i * tb;
+        it.rows = min(tb, count - i * tb);
+        it.pad = 0;
+        a.items[cls][ib + i] = it;
+      }
+    }
+    if (tid == 0) a.n_items[cls] = min(ntot, a.cap[cls]);
+  }
+  pdl_launch_dependents();
+}
+
+size_t group_smem_bytes(int E) { return (size_t)(33 * E + 32) * sizeof(int); }
+
+template <int NPL>
+static cudaError_t launch_rg(const RouteArgs& a, bool fused, cudaStream_t s) {
+  const size_t smem = group_smem_bytes(a.E);
+  cudaError_t err =
+      cudaFuncSetAttribute(group_kernel<NPL>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (err != cudaSuccess) return err;
+  if (fused) {
+    group_kernel<NPL><<<1, 1024, smem, s>>>(a, 1);
+    return cudaGetLastError();
+  }
+  route_kernel<NPL><<<(a.T + 7) / 8, 256, 0, s>>>(a);
+  err = cudaGetLastError();
+  if (err != cudaSuccess) return err;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.gridDim = dim3(1);
+  cfg.blockDim = dim3(1024);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, group_kernel<NPL>, a, 0);
+}
+
+cudaError_t launch_route_group(const RouteArgs& a, bool fused, cudaStream_t s) {
+  if (a.E <= 32) return launch_rg<1>(a, fused, s);
+  if (a.E <= 64) return launch_rg<2>(a, fused, s);
+  if (a.E <= 128) return launch_rg<4>(a, fused, s);
+  if (a.E <= 256) return launch_rg<8>(a, fused, s);
+  if (a.E <= 512) return launch_rg<16>(a, fused, s);
+  return launch_rg<32>(a, fused, s);
+}
+
+// ----------------------------------------------------------------------------
+// Combine: out[t, m] = R_D( sum_j w[t*k+j] * y[pos[t*k+j], m] ), j ascending
+// (qmoe.rs qmoe_combine_impl; fp32 accumulate, round to nearest even).
+// ----------------------------------------------------------------------------
+template <int DT>
+__global__ void __launch_bounds__(256) finalize_kernel(const FinalizeArgs a) {
+  pdl_wait();
+  const int H4 = a.H / 4;
+  const size_t n = (size_t)a.T * H4;
+  const float4* y4 = reinterpret_cast<const float4*>(a.y);
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n;
+       i += (size_t)gridDim.x * blockDim.x) {
+    const int t = (int)(i / H4), m4 = (int)(i % H4);
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int j = 0; j < a.k; ++j) {
+      const int r = t * a.k + j;
+      const float wr = a.w[r];
+      const float4 v = y4[(size_t)a.pos[r] * H4 + m4];
+      acc.x = fmaf(wr, v.x, acc.x);
+      acc.y = fmaf(wr, v.y, acc.y);
+      acc.z = fmaf(wr, v.z, acc.z);
+      acc.w = fmaf(wr, v.w, acc.w);
+    }
+    const size_t o = (size_t)t * a.H + (size_t)m4 * 4;
+    store_d<DT>(a.out, o + 0, acc.x);
+    store_d<DT>(a.out, o + 1, acc.y);
+    store_d<DT>(a.out, o + 2, acc.z);
+    store_d<DT>(a.out, o + 3, acc.w);
+  }
+}
+
+cudaError_t launch_finalize(const FinalizeArgs& a, cudaStream_t s) {
+  const size_t n = (size_t)a.T * (a.H / 4);
+  int grid = (int)((n + 255) / 256);
+  if (grid > 152 * 8) grid = 152 * 8;
+  if (grid < 1) grid = 1;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(256);
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = a.pdl ? 1 : 0;
+  switch (a.dtype) {
+    case QMOE_F32: return cudaLaunchKernelEx(&cfg, finalize_kernel<QMOE_F32>, a);
+    case QMOE_F16: return cudaLaunchKernelEx(&cfg, finalize_kernel<QMOE_F16>, a);
+    default: return cudaLaunchKernelEx(&cfg, finalize_kernel<QMOE_BF16>, a);
+  }
+}
+
+}  // namespace qmoe
