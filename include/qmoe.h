@@ -206,9 +206,16 @@ qmoe_status qmoe_set_trace_events(qmoe_layer* layer, void* const* events, int n)
  * a bounded wait inside a kernel ran out.  Synchronises the device. */
 qmoe_status qmoe_poll_device_status(qmoe_layer* layer);
 
-/* Test hook: the iteration limit of bounded device-side waits (0 = the
- * default).  A tiny limit makes waits run out, to exercise the error path. */
+/* The iteration limit of bounded device-side waits (0 = the default, about
+ * 2^24 polls).  Tests lower it so an injected stall ends quickly. */
 qmoe_status qmoe_set_wait_limit(qmoe_layer* layer, int64_t iterations);
+
+/* Test hook for failure detection without a GPU fault: while enabled, every
+ * warp of the decode projection kernels arms its first copy-stage barrier but
+ * never issues that copy, so its bounded wait runs out; the kernel records
+ * QMOE_ERR_TIMEOUT (see qmoe_poll_device_status), waits for its other copies
+ * and returns.  Results of such forwards are meaningless.  0 disables. */
+qmoe_status qmoe_debug_inject_stall(qmoe_layer* layer, int enable);
 
 /* Message of the last failed call on `layer` ("" if none); static strings
  * for NULL layers. */

@@ -35,7 +35,7 @@ def run_layer(qm, inp, reserve=None, min_rows=None):
     return layer, out
 
 
-def check_routing(layer, inp):
+def check_routing(layer, inp, min_rows=32):
     cfg = inp["cfg"]
     ids, w, perm, offs = layer.routing(cfg.T)
     torch.cuda.synchronize()
@@ -45,11 +45,18 @@ def check_routing(layer, inp):
     np.testing.assert_array_equal(offs.cpu().numpy(), rt["offsets"])
     np.testing.assert_allclose(w.cpu().numpy().reshape(cfg.T, cfg.k), rt["weights"],
                                rtol=2e-6, atol=1e-7)
-    # work-list of the decode kernel: the oracle's order at the same item height
-    items, m_tile = layer.worklist(0, cfg.T)
-    ref = O.build_worklist(rt["offsets"], m_tile)
-    got = [tuple(int(v) for v in row[:3]) for row in items.numpy()]
-    assert got == [(e, s, r) for e, s, r, _ in ref]
+    # Work-lists: experts with more than `min_rows` rows go to the grouped GEMM
+    # (class 1) once T can exceed it; the rest to the decode kernel (class 0).
+    thr = min_rows if (cfg.dtype != "f32" and cfg.T > min_rows) else None
+    for which in (0, 1):
+        items, m_tile = layer.worklist(which, cfg.T)
+        if thr is None:
+            flt = (lambda e, c: which == 0)
+        else:
+            flt = (lambda e, c, w_=which: (c > thr) == (w_ == 1))
+        ref = O.build_worklist(rt["offsets"], m_tile, expert_filter=flt)
+        got = [tuple(int(v) for v in row[:3]) for row in items.numpy()]
+        assert got == [(e, s, r) for e, s, r, _ in ref], f"work-list {which}"
     return rt
 
 
@@ -209,16 +216,20 @@ def test_forward_host_matches_device(qm):
 
 
 def test_bounded_wait_reports_timeout_and_context_survives(qm):
-    # A wait limit of one poll makes the first stage wait run out; the kernel
-    # records QMOE_ERR_TIMEOUT, drains its own copies and returns.
+    # Host-injected failure: the first copy stage of every decode warp is armed
+    # but never issued, so its bounded wait runs out.  The kernel records
+    # QMOE_ERR_TIMEOUT, drains its real copies and returns; the context stays
+    # usable and the next forward is correct.
     cfg = BASE.with_(T=4)
     inp = make_inputs(cfg)
     layer = qm.QMoELayer.from_config(cfg)
     x, logits = qm.load_inputs(layer, inp)
-    layer.set_wait_limit(1)
+    layer.set_wait_limit(2000)
+    layer.inject_stall(True)
     layer.forward(x, logits)
     torch.cuda.synchronize()
     assert layer.poll() == qm.QMOE_ERR_TIMEOUT
+    layer.inject_stall(False)
     layer.set_wait_limit(0)                          # back to the default
     out = layer.forward(x, logits)
     torch.cuda.synchronize()

@@ -114,6 +114,10 @@ class QMoELayer:
         return items[: int(cnt.item())].cpu(), m_tile
 
     def set_trace_events(self, events):
+        # torch only reports elapsed times of events it has seen recorded;
+        # record each once here, the library re-records them every forward.
+        for e in events or []:
+            e.record()
         self._check(binding.qmoe_set_trace_events(
             self.handle, None if events is None else [e.cuda_event for e in events]))
 
@@ -122,6 +126,9 @@ class QMoELayer:
 
     def set_wait_limit(self, n):
         self._check(binding.qmoe_set_wait_limit(self.handle, n))
+
+    def inject_stall(self, enable):
+        self._check(binding.qmoe_debug_inject_stall(self.handle, enable))
 
     def close(self):
         if getattr(self, "handle", None):

@@ -42,6 +42,7 @@ _SIGS = {
     "qmoe_set_trace_events": (_i, [_p, ctypes.POINTER(_p), _i]),
     "qmoe_poll_device_status": (_i, [_p]),
     "qmoe_set_wait_limit": (_i, [_p, _i64]),
+    "qmoe_debug_inject_stall": (_i, [_p, _i]),
     "qmoe_last_error": (ctypes.c_char_p, [_p]),
     "qmoe_status_string": (ctypes.c_char_p, [_i]),
     "qmoe_destroy": (None, [_p]),
@@ -144,6 +145,10 @@ def qmoe_poll_device_status(layer):
 
 def qmoe_set_wait_limit(layer, iterations):
     return load().qmoe_set_wait_limit(layer, int(iterations))
+
+
+def qmoe_debug_inject_stall(layer, enable):
+    return load().qmoe_debug_inject_stall(layer, int(enable))
 
 
 def qmoe_last_error(layer):

@@ -16,6 +16,7 @@
 #include <string>
 
 #include "qmoe_internal.cuh"
+#include "qmoe_prefill.cuh"
 
 using namespace qmoe;
 
@@ -26,9 +27,11 @@ struct Proj {
   void* scales = nullptr;
   uint8_t* zp = nullptr;
   uint8_t* dec = nullptr;
-  size_t codes_bytes = 0, scales_bytes = 0, zp_bytes = 0, dec_bytes = 0;
+  uint8_t* gq = nullptr;
+  size_t codes_bytes = 0, scales_bytes = 0, zp_bytes = 0, dec_bytes = 0, gq_bytes = 0;
   int N = 0, K = 0, bits = 0, zp_row = 0;
   DecodeLayout L{};
+  GemmLayout GL{};
   bool ready = false;
 };
 
@@ -49,6 +52,7 @@ struct qmoe_layer {
   int gemm_min_rows = 32;
   int device = -1;
   long long wait_limit = kDefaultWaitLimit;
+  int inject_stall = 0;
   Proj proj[2];
 
   // workspace for up to cap_T tokens
@@ -68,6 +72,11 @@ struct qmoe_layer {
   void* x_stage = nullptr;
   float* logits_stage = nullptr;
   void* out_stage = nullptr;
+  void* xg = nullptr;          // x gathered in route order (grouped GEMM B operand)
+  float* out_acc = nullptr;    // fp32 [T, H] combine accumulator (mixed forwards)
+  CUtensorMap map_x{}, map_h{};
+  bool maps_ok = false;
+  int num_sms = 0;
 
   int64_t last_T = 0;
   int last_tb[2] = {0, 0};
@@ -119,7 +128,7 @@ cudaError_t dalloc(T** p, size_t bytes) {
 void free_workspace(qmoe_layer* l) {
   void* bufs[] = {l->ids, l->w, l->counts, l->offsets, l->perm, l->pos, l->n_items, l->items[0],
                   l->items[1], l->hbuf, l->ybuf, l->status, l->x_stage, l->logits_stage,
-                  l->out_stage};
+                  l->out_stage, l->xg, l->out_acc};
   for (void* b : bufs)
     if (b) cudaFree(b);
   l->ids = nullptr;
@@ -132,6 +141,9 @@ void free_workspace(qmoe_layer* l) {
   l->x_stage = nullptr;
   l->logits_stage = nullptr;
   l->out_stage = nullptr;
+  l->xg = nullptr;
+  l->out_acc = nullptr;
+  l->maps_ok = false;
   l->cap_T = 0;
 }
 
@@ -151,7 +163,7 @@ void item_heights(const qmoe_layer* l, int64_t T, int* tb0, int* tb1) {
     while (ng > 1 && ng * ktiles * 256 > 160 * 1024) ng /= 2;
     *tb0 = 8 * ng;
   }
-  *tb1 = 128;
+  *tb1 = 256;
 }
 
 int64_t items_cap(const qmoe_layer* l, int which, int64_t T, int tb) {
@@ -185,6 +197,19 @@ qmoe_status ensure_workspace(qmoe_layer* l, int64_t T) {
   QMOE_CUDA(l, dalloc(&l->x_stage, (size_t)T * l->H * ds), "allocate workspace");
   QMOE_CUDA(l, dalloc(&l->logits_stage, (size_t)T * l->E * sizeof(float)), "allocate workspace");
   QMOE_CUDA(l, dalloc(&l->out_stage, (size_t)T * l->H * ds), "allocate workspace");
+  if (l->dtype != QMOE_F32) {
+    QMOE_CUDA(l, dalloc(&l->xg, (size_t)R * l->H * ds), "allocate workspace");
+    QMOE_CUDA(l, dalloc(&l->out_acc, (size_t)T * l->H * sizeof(float)), "allocate workspace");
+    QMOE_CUDA(l, cudaMemset(l->out_acc, 0, (size_t)T * l->H * sizeof(float)), "clear accumulator");
+    const bool bf16 = l->dtype == QMOE_BF16;
+    l->maps_ok = make_token_map(&l->map_x, l->xg, (int)R, l->H, bf16) == cudaSuccess &&
+                 make_token_map(&l->map_h, l->hbuf, (int)R, l->I, bf16) == cudaSuccess;
+  }
+  if (l->num_sms == 0) {
+    int dev = 0;
+    QMOE_CUDA(l, cudaGetDevice(&dev), "cudaGetDevice");
+    QMOE_CUDA(l, cudaDeviceGetAttribute(&l->num_sms, cudaDevAttrMultiProcessorCount, dev), "query SMs");
+  }
   l->cap_T = T;
   return QMOE_OK;
 }
@@ -270,6 +295,12 @@ qmoe_status qmoe_set_wait_limit(qmoe_layer* l, int64_t iterations) {
   return QMOE_OK;
 }
 
+qmoe_status qmoe_debug_inject_stall(qmoe_layer* l, int enable) {
+  if (!l) return QMOE_ERR_INVALID_ARG;
+  l->inject_stall = enable ? 1 : 0;
+  return QMOE_OK;
+}
+
 qmoe_status qmoe_reserve(qmoe_layer* l, int64_t max_tokens) {
   if (!l || max_tokens < 0) return QMOE_ERR_INVALID_ARG;
   if ((max_tokens * l->k) > INT_MAX / 8) return fail(l, QMOE_ERR_INVALID_ARG, "max_tokens too large");
@@ -342,6 +373,25 @@ qmoe_status qmoe_prepack(qmoe_layer* l, int fc, const uint8_t* codes, const void
     ra.dsize = l->dsize;
     ra.L = p.L;
     QMOE_CUDA(l, launch_repack_decode(ra, s), "repack weights");
+    p.GL = make_gemm_layout(p.bits, l->B, fc, p.N, p.K, l->I, l->zp_mode);
+    const size_t gq_bytes = p.GL.expert_bytes * E;
+    if (p.gq_bytes != gq_bytes) {
+      if (p.gq) cudaFree(p.gq);
+      QMOE_CUDA(l, dalloc(&p.gq, gq_bytes), "allocate GEMM layout");
+      p.gq_bytes = gq_bytes;
+    }
+    GemmRepackArgs ga{};
+    ga.codes = p.codes;
+    ga.scales = p.scales;
+    ga.zp = p.zp;
+    ga.out = p.gq;
+    ga.E = l->E;
+    ga.N = p.N;
+    ga.K = p.K;
+    ga.I = l->I;
+    ga.fc = fc;
+    ga.L = p.GL;
+    QMOE_CUDA(l, launch_repack_gemm(ga, s), "repack weights (GEMM layout)");
   }
   p.ready = true;
   return QMOE_OK;
@@ -370,6 +420,10 @@ qmoe_status qmoe_forward(qmoe_layer* l, const void* x, const float* logits, void
   l->last_tb[1] = tb1;
   const int R = (int)(T * l->k);
   const WaitCfg wait{l->status, l->wait_limit};
+  // An expert can receive at most T rows: only when T exceeds the threshold
+  // can the grouped-GEMM class be non-empty.
+  const bool gemm = l->dtype != QMOE_F32 && l->maps_ok && T > l->gemm_min_rows;
+  const int threshold = gemm ? l->gemm_min_rows : INT_MAX;
 
   trace(l, QMOE_TRACE_BEGIN, s);
   RouteArgs ra{};
@@ -389,10 +443,16 @@ qmoe_status qmoe_forward(qmoe_layer* l, const void* x, const float* logits, void
   ra.n_items = l->n_items;
   ra.tb[0] = tb0;
   ra.tb[1] = tb1;
-  ra.threshold = INT_MAX;  // every expert takes the decode/SIMT kernel
+  ra.threshold = threshold;
   ra.cap[0] = (int)items_cap(l, 0, T, tb0);
   ra.cap[1] = (int)items_cap(l, 1, T, tb1);
+  if (gemm) {
+    // class-0 experts have at most `threshold` rows each
+    const int64_t per = ((int64_t)threshold + tb0 - 1) / tb0;
+    if ((int64_t)l->E * per < ra.cap[0]) ra.cap[0] = (int)((int64_t)l->E * per);
+  }
   QMOE_CUDA(l, launch_route_group(ra, T <= 64, s), "launch routing");
+  if (gemm) QMOE_CUDA(l, launch_gather(x, l->perm, l->k, R, l->H, l->xg, s), "launch gather");
   trace(l, QMOE_TRACE_ROUTED, s);
 
   for (int f = 0; f < 2; ++f) {
@@ -443,24 +503,54 @@ qmoe_status qmoe_forward(qmoe_layer* l, const void* x, const float* logits, void
       da.bf16 = l->dtype == QMOE_BF16;
       da.wait = wait;
       da.pdl = 1;
+      da.inject_stall = l->inject_stall;
+      da.atomic = gemm && f == 1;
+      da.out_acc = l->out_acc;
+      da.w = l->w;
       QMOE_CUDA(l, launch_decode_mma(da, s), "launch decode projection");
+      if (gemm) {
+        GemmArgs ga{};
+        ga.wq = p.gq;
+        ga.L = p.GL;
+        ga.items = l->items[1];
+        ga.n_items = l->n_items + 1;
+        ga.max_items = ra.cap[1];
+        const int64_t max_tiles = (int64_t)ra.cap[1] * p.GL.ntiles;
+        ga.grid = (int)(max_tiles < l->num_sms ? max_tiles : l->num_sms);
+        ga.fc = f + 1;
+        ga.act = l->act;
+        ga.zp_mode = l->zp_mode;
+        ga.bf16 = l->dtype == QMOE_BF16;
+        ga.zp_offset = l->zp_offset;
+        ga.hout = l->hbuf;
+        ga.out_acc = l->out_acc;
+        ga.perm = l->perm;
+        ga.w = l->w;
+        ga.k = l->k;
+        ga.N_out = f == 0 ? l->I : l->H;
+        ga.wait = wait;
+        QMOE_CUDA(l, launch_gemm(f == 0 ? l->map_x : l->map_h, ga, s), "launch grouped GEMM");
+      }
     }
     trace(l, f == 0 ? QMOE_TRACE_FC1 : QMOE_TRACE_FC2, s);
   }
 
-  FinalizeArgs fa{};
-  fa.y = l->ybuf;
-  fa.w = l->w;
-  fa.pos = l->pos;
-  fa.out = out;
-  fa.T = (int)T;
-  fa.H = l->H;
-  fa.k = l->k;
-  fa.dtype = l->dtype;
-  fa.pdl = 1;
-  QMOE_CUDA(l, launch_finalize(fa, s), "launch combine");
+  if (gemm) {
+    QMOE_CUDA(l, launch_finalize_acc(l->out_acc, out, (size_t)T * l->H, l->dtype, s), "launch combine");
+  } else {
+    FinalizeArgs fa{};
+    fa.y = l->ybuf;
+    fa.w = l->w;
+    fa.pos = l->pos;
+    fa.out = out;
+    fa.T = (int)T;
+    fa.H = l->H;
+    fa.k = l->k;
+    fa.dtype = l->dtype;
+    fa.pdl = 1;
+    QMOE_CUDA(l, launch_finalize(fa, s), "launch combine");
+  }
   trace(l, QMOE_TRACE_END, s);
-  (void)R;
   return QMOE_OK;
 }
 
@@ -568,6 +658,7 @@ void qmoe_destroy(qmoe_layer* l) {
     if (p.scales) cudaFree(p.scales);
     if (p.zp) cudaFree(p.zp);
     if (p.dec) cudaFree(p.dec);
+    if (p.gq) cudaFree(p.gq);
   }
   delete l;
 }

@@ -98,6 +98,9 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
     const int nck = min(g_chunks, nchunks - i * g_chunks);
     const uint32_t bytes = (uint32_t)(nck * L.scb);
     mbar_arrive_expect_tx(&bar[slot], bytes);
+    // Test hook: the barrier of stage 0 is armed but its copy never issued,
+    // so the wait on it can only run out (host-injected failure).
+    if (a.inject_stall && i == 0) return;
     bulk_g2s(ring + slot * sm.stage_bytes, src + (size_t)i * g_chunks * L.scb, bytes, &bar[slot]);
   };
   int issued = 0;
@@ -240,8 +243,10 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
     // can exit.  This uses the fixed default bound, not the (possibly tiny)
     // configured one, so the copies have landed when the CTA leaves.
     const WaitCfg drain{a.wait.status, kDrainWaitLimit};
-    for (int d = i; d < issued; ++d)
+    for (int d = i; d < issued; ++d) {
+      if (a.inject_stall && d == 0) continue;   // no copy was issued for it
       mbar_wait_bounded(&bar[d % stages], (uint32_t)((d / stages) & 1), drain);
+    }
   }
   pdl_launch_dependents();
 
@@ -287,6 +292,9 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
           const float h = glu(a.act, acc[0][n][q], acc[1][n][q]);
           if (BF16) static_cast<__nv_bfloat16*>(a.dst)[o] = __float2bfloat16_rn(h);
           else static_cast<__half*>(a.dst)[o] = __float2half_rn(h);
+        } else if (a.atomic) {
+          const int route = a.perm[it.start + tok];
+          atomicAdd(a.out_acc + (size_t)(route / a.k) * a.N_out + row, a.w[route] * acc[0][n][q]);
         } else {
           static_cast<float*>(a.dst)[o] = acc[0][n][q];
         }

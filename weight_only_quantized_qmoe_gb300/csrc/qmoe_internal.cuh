@@ -112,6 +112,13 @@ struct DecodeArgs {
   int bf16;
   WaitCfg wait;
   int pdl;                  // launch with programmatic dependent launch
+  int inject_stall;         // test hook: arm stage 0's barrier, never issue its copy
+  // fc2 only: when set, add w[route] * y into out_acc[token, m] (fp32
+  // reductions) instead of writing y rows; used when the grouped GEMM also
+  // contributes to the same forward.
+  int atomic;
+  float* out_acc;
+  const float* w;
 };
 cudaError_t launch_decode_mma(const DecodeArgs& a, cudaStream_t s);
 

@@ -1,0 +1,669 @@
+// Tensor-core grouped GEMM for experts with many routed rows (prefill):
+// fc1 (+ fused gated activation) and fc2 (+ weighted scatter into the fp32
+// combine accumulator) of the QMoE layer forward.
+//
+// What is computed is the same as the decode path (onnx-runtime-ep-cuda
+// src/kernels/qmoe.rs decode_affine_weight; PR "[CUDA] QMoE: fused int2
+// mixed-input GEMM ..." zero_point_offset; PR "[CUDA] Add fast INT3 QMoE
+// kernels" review "Round dequantized weights before accumulation"), written as
+// a dense contraction per (expert, token tile, weight-row tile).
+//
+// GB300 design (ours; the pages' SM80 DqMma prior art does not apply):
+//   D[128 weight rows, N tokens] += A[128 rows, 64 k] * B[N tokens, 64 k]^T
+//   * A = dequantised weights, written by 4 CUDA-core warps straight into
+//     tensor memory (tcgen05.st, one thread per weight row, 64 k per step):
+//     the dequant costs no shared-memory bandwidth, which the B stream needs;
+//   * B = the routed token rows (x gathered in route order for fc1, h for
+//     fc2), TMA tiles of 256 x 64 (128-byte swizzle) in a shared ring;
+//   * tcgen05.mma.cta_group::1.kind::f16, fp32 accumulators in TMEM
+//     (256 columns), N = the tile's rows rounded up to 16 (no padded work);
+//   * warp roles: 0 = TMA / bulk-copy producer, 1 = MMA issuer (one thread)
+//     and TMEM owner, 4..7 = dequant, 8..11 = epilogue (tcgen05.ld);
+//   * persistent CTAs stride over the (item, weight-tile) list; fc1 rows are
+//     interleaved gate/up so the GLU pairs sit in adjacent TMEM lanes;
+//   * every wait is bounded; a timeout aborts all roles, drains in-flight
+//     copies and MMAs, frees TMEM and records QMOE_ERR_TIMEOUT.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include "qmoe_prefill.cuh"
+
+namespace qmoe {
+
+// ----------------------------------------------------------------------------
+// Prepack: canonical -> GEMM layout (see GemmLayout).  One thread per
+// (expert, tile, k-step, tile row).
+// ----------------------------------------------------------------------------
+__device__ __forceinline__ int canon_field(const uint8_t* row, int row_bytes, int bits, int d, int K) {
+  if (d >= K) return 0;
+  const int bo = d * bits;
+  const int byte = bo >> 3, sh = bo & 7;
+  uint32_t v = row[byte];
+  if (byte + 1 < row_bytes) v |= (uint32_t)row[byte + 1] << 8;
+  return (int)((v >> sh) & ((1u << bits) - 1u));
+}
+
+__global__ void repack_gemm_kernel(const GemmRepackArgs a) {
+  const GemmLayout& L = a.L;
+  const size_t total = (size_t)a.E * L.ntiles * L.ksteps * 128;
+  const size_t idx = blockIdx.x * (size_t)blockDim.x + threadIdx.x;
+  if (idx >= total) return;
+  const int r = (int)(idx % 128);
+  const int ks = (int)((idx / 128) % L.ksteps);
+  const int nt = (int)((idx / (128 * (size_t)L.ksteps)) % L.ntiles);
+  const int e = (int)(idx / (128 * (size_t)L.ksteps * L.ntiles));
+  int row;
+  bool valid;
+  if (a.fc == 1) {
+    const int n = nt * 64 + r / 2;
+    valid = n < a.I;
+    row = (r & 1) ? a.I + n : n;
+  } else {
+    row = nt * 128 + r;
+    valid = row < a.N;
+  }
+  const int bits = L.bits;
+  const int row_bytes = a.K * bits / 8;
+  const int nblk = a.K / L.B;
+  const int zrow = (nblk * bits + 7) / 8;
+  const uint8_t* crow = valid ? a.codes + ((size_t)e * a.N + row) * row_bytes : nullptr;
+  auto code = [&](int d) { return valid ? canon_field(crow, row_bytes, bits, d, a.K) : 0; };
+  uint8_t* stage = a.out + ((((size_t)e * L.ntiles + nt) * L.ksteps) + ks) * L.stage_bytes;
+  uint32_t* cw = reinterpret_cast<uint32_t*>(stage + (size_t)r * L.code_row);
+  const int k0 = ks * 64;
+  if (bits == 4) {
+    for (int i = 0; i < 8; ++i) {
+      uint32_t w = 0;
+      for (int m = 0; m < 4; ++m) {
+        w |= (uint32_t)code(k0 + 8 * i + 2 * m) << (4 * m);
+        w |= (uint32_t)code(k0 + 8 * i + 2 * m + 1) << (16 + 4 * m);
+      }
+      cw[i] = w;
+    }
+  } else {
+    for (int i = 0; i < 4; ++i) {
+      uint32_t w = 0;
+      for (int m = 0; m < 8; ++m) {
+        w |= (uint32_t)(code(k0 + 16 * i + 2 * m) & 3) << (2 * m);
+        w |= (uint32_t)(code(k0 + 16 * i + 2 * m + 1) & 3) << (16 + 2 * m);
+      }
+      cw[i] = w;
+    }
+    if (bits == 3) {
+      for (int i = 0; i < 2; ++i) {
+        uint32_t w = 0;
+        for (int m = 0; m < 16; ++m) {
+          w |= (uint32_t)((code(k0 + 32 * i + 2 * m) >> 2) & 1) << m;
+          w |= (uint32_t)((code(k0 + 32 * i + 2 * m + 1) >> 2) & 1) << (16 + m);
+        }
+        cw[4 + i] = w;
+      }
+    }
+  }
+  uint16_t* sc = reinterpret_cast<uint16_t*>(stage + 128 * L.code_row) + (size_t)r * L.nbs;
+  uint8_t* zp = stage + 128 * L.code_row + 128 * L.nbs * 2 + (size_t)r * L.nbs;
+  for (int b = 0; b < L.nbs; ++b) {
+    const int kb = k0 / L.B + b;
+    uint16_t s = 0;
+    uint8_t z = 0;
+    if (valid && kb < nblk) {
+      s = reinterpret_cast<const uint16_t*>(a.scales)[((size_t)e * a.N + row) * nblk + kb];
+      if (a.zp) z = (uint8_t)canon_field(a.zp + ((size_t)e * a.N + row) * zrow, zrow, bits, kb, nblk);
+    }
+    sc[b] = s;
+    if (L.zp_bytes) zp[b] = z;
+  }
+}
+
+GemmLayout make_gemm_layout(int bits, int B, int fc, int N, int K, int I, int zp_mode) {
+  GemmLayout L;
+  L.bits = bits;
+  L.B = B;
+  L.ksteps = (K + 63) / 64;
+  L.ntiles = fc == 1 ? (I + 63) / 64 : (N + 127) / 128;
+  L.code_row = 64 * bits / 8;
+  L.nbs = B >= 64 ? 1 : 64 / B;
+  L.zp_bytes = zp_mode == QMOE_ZP_UINT8 ? ((128 * L.nbs + 15) / 16) * 16 : 0;
+  L.stage_bytes = 128 * L.code_row + 128 * L.nbs * 2 + L.zp_bytes;
+  L.tile_bytes = (size_t)L.ksteps * L.stage_bytes;
+  L.expert_bytes = L.tile_bytes * L.ntiles;
+  return L;
+}
+
+cudaError_t launch_repack_gemm(const GemmRepackArgs& a, cudaStream_t s) {
+  const size_t total = (size_t)a.E * a.L.ntiles * a.L.ksteps * 128;
+  if (total == 0) return cudaSuccess;
+  const size_t blocks = (total + 255) / 256;
+  if (blocks > 0x7fffffff) return cudaErrorInvalidValue;
+  repack_gemm_kernel<<<(unsigned)blocks, 256, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
+// ----------------------------------------------------------------------------
+// Gather of x into route order for the fc1 B operand, and the combine of the
+// fp32 accumulator.
+// ----------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) gather_rows_kernel(const void* __restrict__ x, const int* __restrict__ perm,
+                                                          int k, int R, int H, void* __restrict__ xg) {
+  pdl_wait();
+  const int vec = H / 8;  // 16-byte vectors per row
+  const size_t n = (size_t)R * vec;
+  const uint4* src = static_cast<const uint4*>(x);
+  uint4* dst = static_cast<uint4*>(xg);
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x) {
+    const int p = (int)(i / vec), v = (int)(i % vec);
+    const int t = perm[p] / k;
+    dst[i] = src[(size_t)t * vec + v];
+  }
+  pdl_launch_dependents();
+}
+
+cudaError_t launch_gather(const void* x, const int* perm, int k, int R, int H, void* xg, cudaStream_t s) {
+  const size_t n = (size_t)R * (H / 8);
+  int grid = (int)((n + 255) / 256);
+  if (grid > 152 * 16) grid = 152 * 16;
+  if (grid < 1) grid = 1;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(256);
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, gather_rows_kernel, x, perm, k, R, H, xg);
+}
+
+template <int DT>
+__global__ void __launch_bounds__(256) finalize_acc_kernel(float* __restrict__ acc, void* __restrict__ out, size_t n4) {
+  pdl_wait();
+  float4* a4 = reinterpret_cast<float4*>(acc);
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n4; i += (size_t)gridDim.x * blockDim.x) {
+    const float4 v = a4[i];
+    store_d<DT>(out, 4 * i + 0, v.x);
+    store_d<DT>(out, 4 * i + 1, v.y);
+    store_d<DT>(out, 4 * i + 2, v.z);
+    store_d<DT>(out, 4 * i + 3, v.w);
+    a4[i] = make_float4(0.f, 0.f, 0.f, 0.f);   // ready for the next forward
+  }
+}
+
+cudaError_t launch_finalize_acc(float* acc, void* out, size_t n, int dtype, cudaStream_t s) {
+  const size_t n4 = n / 4;
+  int grid = (int)((n4 + 255) / 256);
+  if (grid > 152 * 8) grid = 152 * 8;
+  if (grid < 1) grid = 1;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(256);
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (dtype == QMOE_F16) return cudaLaunchKernelEx(&cfg, finalize_acc_kernel<QMOE_F16>, acc, out, n4);
+  if (dtype == QMOE_BF16) return cudaLaunchKernelEx(&cfg, finalize_acc_kernel<QMOE_BF16>, acc, out, n4);
+  return cudaLaunchKernelEx(&cfg, finalize_acc_kernel<QMOE_F32>, acc, out, n4);
+}
+
+// ----------------------------------------------------------------------------
+// tcgen05 / TMA helpers
+// ----------------------------------------------------------------------------
+__device__ __forceinline__ void tmem_alloc(uint32_t* dst, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst)),
+               "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+               : "memory");
+}
+// D[tmem] (+)= A[tmem] * B[smem desc]
+__device__ __forceinline__ void umma_ts(uint32_t d, uint32_t a, uint64_t bdesc, uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d),
+      "r"(a), "l"(bdesc), "r"(idesc), "r"(acc)
+      : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+          smem_u32(dst)),
+      "l"(map), "r"(x), "r"(y), "r"(smem_u32(bar))
+      : "memory");
+}
+__device__ __forceinline__ void red_add_f32(float* p, float v) {
+  asm volatile("red.global.add.f32 [%0], %1;" ::"l"(p), "f"(v) : "memory");
+}
+
+#define TC_LD32(taddr, v)                                                                               \
+  asm volatile(                                                                                         \
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"  \
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"                        \
+      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]), \
+        "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]),        \
+        "=r"(v[15]), "=r"(v[16]), "=r"(v[17]), "=r"(v[18]), "=r"(v[19]), "=r"(v[20]), "=r"(v[21]),      \
+        "=r"(v[22]), "=r"(v[23]), "=r"(v[24]), "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]),      \
+        "=r"(v[29]), "=r"(v[30]), "=r"(v[31])                                                           \
+      : "r"(taddr)                                                                                      \
+      : "memory")
+
+#define TC_ST32(taddr, v)                                                                                \
+  asm volatile(                                                                                          \
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15," \
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),              \
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]), \
+      "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]), "r"(v[16]),    \
+      "r"(v[17]), "r"(v[18]), "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]), "r"(v[24]),    \
+      "r"(v[25]), "r"(v[26]), "r"(v[27]), "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])                 \
+      : "memory")
+
+__device__ __forceinline__ void tc_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+__device__ __forceinline__ void tc_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+// Shared-memory matrix descriptor: K-major, 128-byte swizzle, 8-row groups
+// 1024 bytes apart.
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((addr & 0x3FFFF) >> 4);          // start address
+  d |= (uint64_t)1 << 16;                           // leading byte offset (unused for SW128 K-major)
+  d |= (uint64_t)(1024 >> 4) << 32;                 // stride byte offset
+  d |= (uint64_t)1 << 46;                           // descriptor version
+  d |= (uint64_t)2 << 61;                           // 128-byte swizzle
+  return d;
+}
+
+// Instruction descriptor, kind::f16: D f32, A/B f16 or bf16, both K-major.
+__device__ __forceinline__ uint32_t idesc_f16(bool bf16, int M, int N) {
+  uint32_t d = 0;
+  d |= 1u << 4;                                     // D = f32
+  d |= (bf16 ? 1u : 0u) << 7;                       // A type
+  d |= (bf16 ? 1u : 0u) << 10;                      // B type
+  d |= (uint32_t)(N >> 3) << 17;
+  d |= (uint32_t)(M >> 4) << 24;
+  return d;
+}
+
+// Bounded wait that also gives up when another role has aborted.
+__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, const WaitCfg& w,
+                                              volatile int* abort_flag) {
+  for (long long i = 0; i < w.limit; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 63) == 63 && *abort_flag) return false;
+  }
+  atomicExch(w.status, DEV_TIMEOUT);
+  *abort_flag = 1;
+  return false;
+}
+
+// ----------------------------------------------------------------------------
+// The grouped GEMM kernel
+// ----------------------------------------------------------------------------
+constexpr int kStagesB = 4;       // token tiles: 256 x 64 x 2 B = 32 KB each
+constexpr int kStagesW = 6;       // packed weight stages
+constexpr int kStagesA = 4;       // dequantised A stages in TMEM (32 columns each)
+constexpr int kTileN = 256;       // token rows per tile (max MMA N)
+constexpr int kBBytes = kTileN * 128;
+constexpr int kTmemCols = 512;
+constexpr int kAcol0 = 256;       // first TMEM column of the A ring
+constexpr int kGemmThreads = 384;
+
+struct GemmSmem {
+  static constexpr int b_off = 0;
+  static constexpr int w_off = kStagesB * kBBytes;
+  __host__ __device__ static int bar_off(int wstage) { return w_off + kStagesW * ((wstage + 127) / 128 * 128); }
+  __host__ __device__ static int total(int wstage) { return bar_off(wstage) + 1024; }
+};
+
+template <int BITS, int ZPM, bool BF16>
+__device__ __forceinline__ void dequant_row(const uint8_t* stage, const GemmLayout& L, int r, uint32_t zoff2,
+                                            uint32_t* v) {
+  constexpr uint32_t MAGIC = BF16 ? 0x43004300u : 0x64006400u;
+  const uint8_t* row = stage + r * (64 * BITS / 8);
+  constexpr int NW = BITS == 4 ? 8 : (BITS == 3 ? 6 : 4);
+  uint32_t w[NW];
+  if constexpr (BITS == 4) {
+    const uint4 q0 = reinterpret_cast<const uint4*>(row)[0];
+    const uint4 q1 = reinterpret_cast<const uint4*>(row)[1];
+    w[0] = q0.x; w[1] = q0.y; w[2] = q0.z; w[3] = q0.w;
+    w[4] = q1.x; w[5] = q1.y; w[6] = q1.z; w[7] = q1.w;
+  } else if constexpr (BITS == 2) {
+    const uint4 q0 = reinterpret_cast<const uint4*>(row)[0];
+    w[0] = q0.x; w[1] = q0.y; w[2] = q0.z; w[3] = q0.w;
+  } else {
+    // 24-byte rows: 8-byte aligned
+    const uint2 q0 = reinterpret_cast<const uint2*>(row)[0];
+    const uint2 q1 = reinterpret_cast<const uint2*>(row)[1];
+    const uint2 q2 = reinterpret_cast<const uint2*>(row)[2];
+    w[0] = q0.x; w[1] = q0.y; w[2] = q1.x; w[3] = q1.y; w[4] = q2.x; w[5] = q2.y;
+  }
+  const uint16_t* sc = reinterpret_cast<const uint16_t*>(stage + 128 * L.code_row) + r * L.nbs;
+  const uint8_t* zp = stage + 128 * L.code_row + 128 * L.nbs * 2 + r * L.nbs;
+  uint32_t ss[2], zz[2];
+#pragma unroll
+  for (int b = 0; b < 2; ++b) {
+    const int bb = b < L.nbs ? b : 0;
+    ss[b] = (uint32_t)sc[bb] * 0x00010001u;
+    if (ZPM == QMOE_ZP_UINT8) zz[b] = MAGIC | ((uint32_t)zp[bb] * 0x00010001u);
+    else zz[b] = MAGIC | ((1u << (BITS - 1)) * 0x00010001u);
+  }
+  const int half = L.nbs > 1 ? 16 : 32;  // registers per scale block
+#pragma unroll
+  for (int j = 0; j < 32; ++j) {
+    uint32_t p;
+    if constexpr (BITS == 4) p = (w[j >> 2] >> (4 * (j & 3))) & 0x000F000Fu;
+    else if constexpr (BITS == 2) p = (w[j >> 3] >> (2 * (j & 7))) & 0x00030003u;
+    else p = ((w[j >> 3] >> (2 * (j & 7))) & 0x00030003u) | (((w[4 + (j >> 4)] >> (j & 15)) & 0x00010001u) << 2);
+    uint32_t x = p | MAGIC;
+    const int b = j >= half ? 1 : 0;
+    if (ZPM == QMOE_ZP_OFFSET) {
+      x = sub2<BF16>(x, MAGIC);
+      x = sub2<BF16>(x, zoff2);
+    } else {
+      x = sub2<BF16>(x, zz[b]);
+    }
+    v[j] = mul2<BF16>(x, ss[b]);
+  }
+}
+
+template <int BITS, int ZPM, bool BF16, bool GLU>
+__global__ void __launch_bounds__(kGemmThreads, 1)
+    gemm_kernel(const __grid_constant__ CUtensorMap tmB, const GemmArgs a) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  // 1024-byte alignment for the swizzled B tiles
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const GemmLayout& L = a.L;
+  const int wstage = (L.stage_bytes + 127) / 128 * 128;
+  uint8_t* bring = smem + GemmSmem::b_off;
+  uint8_t* wring = smem + GemmSmem::w_off;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + GemmSmem::bar_off(wstage));
+  uint64_t* b_full = bars;
+  uint64_t* b_empty = b_full + kStagesB;
+  uint64_t* w_full = b_empty + kStagesB;
+  uint64_t* w_empty = w_full + kStagesW;
+  uint64_t* a_full = w_empty + kStagesW;
+  uint64_t* a_empty = a_full + kStagesA;
+  uint64_t* acc_full = a_empty + kStagesA;
+  uint64_t* acc_empty = acc_full + 1;
+  uint64_t* drain_bar = acc_empty + 1;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain_bar + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+  volatile int* counters = abort_flag + 1;   // [0] = B steps consumed, [1] = W steps consumed
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kStagesB; ++i) { mbar_init(&b_full[i], 1); mbar_init(&b_empty[i], 1); }
+    for (int i = 0; i < kStagesW; ++i) { mbar_init(&w_full[i], 1); mbar_init(&w_empty[i], 4); }
+    for (int i = 0; i < kStagesA; ++i) { mbar_init(&a_full[i], 4); mbar_init(&a_empty[i], 1); }
+    mbar_init(acc_full, 1);
+    mbar_init(acc_empty, 4);
+    mbar_init(drain_bar, 1);
+    *abort_flag = 0;
+    counters[0] = counters[1] = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_holder, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_holder;
+
+  pdl_wait();
+  const int n_items = *a.n_items;
+  const int total_tiles = n_items * L.ntiles;
+
+  if (warp == 0 && lane == 0) {
+    // ---------------- producer: token tiles (TMA) + weight stages (bulk) ----------------
+    int kc = 0, nb_issued = 0, nw_issued = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; tile < total_tiles && ok; tile += gridDim.x) {
+      const Item it = a.items[tile / L.ntiles];
+      const int nt = tile % L.ntiles;
+      const uint8_t* wsrc = a.wq + (size_t)it.e * L.expert_bytes + (size_t)nt * L.tile_bytes;
+      for (int ks = 0; ks < L.ksteps && ok; ++ks, ++kc) {
+        const int sb = kc % kStagesB, sw = kc % kStagesW;
+        ok = wait_or_abort(&b_empty[sb], ((kc / kStagesB) & 1) ^ 1, a.wait, abort_flag);
+        if (!ok) break;
+        mbar_arrive_expect_tx(&b_full[sb], kBBytes);
+        tma_load_2d(bring + sb * kBBytes, &tmB, ks * 64, it.start, &b_full[sb]);
+        nb_issued = kc + 1;
+        ok = wait_or_abort(&w_empty[sw], ((kc / kStagesW) & 1) ^ 1, a.wait, abort_flag);
+        if (!ok) break;
+        mbar_arrive_expect_tx(&w_full[sw], L.stage_bytes);
+        bulk_g2s(wring + sw * wstage, wsrc + (size_t)ks * L.stage_bytes, L.stage_bytes, &w_full[sw]);
+        nw_issued = kc + 1;
+      }
+    }
+    if (!ok) {
+      // Drain: wait for every copy issued but not consumed (fixed large bound)
+      // so that none lands in shared memory after the CTA has left.
+      const WaitCfg drain{a.wait.status, kDrainWaitLimit};
+      for (int i = counters[0]; i < nb_issued; ++i)
+        mbar_wait_bounded(&b_full[i % kStagesB], (i / kStagesB) & 1, drain);
+      for (int i = counters[1]; i < nw_issued; ++i)
+        mbar_wait_bounded(&w_full[i % kStagesW], (i / kStagesW) & 1, drain);
+    }
+  } else if (warp == 1 && lane == 0) {
+    // ---------------- MMA issuer ----------------
+    int kc = 0, tc = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; tile < total_tiles && ok; tile += gridDim.x, ++tc) {
+      const Item it = a.items[tile / L.ntiles];
+      const int N = (it.rows + 15) & ~15;
+      const uint32_t idesc = idesc_f16(BF16, 128, N);
+      ok = wait_or_abort(acc_empty, (tc & 1) ^ 1, a.wait, abort_flag);
+      if (!ok) break;
+      tc_fence_after();
+      for (int ks = 0; ks < L.ksteps; ++ks, ++kc) {
+        const int sb = kc % kStagesB, sa = kc % kStagesA;
+        ok = wait_or_abort(&b_full[sb], (kc / kStagesB) & 1, a.wait, abort_flag);
+        if (ok) ok = wait_or_abort(&a_full[sa], (kc / kStagesA) & 1, a.wait, abort_flag);
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t baddr = smem_u32(bring + sb * kBBytes);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+          umma_ts(tmem, tmem + kAcol0 + sa * 32 + kk * 8, smem_desc_sw128(baddr + kk * 32), idesc,
+                  (ks | kk) != 0 ? 1u : 0u);
+        tc_commit(&b_empty[sb]);
+        tc_commit(&a_empty[sa]);
+        counters[0] = kc + 1;
+      }
+      if (ok) tc_commit(acc_full);
+    }
+    // All MMAs issued by this thread have completed once drain_bar flips.
+    tc_commit(drain_bar);
+    const WaitCfg drain{a.wait.status, kDrainWaitLimit};
+    mbar_wait_bounded(drain_bar, 0, drain);
+  } else if (warp >= 4 && warp < 8) {
+    // ---------------- dequant: packed weights -> bf16/f16 pairs in TMEM ----------------
+    const int q = warp & 3;
+    const int r = q * 32 + lane;          // TMEM lane = weight row of the tile
+    uint32_t zoff2 = 0;
+    if (ZPM == QMOE_ZP_OFFSET) {
+      if (BF16) zoff2 = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(a.zp_offset)) * 0x00010001u;
+      else zoff2 = (uint32_t)__half_as_ushort(__float2half_rn(a.zp_offset)) * 0x00010001u;
+    }
+    int kc = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; tile < total_tiles && ok; tile += gridDim.x) {
+      for (int ks = 0; ks < L.ksteps; ++ks, ++kc) {
+        const int sw = kc % kStagesW, sa = kc % kStagesA;
+        ok = wait_or_abort(&w_full[sw], (kc / kStagesW) & 1, a.wait, abort_flag);
+        if (ok) ok = wait_or_abort(&a_empty[sa], ((kc / kStagesA) & 1) ^ 1, a.wait, abort_flag);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+        tc_fence_after();
+        uint32_t v[32];
+        dequant_row<BITS, ZPM, BF16>(wring + sw * wstage, L, r, zoff2, v);
+        const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + kAcol0 + sa * 32;
+        TC_ST32(taddr, v);
+        tc_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(&a_full[sa]);
+          mbar_arrive(&w_empty[sw]);
+          if (q == 0) counters[1] = kc + 1;
+        }
+      }
+    }
+  } else if (warp >= 8) {
+    // ---------------- epilogue: TMEM -> GLU -> h (fc1) | weighted scatter (fc2) ----------------
+    const int q = warp & 3;
+    const int r = q * 32 + lane;
+    int tc = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; tile < total_tiles && ok; tile += gridDim.x, ++tc) {
+      const Item it = a.items[tile / L.ntiles];
+      const int nt = tile % L.ntiles;
+      ok = wait_or_abort(acc_full, tc & 1, a.wait, abort_flag);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      tc_fence_after();
+      for (int c0 = 0; c0 < it.rows; c0 += 32) {
+        uint32_t v[32];
+        TC_LD32(tmem + ((uint32_t)(q * 32) << 16) + c0, v);
+        tc_wait_ld();
+        if (GLU) {
+          const int n = nt * 64 + (r >> 1);
+          const bool odd = lane & 1;
+          const int jbeg = odd ? 16 : 0;
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const float mine = __uint_as_float(v[j]);
+            const float other = __shfl_xor_sync(0xffffffffu, mine, 1);
+            if (j >= jbeg && j < jbeg + 16) {
+              const int c = c0 + j;
+              if (c < it.rows && n < a.N_out) {
+                const float g = odd ? other : mine, u = odd ? mine : other;
+                const float h = glu(a.act, g, u);
+                const size_t o = (size_t)(it.start + c) * a.N_out + n;
+                if (BF16) static_cast<__nv_bfloat16*>(a.hout)[o] = __float2bfloat16_rn(h);
+                else static_cast<__half*>(a.hout)[o] = __float2half_rn(h);
+              }
+            }
+          }
+        } else {
+          const int m = nt * 128 + r;
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const int c = c0 + j;
+            if (c < it.rows) {
+              const int route = a.perm[it.start + c];
+              const float wr = a.w[route];
+              if (m < a.N_out)
+                red_add_f32(a.out_acc + (size_t)(route / a.k) * a.N_out + m, wr * __uint_as_float(v[j]));
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(acc_empty);
+    }
+  }
+  pdl_launch_dependents();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem, kTmemCols);
+}
+
+// ----------------------------------------------------------------------------
+// Host side
+// ----------------------------------------------------------------------------
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+cudaError_t make_token_map(CUtensorMap* map, const void* base, int rows, int K, bool bf16) {
+  auto fn = encode_fn();
+  if (!fn) return cudaErrorNotSupported;
+  cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)K * 2};
+  cuuint32_t box[2] = {64, (cuuint32_t)kTileN};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
+                  const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+template <int BITS, int ZPM, bool BF16, bool GLU>
+static cudaError_t launch_g(const CUtensorMap& map, const GemmArgs& a, cudaStream_t s) {
+  const int wstage = (a.L.stage_bytes + 127) / 128 * 128;
+  const int smem = GemmSmem::total(wstage) + 1024;  // + alignment slack
+  auto kern = gemm_kernel<BITS, ZPM, BF16, GLU>;
+  cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (err != cudaSuccess) return err;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.gridDim = dim3(a.grid);
+  cfg.blockDim = dim3(kGemmThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, map, a);
+}
+
+template <int BITS, int ZPM, bool BF16>
+static cudaError_t launch_g_glu(const CUtensorMap& m, const GemmArgs& a, cudaStream_t s) {
+  return a.fc == 1 ? launch_g<BITS, ZPM, BF16, true>(m, a, s) : launch_g<BITS, ZPM, BF16, false>(m, a, s);
+}
+template <int BITS, int ZPM>
+static cudaError_t launch_g_dt(const CUtensorMap& m, const GemmArgs& a, cudaStream_t s) {
+  return a.bf16 ? launch_g_glu<BITS, ZPM, true>(m, a, s) : launch_g_glu<BITS, ZPM, false>(m, a, s);
+}
+template <int BITS>
+static cudaError_t launch_g_zp(const CUtensorMap& m, const GemmArgs& a, cudaStream_t s) {
+  if (a.zp_mode == QMOE_ZP_UINT8) return launch_g_dt<BITS, QMOE_ZP_UINT8>(m, a, s);
+  if (a.zp_mode == QMOE_ZP_OFFSET) return launch_g_dt<BITS, QMOE_ZP_OFFSET>(m, a, s);
+  return launch_g_dt<BITS, QMOE_ZP_SYMMETRIC>(m, a, s);
+}
+
+cudaError_t launch_gemm(const CUtensorMap& map, const GemmArgs& a, cudaStream_t s) {
+  if (a.max_items <= 0 || a.grid <= 0) return cudaSuccess;
+  switch (a.L.bits) {
+    case 2: return launch_g_zp<2>(map, a, s);
+    case 3: return launch_g_zp<3>(map, a, s);
+    case 4: return launch_g_zp<4>(map, a, s);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace qmoe
