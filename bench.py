@@ -52,6 +52,24 @@ def dist_env():
     return rank, world, local
 
 
+def max_over_ranks(value: float, device=None) -> float:
+    """Max of a per-rank scalar over all ranks (identity without a process
+    group).  Each rank runs an independent replica, so the job's time is the
+    slowest rank's."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(value)
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(tokens_per_rank: int, world: int, ms: float) -> float:
+    """Whole-job tokens/s: every rank processes its own batch (weak scaling)."""
+    return world * tokens_per_rank / (ms * 1e-3)
+
+
 def measured_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -257,12 +275,8 @@ def run_ours(args):
     clk = clocks.stop()
     layer.poll()
 
-    ms = sum(per_step) / len(per_step)
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
-    value = world * cfg.T / (ms * 1e-3)
+    ms = max_over_ranks(sum(per_step) / len(per_step), dev)
+    value = job_throughput(cfg.T, world, ms)
 
     # Routing of the run: distinct experts -> algorithmic bytes.
     _, _, _, offs = layer.routing(cfg.T, stream=None)
@@ -289,11 +303,7 @@ def run_ours(args):
         t0 = time.perf_counter()
         layer.forward_host(xh, lh, oh, stream=stream)
         e2e_ms.append((time.perf_counter() - t0) * 1e3)
-    e2e = statistics.mean(e2e_ms)
-    if world > 1:
-        t = torch.tensor([e2e], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e = float(t.item())
+    e2e = max_over_ranks(statistics.mean(e2e_ms), dev)
 
     launches_per_step = 4 if cfg.T <= 64 else 5
     line = {
@@ -315,7 +325,7 @@ def run_ours(args):
                      "kernel": "fc1 decode (decode_mma_kernel)", "bytes_per_launch": fc1_bytes,
                      "peak_kind": peak_kind},
         "clocks": clk,
-        "e2e": {"value": world * cfg.T / (e2e * 1e-3), "unit": "tokens/s",
+        "e2e": {"value": job_throughput(cfg.T, world, e2e), "unit": "tokens/s",
                 "h2d_bytes_per_step": cfg.T * cfg.H * ds + cfg.T * cfg.E * 4,
                 "d2h_bytes_per_step": cfg.T * cfg.H * ds},
         "gpu_launches": launches_per_step * args.steps,

@@ -149,6 +149,7 @@ qmoe_status qmoe_prepack(qmoe_layer* layer, int fc, const uint8_t* codes_dev,
  *   x_dev       D [num_tokens, H]
  *   logits_dev  float32 [num_tokens, E]
  *   out_dev     D [num_tokens, H] (written)
+ * x_dev and out_dev must be 16-byte aligned (INVALID_ARG otherwise).
  * num_tokens == 0 returns QMOE_OK without launching anything.  Both fcs
  * must have been prepacked.  No host synchronisation.
  */

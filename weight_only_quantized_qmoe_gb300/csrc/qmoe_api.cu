@@ -403,6 +403,8 @@ qmoe_status qmoe_forward(qmoe_layer* l, const void* x, const float* logits, void
   if (T < 0) return fail(l, QMOE_ERR_INVALID_ARG, "num_tokens < 0");
   if (T == 0) return QMOE_OK;
   if (!x || !logits || !out) return fail(l, QMOE_ERR_INVALID_ARG, "null x / logits / out");
+  if ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(out)) & 15)
+    return fail(l, QMOE_ERR_INVALID_ARG, "x and out must be 16-byte aligned");
   if (!l->proj[0].ready || !l->proj[1].ready)
     return fail(l, QMOE_ERR_STATE, "prepack fc1 and fc2 before qmoe_forward");
   if (T * l->k > INT_MAX / 8) return fail(l, QMOE_ERR_INVALID_ARG, "num_tokens too large");

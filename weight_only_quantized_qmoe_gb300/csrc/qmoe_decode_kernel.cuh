@@ -114,22 +114,52 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
 
   // Stage the item's rows (B operand) in fragment order:
   // bop[((kt * NG + ng) * 32 + g*4 + t) * 2 + hi] = (row ng*8+g, k = kt*16 + hi*8 + 2t, +1)
+  // Only the item's rows are loaded (16 bytes per thread, all loads of a pass
+  // in flight before any store); token columns past it.rows are never stored
+  // by the epilogue, so their fragments may hold anything.  The K padding
+  // (when K is not a multiple of SC) must be zero: it meets zero weights.
   {
-    const int Kp2 = L.nkc * SC / 2;
-    const int K = a.K;
+    const int K = a.K;                 // multiple of 32
+    const int Kp = L.nkc * SC;
+    const int vrow = K / 8;            // 16-byte vectors per row
+    const int nvec = it.rows * vrow;
     const uint16_t* src16 = static_cast<const uint16_t*>(a.src);
-    for (int idx = threadIdx.x; idx < NG * 8 * Kp2; idx += blockDim.x) {
-      const int n = idx / Kp2, q = idx % Kp2;
-      uint32_t v = 0;
-      if (n < it.rows && 2 * q < K) {
-        size_t row;
-        if (a.fc == 1) row = (size_t)(a.perm[it.start + n] / a.k);
-        else row = (size_t)(it.start + n);
-        v = *reinterpret_cast<const uint32_t*>(src16 + row * K + 2 * q);
+    constexpr int U = 4;
+    for (int base = threadIdx.x; base < nvec; base += U * blockDim.x) {
+      uint4 v[U];
+      int nn[U], kv[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int idx = base + u * blockDim.x;
+        nn[u] = -1;
+        if (idx < nvec) {
+          nn[u] = idx / vrow;
+          kv[u] = idx % vrow;
+          const size_t row = a.fc == 1 ? (size_t)(a.perm[it.start + nn[u]] / a.k)
+                                       : (size_t)(it.start + nn[u]);
+          v[u] = ld_nc_v4(src16 + row * K + kv[u] * 8);
+        }
       }
-      const int kk = 2 * q, kt = kk >> 4, within = kk & 15;
-      const int tt = (within & 7) >> 1, hi = within >> 3;
-      bop[((kt * NG + (n >> 3)) * 32 + (n & 7) * 4 + tt) * 2 + hi] = v;
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        if (nn[u] < 0) continue;
+        const uint32_t w4[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+          const int kk = kv[u] * 8 + 2 * w, kt = kk >> 4, within = kk & 15;
+          const int tt = (within & 7) >> 1, hi = within >> 3;
+          bop[((kt * NG + (nn[u] >> 3)) * 32 + (nn[u] & 7) * 4 + tt) * 2 + hi] = w4[w];
+        }
+      }
+    }
+    if (Kp > K) {
+      const int pad2 = (Kp - K) / 2;   // 32-bit pairs of padding per row
+      for (int idx = threadIdx.x; idx < NG * 8 * pad2; idx += blockDim.x) {
+        const int n = idx / pad2, kk = K + 2 * (idx % pad2);
+        const int kt = kk >> 4, within = kk & 15;
+        const int tt = (within & 7) >> 1, hi = within >> 3;
+        bop[((kt * NG + (n >> 3)) * 32 + (n & 7) * 4 + tt) * 2 + hi] = 0u;
+      }
     }
   }
   __syncthreads();
