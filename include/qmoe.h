@@ -115,10 +115,10 @@ qmoe_status qmoe_create(int hidden, int inter, int experts, int top_k, int bits_
 qmoe_status qmoe_set_routing(qmoe_layer* layer, int normalize);
 
 /* Fractional zero point for QMOE_ZP_OFFSET: w = (code - offset) * scale.
- * [PR "fused int2 ...", zero_point_offset]  Every (code - offset) must be
- * exactly representable in the activation type (e.g. offsets that are
- * multiples of 1/8 for 4-bit codes); other values return UNSUPPORTED.
- * Must be called before qmoe_prepack in that mode. */
+ * [PR "fused int2 ...", zero_point_offset]  Supported centres are multiples
+ * of 0.5 in [0, 2^bits - 1] (e.g. 1.5 for 2-bit codes); other values return
+ * UNSUPPORTED with a "requantize" hint.  Must be called before qmoe_prepack
+ * in that mode. */
 qmoe_status qmoe_set_zero_point_offset(qmoe_layer* layer, float offset);
 
 /* Experts with more than `min_rows` routed rows take the tensor-core grouped

@@ -46,7 +46,7 @@ def test_gemm_variant_parity(qm, name):
     layer, out = run_layer(qm, inp, min_rows=0)
     check_routing(layer, inp, min_rows=0)
     items, m_tile = layer.worklist(1, cfg.T)
-    assert m_tile == 256 and len(items) > 0
+    assert m_tile == 128 and len(items) > 0
     check_out(out, O.forward(inp), cfg.dtype)
 
 

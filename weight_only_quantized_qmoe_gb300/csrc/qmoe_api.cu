@@ -39,7 +39,9 @@ const char* kStatusNames[] = {"QMOE_OK",          "QMOE_ERR_INVALID_ARG", "QMOE_
                               "QMOE_ERR_CUDA",    "QMOE_ERR_OOM",         "QMOE_ERR_STATE",
                               "QMOE_ERR_TIMEOUT"};
 
-constexpr long long kDefaultWaitLimit = 1LL << 24;
+// Polls of a bounded device-side wait (each poll parks the warp for up to
+// ~1 us): about two seconds before a wait gives up.
+constexpr long long kDefaultWaitLimit = 1LL << 21;
 
 }  // namespace
 
@@ -163,7 +165,7 @@ void item_heights(const qmoe_layer* l, int64_t T, int* tb0, int* tb1) {
     while (ng > 1 && ng * ktiles * 256 > 160 * 1024) ng /= 2;
     *tb0 = 8 * ng;
   }
-  *tb1 = 256;
+  *tb1 = 128;
 }
 
 int64_t items_cap(const qmoe_layer* l, int which, int64_t T, int tb) {
@@ -272,6 +274,14 @@ qmoe_status qmoe_set_zero_point_offset(qmoe_layer* l, float offset) {
   if (l->zp_mode != QMOE_ZP_OFFSET)
     return fail(l, QMOE_ERR_STATE, "zero_point_offset needs zp_mode == QMOE_ZP_OFFSET");
   if (!std::isfinite(offset)) return fail(l, QMOE_ERR_INVALID_ARG, "zero_point_offset must be finite");
+  // Supported centres: multiples of 1/2 inside the code range.  Then every
+  // (code - offset) is exact in D and the kernels form it with one packed
+  // subtraction from a half-unit magic number.
+  const int maxcode = (1 << (l->bits[0] < l->bits[1] ? l->bits[0] : l->bits[1])) - 1;
+  if (std::floor(2.0 * offset) != 2.0 * offset || offset < 0.0f || offset > (float)maxcode)
+    return fail(l, QMOE_ERR_UNSUPPORTED,
+                "zero_point_offset must be a multiple of 0.5 within the code range; "
+                "requantize with a half-integer centre");
   for (int f = 0; f < 2; ++f)
     for (int c = 0; c < (1 << l->bits[f]); ++c)
       if (!exact_in((double)c - (double)offset, l->dtype) || !exact_in((double)offset, l->dtype))
@@ -666,3 +676,4 @@ void qmoe_destroy(qmoe_layer* l) {
 }
 
 }  // extern "C"
+

@@ -31,16 +31,6 @@ __host__ __device__ inline DecodeSmem decode_smem(const DecodeLayout& L, int NG,
   return m;
 }
 
-template <bool BF16>
-struct Magic;
-template <>
-struct Magic<true> {
-  static constexpr uint32_t v = 0x43004300u;  // bf16 pair (128, 128), ulp 1
-};
-template <>
-struct Magic<false> {
-  static constexpr uint32_t v = 0x64006400u;  // f16 pair (1024, 1024), ulp 1
-};
 
 // Fragment pair r (0..3) of k-tile j of this lane's code words (pairs of
 // 16-bit fields, low element in bits 0.., high element in bits 16..).
@@ -174,16 +164,7 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
 
   const int ng_act = (it.rows + 7) >> 3;
   constexpr uint32_t MAGIC = Magic<BF16>::v;
-  uint32_t zoff2 = 0;
-  if (ZPM == QMOE_ZP_OFFSET) {
-    if (BF16) {
-      const __nv_bfloat16 z = __float2bfloat16_rn(a.zp_offset);
-      zoff2 = (uint32_t)__bfloat16_as_ushort(z) * 0x00010001u;
-    } else {
-      const __half z = __float2half_rn(a.zp_offset);
-      zoff2 = (uint32_t)__half_as_ushort(z) * 0x00010001u;
-    }
-  }
+  const uint32_t zoff2 = ZPM == QMOE_ZP_OFFSET ? half_magic_offset<BF16>(a.zp_offset) : 0u;
   constexpr uint32_t ZSYM = MAGIC | ((1u << (BITS - 1)) * 0x00010001u);
 
   bool ok = true;
@@ -207,9 +188,21 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
 #pragma unroll
       for (int s = 0; s < NSUB; ++s) {
         const uint32_t* base = reinterpret_cast<const uint32_t*>(ch + s * L.code_bytes);
+        if constexpr (WPL % 4 == 0) {
 #pragma unroll
-        for (int w = 0; w < WPL; ++w) cw[s][w] = base[lane * WPL + w];
-        if (BITS == 3) {
+          for (int w = 0; w < WPL; w += 4) {
+            const uint4 q4 = *reinterpret_cast<const uint4*>(base + lane * WPL + w);
+            cw[s][w] = q4.x; cw[s][w + 1] = q4.y; cw[s][w + 2] = q4.z; cw[s][w + 3] = q4.w;
+          }
+        } else {
+          static_assert(WPL % 2 == 0, "code words per lane");
+#pragma unroll
+          for (int w = 0; w < WPL; w += 2) {
+            const uint2 q2 = *reinterpret_cast<const uint2*>(base + lane * WPL + w);
+            cw[s][w] = q2.x; cw[s][w + 1] = q2.y;
+          }
+        }
+        if constexpr (BITS == 3) {
 #pragma unroll
           for (int w = 0; w < WPH; ++w) hw[s][w] = base[32 * WPL + lane * WPH + w];
         }
@@ -239,11 +232,14 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
           for (int s = 0; s < NSUB; ++s) {
 #pragma unroll
             for (int r = 0; r < 4; ++r) {
-              uint32_t v = code_pair<BITS>(cw[s], hw[s], j, r) | MAGIC;
-              if (ZPM == QMOE_ZP_OFFSET) {
-                v = sub2<BF16>(v, MAGIC);
+              uint32_t v;
+              if constexpr (ZPM == QMOE_ZP_OFFSET) {
+                // half-unit magic: (M/2 + c) - (M/2 + z) = c - z, exact for
+                // half-integer z (the only centres the API accepts)
+                v = (code_pair<BITS>(cw[s], hw[s], j, r) << 1) | Magic<BF16>::half;
                 v = sub2<BF16>(v, zoff2);
               } else {
+                v = code_pair<BITS>(cw[s], hw[s], j, r) | MAGIC;
                 v = sub2<BF16>(v, zz[s][r & 1]);
               }
               afrag[s][r] = mul2<BF16>(v, ss[s][r & 1]);

@@ -22,7 +22,7 @@ struct WaitCfg {
 
 // Polls of the wait that drains a CTA's own in-flight copies after another
 // wait ran out (large: those copies always complete).
-constexpr long long kDrainWaitLimit = 1LL << 24;
+constexpr long long kDrainWaitLimit = 1LL << 21;
 
 // ----------------------------------------------------------------------------
 // Work-list item: (expert, row_start in grouped order, rows, pad)
@@ -194,14 +194,19 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
       : "memory");
 }
 
+// One poll of an mbarrier phase.  The suspend-time hint lets the hardware
+// park the warp (up to ~1 us) until the phase completes instead of spinning,
+// so waiting warps leave issue slots to the warps that compute.
+constexpr uint32_t kSuspendHintNs = 1000;
+
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
+      : "r"(smem_u32(bar)), "r"(parity), "n"(kSuspendHintNs)
       : "memory");
   return ok != 0;
 }
@@ -261,6 +266,34 @@ __device__ __forceinline__ uint32_t mul2<false>(uint32_t a, uint32_t b) {
   uint32_t d;
   asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
   return d;
+}
+
+// Magic numbers that turn small codes into exact 16-bit floats with one OR.
+//   v:    the pair (M, M) with ulp 1 at M (bf16 M = 128, f16 M = 1024):
+//         M | c = M + c, then (M + c) - (M + z) = c - z for integer z;
+//   half: the pair (M/2, M/2) with ulp 1/2 there (bf16 64, f16 512):
+//         M/2 | (c << 1) = M/2 + c, and M/2 + z is exact for half-integer z.
+template <bool BF16>
+struct Magic;
+template <>
+struct Magic<true> {
+  static constexpr uint32_t v = 0x43004300u;
+  static constexpr uint32_t half = 0x42804280u;
+  static constexpr float half_base = 64.f;
+};
+template <>
+struct Magic<false> {
+  static constexpr uint32_t v = 0x64006400u;
+  static constexpr uint32_t half = 0x60006000u;
+  static constexpr float half_base = 512.f;
+};
+
+// The pair (M/2 + z, M/2 + z) for a half-integer zero point z.
+template <bool BF16>
+__device__ __forceinline__ uint32_t half_magic_offset(float z) {
+  const float v = Magic<BF16>::half_base + z;
+  if (BF16) return (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(v)) * 0x00010001u;
+  return (uint32_t)__half_as_ushort(__float2half_rn(v)) * 0x00010001u;
 }
 
 // D = A(16x16, row) * B(16x8, col) + C, fp32 accumulate.

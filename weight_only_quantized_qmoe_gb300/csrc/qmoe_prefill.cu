@@ -10,15 +10,17 @@
 //
 // GB300 design (ours; the pages' SM80 DqMma prior art does not apply):
 //   D[128 weight rows, N tokens] += A[128 rows, 64 k] * B[N tokens, 64 k]^T
-//   * A = dequantised weights, written by 4 CUDA-core warps straight into
-//     tensor memory (tcgen05.st, one thread per weight row, 64 k per step):
-//     the dequant costs no shared-memory bandwidth, which the B stream needs;
+//   * A = dequantised weights, written by CUDA-core warps straight into
+//     tensor memory (tcgen05.st, one thread per weight row, 64 k per step;
+//     two warp groups take alternate k-steps): the dequant costs no
+//     shared-memory bandwidth, which the B stream needs;
 //   * B = the routed token rows (x gathered in route order for fc1, h for
-//     fc2), TMA tiles of 256 x 64 (128-byte swizzle) in a shared ring;
-//   * tcgen05.mma.cta_group::1.kind::f16, fp32 accumulators in TMEM
-//     (256 columns), N = the tile's rows rounded up to 16 (no padded work);
+//     fc2), TMA tiles of 128 x 64 (128-byte swizzle) in a shared ring;
+//   * tcgen05.mma.cta_group::1.kind::f16, fp32 accumulators in TMEM, two of
+//     128 columns so the epilogue of one tile overlaps the next tile's MMAs;
+//     N = the tile's rows rounded up to 16 (no padded work);
 //   * warp roles: 0 = TMA / bulk-copy producer, 1 = MMA issuer (one thread)
-//     and TMEM owner, 4..7 = dequant, 8..11 = epilogue (tcgen05.ld);
+//     and TMEM owner, 4..11 = dequant, 12..15 = epilogue (tcgen05.ld);
 //   * persistent CTAs stride over the (item, weight-tile) list; fc1 rows are
 //     interleaved gate/up so the GLU pairs sit in adjacent TMEM lanes;
 //   * every wait is bounded; a timeout aborts all roles, drains in-flight
@@ -317,14 +319,15 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, co
 // ----------------------------------------------------------------------------
 // The grouped GEMM kernel
 // ----------------------------------------------------------------------------
-constexpr int kStagesB = 4;       // token tiles: 256 x 64 x 2 B = 32 KB each
-constexpr int kStagesW = 6;       // packed weight stages
-constexpr int kStagesA = 4;       // dequantised A stages in TMEM (32 columns each)
-constexpr int kTileN = 256;       // token rows per tile (max MMA N)
+constexpr int kStagesB = 8;       // token tiles: 128 x 64 x 2 B = 16 KB each
+constexpr int kStagesW = 8;       // packed weight stages
+constexpr int kStagesA = 8;       // dequantised A stages in TMEM (32 columns each)
+constexpr int kTileN = 128;       // token rows per tile (MMA N <= 128)
 constexpr int kBBytes = kTileN * 128;
 constexpr int kTmemCols = 512;
+constexpr int kAccCols = 128;     // two accumulators: columns [0,128) and [128,256)
 constexpr int kAcol0 = 256;       // first TMEM column of the A ring
-constexpr int kGemmThreads = 384;
+constexpr int kGemmThreads = 512; // 16 warps, see the role map in the kernel
 
 struct GemmSmem {
   static constexpr int b_off = 0;
@@ -357,33 +360,49 @@ __device__ __forceinline__ void dequant_row(const uint8_t* stage, const GemmLayo
   }
   const uint16_t* sc = reinterpret_cast<const uint16_t*>(stage + 128 * L.code_row) + r * L.nbs;
   const uint8_t* zp = stage + 128 * L.code_row + 128 * L.nbs * 2 + r * L.nbs;
-  uint32_t ss[2], zz[2];
-#pragma unroll
-  for (int b = 0; b < 2; ++b) {
-    const int bb = b < L.nbs ? b : 0;
-    ss[b] = (uint32_t)sc[bb] * 0x00010001u;
-    if (ZPM == QMOE_ZP_UINT8) zz[b] = MAGIC | ((uint32_t)zp[bb] * 0x00010001u);
-    else zz[b] = MAGIC | ((1u << (BITS - 1)) * 0x00010001u);
+  // Registers 0..15 cover k 0..31 (block 0); registers 16..31 cover k 32..63,
+  // block 1 when B = 32 (nbs = 2), else still block 0.  Selecting the second
+  // block's scale / zero point once keeps every index below compile-time.
+  const int b1 = L.nbs > 1 ? 1 : 0;
+  const uint32_t ss0 = (uint32_t)sc[0] * 0x00010001u;
+  const uint32_t ss1 = (uint32_t)sc[b1] * 0x00010001u;
+  uint32_t zz0 = MAGIC | ((1u << (BITS - 1)) * 0x00010001u), zz1 = zz0;
+  if constexpr (ZPM == QMOE_ZP_UINT8) {
+    zz0 = MAGIC | ((uint32_t)zp[0] * 0x00010001u);
+    zz1 = MAGIC | ((uint32_t)zp[b1] * 0x00010001u);
   }
-  const int half = L.nbs > 1 ? 16 : 32;  // registers per scale block
 #pragma unroll
   for (int j = 0; j < 32; ++j) {
     uint32_t p;
     if constexpr (BITS == 4) p = (w[j >> 2] >> (4 * (j & 3))) & 0x000F000Fu;
     else if constexpr (BITS == 2) p = (w[j >> 3] >> (2 * (j & 7))) & 0x00030003u;
     else p = ((w[j >> 3] >> (2 * (j & 7))) & 0x00030003u) | (((w[4 + (j >> 4)] >> (j & 15)) & 0x00010001u) << 2);
-    uint32_t x = p | MAGIC;
-    const int b = j >= half ? 1 : 0;
-    if (ZPM == QMOE_ZP_OFFSET) {
-      x = sub2<BF16>(x, MAGIC);
-      x = sub2<BF16>(x, zoff2);
+    uint32_t x;
+    if constexpr (ZPM == QMOE_ZP_OFFSET) {
+      x = sub2<BF16>((p << 1) | Magic<BF16>::half, zoff2);   // exact c - z, half-integer z
     } else {
-      x = sub2<BF16>(x, zz[b]);
+      x = sub2<BF16>(p | MAGIC, j < 16 ? zz0 : zz1);
     }
-    v[j] = mul2<BF16>(x, ss[b]);
+    v[j] = mul2<BF16>(x, j < 16 ? ss0 : ss1);
   }
 }
 
+// Gated activations for the GEMM epilogue, from exp (CUDA's __expf):
+// silu(g) = g / (1 + e^-g); tanh(y) = 1 - 2 / (e^{2y} + 1).
+__device__ __forceinline__ float glu_fast(int act, float g, float u) {
+  if (act == QMOE_ACT_SWIGLU) return __fdividef(g, 1.f + __expf(-g)) * u;
+  const float y = 0.7978845608028654f * (g + 0.044715f * g * g * g);
+  const float t = 1.f - __fdividef(2.f, __expf(2.f * y) + 1.f);
+  return 0.5f * g * (1.f + t) * u;
+}
+
+// Warp roles (16 warps):
+//   0      TMA / bulk-copy producer (one thread)
+//   1      MMA issuer (one thread) and TMEM owner
+//   2..3   idle
+//   4..7   dequant group 0 (even k-steps), warp w owns TMEM lanes 32*(w%4)
+//   8..11  dequant group 1 (odd k-steps)
+//   12..15 epilogue (TMEM lanes 32*(w%4))
 template <int BITS, int ZPM, bool BF16, bool GLU>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmB, const GemmArgs a) {
@@ -401,9 +420,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   uint64_t* w_empty = w_full + kStagesW;
   uint64_t* a_full = w_empty + kStagesW;
   uint64_t* a_empty = a_full + kStagesA;
-  uint64_t* acc_full = a_empty + kStagesA;
-  uint64_t* acc_empty = acc_full + 1;
-  uint64_t* drain_bar = acc_empty + 1;
+  uint64_t* acc_full = a_empty + kStagesA;   // [2]
+  uint64_t* acc_empty = acc_full + 2;        // [2]
+  uint64_t* drain_bar = acc_empty + 2;
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain_bar + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
   volatile int* counters = abort_flag + 1;   // [0] = B steps consumed, [1] = W steps consumed
@@ -413,8 +432,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     for (int i = 0; i < kStagesB; ++i) { mbar_init(&b_full[i], 1); mbar_init(&b_empty[i], 1); }
     for (int i = 0; i < kStagesW; ++i) { mbar_init(&w_full[i], 1); mbar_init(&w_empty[i], 4); }
     for (int i = 0; i < kStagesA; ++i) { mbar_init(&a_full[i], 4); mbar_init(&a_empty[i], 1); }
-    mbar_init(acc_full, 1);
-    mbar_init(acc_empty, 4);
+    for (int i = 0; i < 2; ++i) { mbar_init(&acc_full[i], 1); mbar_init(&acc_empty[i], 4); }
     mbar_init(drain_bar, 1);
     *abort_flag = 0;
     counters[0] = counters[1] = 0;
@@ -443,16 +461,16 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       const uint8_t* wsrc = a.wq + (size_t)it.e * L.expert_bytes + (size_t)nt * L.tile_bytes;
       for (int ks = 0; ks < L.ksteps && ok; ++ks, ++kc) {
         const int sb = kc % kStagesB, sw = kc % kStagesW;
-        ok = wait_or_abort(&b_empty[sb], ((kc / kStagesB) & 1) ^ 1, a.wait, abort_flag);
-        if (!ok) break;
-        mbar_arrive_expect_tx(&b_full[sb], kBBytes);
-        tma_load_2d(bring + sb * kBBytes, &tmB, ks * 64, it.start, &b_full[sb]);
-        nb_issued = kc + 1;
         ok = wait_or_abort(&w_empty[sw], ((kc / kStagesW) & 1) ^ 1, a.wait, abort_flag);
         if (!ok) break;
         mbar_arrive_expect_tx(&w_full[sw], L.stage_bytes);
         bulk_g2s(wring + sw * wstage, wsrc + (size_t)ks * L.stage_bytes, L.stage_bytes, &w_full[sw]);
         nw_issued = kc + 1;
+        ok = wait_or_abort(&b_empty[sb], ((kc / kStagesB) & 1) ^ 1, a.wait, abort_flag);
+        if (!ok) break;
+        mbar_arrive_expect_tx(&b_full[sb], kBBytes);
+        tma_load_2d(bring + sb * kBBytes, &tmB, ks * 64, it.start, &b_full[sb]);
+        nb_issued = kc + 1;
       }
     }
     if (!ok) {
@@ -472,9 +490,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       const Item it = a.items[tile / L.ntiles];
       const int N = (it.rows + 15) & ~15;
       const uint32_t idesc = idesc_f16(BF16, 128, N);
-      ok = wait_or_abort(acc_empty, (tc & 1) ^ 1, a.wait, abort_flag);
+      const int ab = tc & 1;
+      ok = wait_or_abort(&acc_empty[ab], ((tc >> 1) & 1) ^ 1, a.wait, abort_flag);
       if (!ok) break;
       tc_fence_after();
+      const uint32_t dacc = tmem + ab * kAccCols;
       for (int ks = 0; ks < L.ksteps; ++ks, ++kc) {
         const int sb = kc % kStagesB, sa = kc % kStagesA;
         ok = wait_or_abort(&b_full[sb], (kc / kStagesB) & 1, a.wait, abort_flag);
@@ -484,31 +504,29 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         const uint32_t baddr = smem_u32(bring + sb * kBBytes);
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)
-          umma_ts(tmem, tmem + kAcol0 + sa * 32 + kk * 8, smem_desc_sw128(baddr + kk * 32), idesc,
+          umma_ts(dacc, tmem + kAcol0 + sa * 32 + kk * 8, smem_desc_sw128(baddr + kk * 32), idesc,
                   (ks | kk) != 0 ? 1u : 0u);
         tc_commit(&b_empty[sb]);
         tc_commit(&a_empty[sa]);
         counters[0] = kc + 1;
       }
-      if (ok) tc_commit(acc_full);
+      if (ok) tc_commit(&acc_full[ab]);
     }
     // All MMAs issued by this thread have completed once drain_bar flips.
     tc_commit(drain_bar);
     const WaitCfg drain{a.wait.status, kDrainWaitLimit};
     mbar_wait_bounded(drain_bar, 0, drain);
-  } else if (warp >= 4 && warp < 8) {
-    // ---------------- dequant: packed weights -> bf16/f16 pairs in TMEM ----------------
+  } else if (warp >= 4 && warp < 12) {
+    // ---------------- dequant: packed weights -> 16-bit pairs in TMEM ----------------
     const int q = warp & 3;
+    const int grp = (warp - 4) >> 2;      // 0: even k-steps, 1: odd k-steps
     const int r = q * 32 + lane;          // TMEM lane = weight row of the tile
-    uint32_t zoff2 = 0;
-    if (ZPM == QMOE_ZP_OFFSET) {
-      if (BF16) zoff2 = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(a.zp_offset)) * 0x00010001u;
-      else zoff2 = (uint32_t)__half_as_ushort(__float2half_rn(a.zp_offset)) * 0x00010001u;
-    }
+    const uint32_t zoff2 = ZPM == QMOE_ZP_OFFSET ? half_magic_offset<BF16>(a.zp_offset) : 0u;
     int kc = 0;
     bool ok = true;
     for (int tile = blockIdx.x; tile < total_tiles && ok; tile += gridDim.x) {
       for (int ks = 0; ks < L.ksteps; ++ks, ++kc) {
+        if ((kc & 1) != grp) continue;
         const int sw = kc % kStagesW, sa = kc % kStagesA;
         ok = wait_or_abort(&w_full[sw], (kc / kStagesW) & 1, a.wait, abort_flag);
         if (ok) ok = wait_or_abort(&a_empty[sa], ((kc / kStagesA) & 1) ^ 1, a.wait, abort_flag);
@@ -529,7 +547,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         }
       }
     }
-  } else if (warp >= 8) {
+  } else if (warp >= 12) {
     // ---------------- epilogue: TMEM -> GLU -> h (fc1) | weighted scatter (fc2) ----------------
     const int q = warp & 3;
     const int r = q * 32 + lane;
@@ -538,13 +556,22 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     for (int tile = blockIdx.x; tile < total_tiles && ok; tile += gridDim.x, ++tc) {
       const Item it = a.items[tile / L.ntiles];
       const int nt = tile % L.ntiles;
-      ok = wait_or_abort(acc_full, tc & 1, a.wait, abort_flag);
+      const int ab = tc & 1;
+      ok = wait_or_abort(&acc_full[ab], (tc >> 1) & 1, a.wait, abort_flag);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after();
       for (int c0 = 0; c0 < it.rows; c0 += 32) {
         uint32_t v[32];
-        TC_LD32(tmem + ((uint32_t)(q * 32) << 16) + c0, v);
+        TC_LD32(tmem + ((uint32_t)(q * 32) << 16) + ab * kAccCols + c0, v);
+        // route of column c0 + lane (one load per lane, broadcast below)
+        int my_tok = 0;
+        float my_w = 0.f;
+        if (!GLU && c0 + lane < it.rows) {
+          const int route = a.perm[it.start + c0 + lane];
+          my_tok = route / a.k;
+          my_w = a.w[route];
+        }
         tc_wait_ld();
         if (GLU) {
           const int n = nt * 64 + (r >> 1);
@@ -558,7 +585,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
               const int c = c0 + j;
               if (c < it.rows && n < a.N_out) {
                 const float g = odd ? other : mine, u = odd ? mine : other;
-                const float h = glu(a.act, g, u);
+                const float h = glu_fast(a.act, g, u);
                 const size_t o = (size_t)(it.start + c) * a.N_out + n;
                 if (BF16) static_cast<__nv_bfloat16*>(a.hout)[o] = __float2bfloat16_rn(h);
                 else static_cast<__half*>(a.hout)[o] = __float2half_rn(h);
@@ -569,19 +596,16 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           const int m = nt * 128 + r;
 #pragma unroll
           for (int j = 0; j < 32; ++j) {
-            const int c = c0 + j;
-            if (c < it.rows) {
-              const int route = a.perm[it.start + c];
-              const float wr = a.w[route];
-              if (m < a.N_out)
-                red_add_f32(a.out_acc + (size_t)(route / a.k) * a.N_out + m, wr * __uint_as_float(v[j]));
-            }
+            const int tok = __shfl_sync(0xffffffffu, my_tok, j);
+            const float wr = __shfl_sync(0xffffffffu, my_w, j);
+            if (c0 + j < it.rows && m < a.N_out)
+              red_add_f32(a.out_acc + (size_t)tok * a.N_out + m, wr * __uint_as_float(v[j]));
           }
         }
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(acc_empty);
+      if (lane == 0) mbar_arrive(&acc_empty[ab]);
     }
   }
   pdl_launch_dependents();
