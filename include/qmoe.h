@@ -211,6 +211,46 @@ qmoe_status qmoe_poll_device_status(qmoe_layer* layer);
  * 2^24 polls).  Tests lower it so an injected stall ends quickly. */
 qmoe_status qmoe_set_wait_limit(qmoe_layer* layer, int64_t iterations);
 
+/*
+ * Size of the library's static scratch array used by qmoe_forward_noalloc.
+ */
+#define QMOE_NOALLOC_SCRATCH_BYTES (4u << 20)
+
+/*
+ * qmoe_forward without any allocation.  (No counterpart in the paper: this
+ * is a convenience of this library.)
+ *
+ * Who needs it: callers that may not call cudaMalloc at the moment they run
+ * the layer -- e.g. code executing while a framework captures a CUDA graph in
+ * a capture mode that forbids allocation, runtimes whose caching allocator
+ * owns all device memory, or embedded deployments with a fixed memory plan.
+ * qmoe_forward would allocate its workspace on first use (or when num_tokens
+ * outgrows qmoe_reserve); this entry point instead uses one file-scope device
+ * array of QMOE_NOALLOC_SCRATCH_BYTES that every GPU loading the library
+ * holds until the process exits.  It never calls cudaMalloc, cudaFree or any
+ * allocating library routine.
+ *
+ * Arguments and layouts are those of qmoe_forward (x_dev, logits_dev,
+ * out_dev are device pointers owned by the caller; x and out 16-byte
+ * aligned).  The layer must already be prepacked.  Only the weight-streaming
+ * decode kernels run (no grouped GEMM), so results equal qmoe_forward's
+ * decode path.  Returns UNSUPPORTED (with the byte count in
+ * qmoe_last_error) when num_tokens needs more scratch than the array holds;
+ * use qmoe_forward for such sizes.
+ *
+ * Set-up: the first call on a device, with that device current, looks up the
+ * array's device address (cudaGetSymbolAddress) and caches it; make that
+ * first call before any stream capture.  All calls share the one array and it
+ * keeps the last call's contents (each call clears its status word itself):
+ * calls that overlap on the GPU (other streams, other layers) race and must
+ * be serialised by the caller.  Bounded-wait timeouts of this entry point are
+ * recorded in the scratch array, not in the layer (qmoe_poll_device_status
+ * does not see them); routing of such a call is not kept for
+ * qmoe_get_routing.
+ */
+qmoe_status qmoe_forward_noalloc(qmoe_layer* layer, const void* x_dev, const float* logits_dev,
+                                 void* out_dev, int64_t num_tokens, void* stream);
+
 /* Test hook for failure detection without a GPU fault: while enabled, every
  * warp of the decode projection kernels arms its first copy-stage barrier but
  * never issues that copy, so its bounded wait runs out; the kernel records

@@ -43,6 +43,7 @@ _SIGS = {
     "qmoe_poll_device_status": (_i, [_p]),
     "qmoe_set_wait_limit": (_i, [_p, _i64]),
     "qmoe_debug_inject_stall": (_i, [_p, _i]),
+    "qmoe_forward_noalloc": (_i, [_p, _p, _p, _p, _i64, _p]),
     "qmoe_last_error": (ctypes.c_char_p, [_p]),
     "qmoe_status_string": (ctypes.c_char_p, [_i]),
     "qmoe_destroy": (None, [_p]),
@@ -112,6 +113,12 @@ def qmoe_forward(layer, x, logits, out, num_tokens, stream):
 def qmoe_forward_host(layer, x_host, logits_host, out_host, num_tokens, stream):
     return load().qmoe_forward_host(layer, x_host, logits_host, out_host, int(num_tokens),
                                     stream or None)
+
+
+def qmoe_forward_noalloc(layer, x, logits, out, num_tokens, stream):
+    """The forward for callers that may not allocate device memory: its
+    workspace is the library's static scratch array (see include/qmoe.h)."""
+    return load().qmoe_forward_noalloc(layer, x, logits, out, int(num_tokens), stream or None)
 
 
 def qmoe_get_routing(layer, ids, weights, perm, offsets, stream):

@@ -677,3 +677,191 @@ void qmoe_destroy(qmoe_layer* l) {
 
 }  // extern "C"
 
+// ----------------------------------------------------------------------------
+// Forward without allocation: the workspace lives in one static device array.
+//
+// For callers that may not allocate device memory when they run the layer
+// (allocation-free graph capture, a framework allocator that owns the whole
+// device, fixed memory plans).  See qmoe_forward_noalloc in qmoe.h.
+// ----------------------------------------------------------------------------
+namespace {
+
+// Every GPU that loads the library holds this array until the process exits.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[QMOE_NOALLOC_SCRATCH_BYTES];
+
+constexpr int kMaxDevices = 256;
+std::mutex g_noalloc_mu;
+void* g_noalloc_ptr[kMaxDevices] = {};
+
+// Device address of g_noalloc_scratch on the current device.  In host code
+// the array's name is only a host-side stand-in, so the address is looked up
+// once per device (with that device current) and cached.
+cudaError_t noalloc_scratch(void** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (!g_noalloc_ptr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess) return e;
+    g_noalloc_ptr[dev] = p;
+  }
+  *out = g_noalloc_ptr[dev];
+  return cudaSuccess;
+}
+
+struct NoAllocPlan {
+  size_t ids, w, counts, offsets, perm, pos, n_items, items0, items1, hbuf, ybuf, status, total;
+};
+
+size_t up256(size_t v) { return (v + 255) & ~size_t(255); }
+
+NoAllocPlan noalloc_plan(const qmoe_layer* l, int64_t T, int cap0) {
+  const size_t R = (size_t)T * l->k;
+  NoAllocPlan p;
+  size_t o = 0;
+  auto take = [&](size_t bytes) { const size_t at = o; o = up256(o + bytes); return at; };
+  p.ids = take(R * sizeof(int));
+  p.w = take(R * sizeof(float));
+  p.counts = take((size_t)l->E * sizeof(int));
+  p.offsets = take(((size_t)l->E + 1) * sizeof(int));
+  p.perm = take(R * sizeof(int));
+  p.pos = take(R * sizeof(int));
+  p.n_items = take(2 * sizeof(int));
+  p.items0 = take((size_t)cap0 * sizeof(Item));
+  p.items1 = take(sizeof(Item));
+  p.hbuf = take(R * l->I * (size_t)l->dsize);
+  p.ybuf = take(R * l->H * sizeof(float));
+  p.status = take(sizeof(int));
+  p.total = o;
+  return p;
+}
+
+}  // namespace
+
+extern "C" qmoe_status qmoe_forward_noalloc(qmoe_layer* l, const void* x, const float* logits,
+                                            void* out, int64_t T, void* stream) {
+  if (!l) return QMOE_ERR_INVALID_ARG;
+  if (T < 0) return fail(l, QMOE_ERR_INVALID_ARG, "num_tokens < 0");
+  if (T == 0) return QMOE_OK;
+  if (!x || !logits || !out) return fail(l, QMOE_ERR_INVALID_ARG, "null x / logits / out");
+  if ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(out)) & 15)
+    return fail(l, QMOE_ERR_INVALID_ARG, "x and out must be 16-byte aligned");
+  if (!l->proj[0].ready || !l->proj[1].ready)
+    return fail(l, QMOE_ERR_STATE, "prepack fc1 and fc2 before qmoe_forward_noalloc");
+  if (T * l->k > INT_MAX / 8) return fail(l, QMOE_ERR_INVALID_ARG, "num_tokens too large");
+  int tb0, tb1;
+  item_heights(l, T, &tb0, &tb1);
+  const int64_t cap0 = items_cap(l, 0, T, tb0);
+  const NoAllocPlan plan = noalloc_plan(l, T, (int)cap0);
+  if (plan.total > (size_t)QMOE_NOALLOC_SCRATCH_BYTES)
+    return fail(l, QMOE_ERR_UNSUPPORTED,
+                "qmoe_forward_noalloc: " + std::to_string(T) + " tokens need " +
+                    std::to_string(plan.total) + " bytes of scratch, more than the " +
+                    std::to_string((size_t)QMOE_NOALLOC_SCRATCH_BYTES) +
+                    "-byte static array; use qmoe_forward");
+  void* base = nullptr;
+  QMOE_CUDA(l, noalloc_scratch(&base), "look up the static scratch array");
+  unsigned char* sb = static_cast<unsigned char*>(base);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int* status = reinterpret_cast<int*>(sb + plan.status);
+  // The array keeps the previous call's contents: the status word must start at zero.
+  QMOE_CUDA(l, cudaMemsetAsync(status, 0, sizeof(int), s), "clear status");
+  int* ids = reinterpret_cast<int*>(sb + plan.ids);
+  float* w = reinterpret_cast<float*>(sb + plan.w);
+  int* perm = reinterpret_cast<int*>(sb + plan.perm);
+  int* pos = reinterpret_cast<int*>(sb + plan.pos);
+  int* n_items = reinterpret_cast<int*>(sb + plan.n_items);
+  Item* items0 = reinterpret_cast<Item*>(sb + plan.items0);
+  void* hbuf = sb + plan.hbuf;
+  float* ybuf = reinterpret_cast<float*>(sb + plan.ybuf);
+
+  RouteArgs ra{};
+  ra.logits = logits;
+  ra.T = (int)T;
+  ra.E = l->E;
+  ra.k = l->k;
+  ra.normalize = l->normalize;
+  ra.ids = ids;
+  ra.w = w;
+  ra.counts = reinterpret_cast<int*>(sb + plan.counts);
+  ra.offsets = reinterpret_cast<int*>(sb + plan.offsets);
+  ra.perm = perm;
+  ra.pos = pos;
+  ra.items[0] = items0;
+  ra.items[1] = reinterpret_cast<Item*>(sb + plan.items1);
+  ra.n_items = n_items;
+  ra.tb[0] = tb0;
+  ra.tb[1] = tb1;
+  ra.threshold = INT_MAX;  // decode kernels only
+  ra.cap[0] = (int)cap0;
+  ra.cap[1] = 1;
+  QMOE_CUDA(l, launch_route_group(ra, T <= 64, s), "launch routing");
+
+  const WaitCfg wait{status, l->wait_limit};
+  for (int f = 0; f < 2; ++f) {
+    const Proj& p = l->proj[f];
+    if (l->dtype == QMOE_F32) {
+      SimtArgs sa{};
+      sa.codes = p.codes;
+      sa.scales = p.scales;
+      sa.zp = p.zp;
+      sa.bits = p.bits;
+      sa.B = l->B;
+      sa.K = p.K;
+      sa.N_out = f == 0 ? l->I : l->H;
+      sa.I_or_0 = f == 0 ? l->I : 0;
+      sa.zp_bytes_row = p.zp_row;
+      sa.items = items0;
+      sa.n_items = n_items;
+      sa.max_items = (int)cap0;
+      sa.src = f == 0 ? x : hbuf;
+      sa.perm = perm;
+      sa.k = l->k;
+      sa.fc = f + 1;
+      sa.dtype = l->dtype;
+      sa.act = l->act;
+      sa.zp_mode = l->zp_mode;
+      sa.zp_offset = l->zp_offset;
+      sa.dst = f == 0 ? hbuf : (void*)ybuf;
+      sa.E = l->E;
+      QMOE_CUDA(l, launch_simt(sa, s), "launch SIMT projection");
+    } else {
+      DecodeArgs da{};
+      da.wpk = p.dec;
+      da.L = p.L;
+      da.K = p.K;
+      da.N_out = f == 0 ? l->I : l->H;
+      da.items = items0;
+      da.n_items = n_items;
+      da.max_items = (int)cap0;
+      da.src = f == 0 ? x : hbuf;
+      da.perm = perm;
+      da.k = l->k;
+      da.fc = f + 1;
+      da.ng = tb0 / 8;
+      da.dst = f == 0 ? hbuf : (void*)ybuf;
+      da.act = l->act;
+      da.zp_mode = l->zp_mode;
+      da.zp_offset = l->zp_offset;
+      da.bf16 = l->dtype == QMOE_BF16;
+      da.wait = wait;
+      da.pdl = 1;
+      QMOE_CUDA(l, launch_decode_mma(da, s), "launch decode projection");
+    }
+  }
+  FinalizeArgs fa{};
+  fa.y = ybuf;
+  fa.w = w;
+  fa.pos = pos;
+  fa.out = out;
+  fa.T = (int)T;
+  fa.H = l->H;
+  fa.k = l->k;
+  fa.dtype = l->dtype;
+  fa.pdl = 1;
+  QMOE_CUDA(l, launch_finalize(fa, s), "launch combine");
+  return QMOE_OK;
+}
