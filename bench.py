@@ -42,6 +42,8 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--mode", default="graph", choices=["graph", "eager"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--gemm-min-rows", type=int, default=None,
+                    help="experts with more rows take the tensor-core grouped GEMM")
     return ap.parse_args()
 
 
@@ -224,6 +226,8 @@ def run_ours(args):
     cfg = CONFIGS[args.workload]
     inp = make_inputs(cfg)
     layer = q.QMoELayer.from_config(cfg)
+    if args.gemm_min_rows is not None:
+        layer.set_gemm_min_rows(args.gemm_min_rows)
     layer.reserve(cfg.T)
     x, logits = q.load_inputs(layer, inp, device=dev)
     out = torch.empty_like(x)

@@ -74,10 +74,10 @@ struct qmoe_layer {
   void* x_stage = nullptr;
   float* logits_stage = nullptr;
   void* out_stage = nullptr;
-  void* xg = nullptr;          // x gathered in route order (grouped GEMM B operand)
+  uint8_t* xt = nullptr;       // x of GEMM-class items, tiled token layout (fc1 B operand)
+  uint8_t* ht = nullptr;       // h of GEMM-class items, tiled token layout (fc2 B operand)
   float* out_acc = nullptr;    // fp32 [T, H] combine accumulator (mixed forwards)
-  CUtensorMap map_x{}, map_h{};
-  bool maps_ok = false;
+  bool tiles_ok = false;
   int num_sms = 0;
 
   int64_t last_T = 0;
@@ -130,7 +130,7 @@ cudaError_t dalloc(T** p, size_t bytes) {
 void free_workspace(qmoe_layer* l) {
   void* bufs[] = {l->ids, l->w, l->counts, l->offsets, l->perm, l->pos, l->n_items, l->items[0],
                   l->items[1], l->hbuf, l->ybuf, l->status, l->x_stage, l->logits_stage,
-                  l->out_stage, l->xg, l->out_acc};
+                  l->out_stage, l->xt, l->ht, l->out_acc};
   for (void* b : bufs)
     if (b) cudaFree(b);
   l->ids = nullptr;
@@ -143,9 +143,10 @@ void free_workspace(qmoe_layer* l) {
   l->x_stage = nullptr;
   l->logits_stage = nullptr;
   l->out_stage = nullptr;
-  l->xg = nullptr;
+  l->xt = nullptr;
+  l->ht = nullptr;
   l->out_acc = nullptr;
-  l->maps_ok = false;
+  l->tiles_ok = false;
   l->cap_T = 0;
 }
 
@@ -200,12 +201,13 @@ qmoe_status ensure_workspace(qmoe_layer* l, int64_t T) {
   QMOE_CUDA(l, dalloc(&l->logits_stage, (size_t)T * l->E * sizeof(float)), "allocate workspace");
   QMOE_CUDA(l, dalloc(&l->out_stage, (size_t)T * l->H * ds), "allocate workspace");
   if (l->dtype != QMOE_F32) {
-    QMOE_CUDA(l, dalloc(&l->xg, (size_t)R * l->H * ds), "allocate workspace");
+    // GEMM-class items hold at most 128 rows each: one 128-row block per item.
+    const size_t blocks = (size_t)items_cap(l, 1, T, 128);
+    QMOE_CUDA(l, dalloc(&l->xt, blocks * (size_t)((l->H + 63) / 64) * kTokTileBytes), "allocate workspace");
+    QMOE_CUDA(l, dalloc(&l->ht, blocks * (size_t)((l->I + 63) / 64) * kTokTileBytes), "allocate workspace");
     QMOE_CUDA(l, dalloc(&l->out_acc, (size_t)T * l->H * sizeof(float)), "allocate workspace");
     QMOE_CUDA(l, cudaMemset(l->out_acc, 0, (size_t)T * l->H * sizeof(float)), "clear accumulator");
-    const bool bf16 = l->dtype == QMOE_BF16;
-    l->maps_ok = make_token_map(&l->map_x, l->xg, (int)R, l->H, bf16) == cudaSuccess &&
-                 make_token_map(&l->map_h, l->hbuf, (int)R, l->I, bf16) == cudaSuccess;
+    l->tiles_ok = true;
   }
   if (l->num_sms == 0) {
     int dev = 0;
@@ -434,7 +436,7 @@ qmoe_status qmoe_forward(qmoe_layer* l, const void* x, const float* logits, void
   const WaitCfg wait{l->status, l->wait_limit};
   // An expert can receive at most T rows: only when T exceeds the threshold
   // can the grouped-GEMM class be non-empty.
-  const bool gemm = l->dtype != QMOE_F32 && l->maps_ok && T > l->gemm_min_rows;
+  const bool gemm = l->dtype != QMOE_F32 && l->tiles_ok && T > l->gemm_min_rows;
   const int threshold = gemm ? l->gemm_min_rows : INT_MAX;
 
   trace(l, QMOE_TRACE_BEGIN, s);
@@ -464,7 +466,9 @@ qmoe_status qmoe_forward(qmoe_layer* l, const void* x, const float* logits, void
     if ((int64_t)l->E * per < ra.cap[0]) ra.cap[0] = (int)((int64_t)l->E * per);
   }
   QMOE_CUDA(l, launch_route_group(ra, T <= 64, s), "launch routing");
-  if (gemm) QMOE_CUDA(l, launch_gather(x, l->perm, l->k, R, l->H, l->xg, s), "launch gather");
+  if (gemm)
+    QMOE_CUDA(l, launch_gather_tiles(x, l->perm, l->k, l->H, l->items[1], l->n_items + 1, ra.cap[1], l->xt, s),
+              "launch gather");
   trace(l, QMOE_TRACE_ROUTED, s);
 
   for (int f = 0; f < 2; ++f) {
@@ -534,14 +538,16 @@ qmoe_status qmoe_forward(qmoe_layer* l, const void* x, const float* logits, void
         ga.zp_mode = l->zp_mode;
         ga.bf16 = l->dtype == QMOE_BF16;
         ga.zp_offset = l->zp_offset;
-        ga.hout = l->hbuf;
+        ga.btiles = f == 0 ? l->xt : l->ht;
+        ga.htiles = l->ht;
+        ga.h_ksteps = (l->I + 63) / 64;
         ga.out_acc = l->out_acc;
         ga.perm = l->perm;
         ga.w = l->w;
         ga.k = l->k;
         ga.N_out = f == 0 ? l->I : l->H;
         ga.wait = wait;
-        QMOE_CUDA(l, launch_gemm(f == 0 ? l->map_x : l->map_h, ga, s), "launch grouped GEMM");
+        QMOE_CUDA(l, launch_gemm(ga, s), "launch grouped GEMM");
       }
     }
     trace(l, f == 0 ? QMOE_TRACE_FC1 : QMOE_TRACE_FC2, s);

@@ -12,22 +12,22 @@
 //   D[128 weight rows, N tokens] += A[128 rows, 64 k] * B[N tokens, 64 k]^T
 //   * A = dequantised weights, written by CUDA-core warps straight into
 //     tensor memory (tcgen05.st, one thread per weight row, 64 k per step;
-//     two warp groups take alternate k-steps): the dequant costs no
+//     three warp groups take k-steps in turn): the dequant costs no
 //     shared-memory bandwidth, which the B stream needs;
-//   * B = the routed token rows (x gathered in route order for fc1, h for
-//     fc2), TMA tiles of 128 x 64 (128-byte swizzle) in a shared ring;
+//   * B = the routed token rows (x gathered per work item for fc1, h written
+//     by fc1's epilogue for fc2), pre-tiled in the MMA's K-major 128-byte
+//     swizzle so each 128 x 64 operand tile is one contiguous 16 KB bulk
+//     copy (strided 2-D tensor loads of the same tile were ~7x slower to
+//     arrive);
 //   * tcgen05.mma.cta_group::1.kind::f16, fp32 accumulators in TMEM, two of
 //     128 columns so the epilogue of one tile overlaps the next tile's MMAs;
 //     N = the tile's rows rounded up to 16 (no padded work);
-//   * warp roles: 0 = TMA / bulk-copy producer, 1 = MMA issuer (one thread)
-//     and TMEM owner, 4..11 = dequant, 12..15 = epilogue (tcgen05.ld);
+//   * warp roles: 0 = bulk-copy producer, 1 = MMA issuer (one thread) and
+//     TMEM owner, then the dequant groups, then 4 epilogue warps (tcgen05.ld);
 //   * persistent CTAs stride over the (item, weight-tile) list; fc1 rows are
 //     interleaved gate/up so the GLU pairs sit in adjacent TMEM lanes;
 //   * every wait is bounded; a timeout aborts all roles, drains in-flight
 //     copies and MMAs, frees TMEM and records QMOE_ERR_TIMEOUT.
-#include <cuda.h>
-#include <cudaTypedefs.h>
-
 #include "qmoe_prefill.cuh"
 
 namespace qmoe {
@@ -142,39 +142,66 @@ cudaError_t launch_repack_gemm(const GemmRepackArgs& a, cudaStream_t s) {
 }
 
 // ----------------------------------------------------------------------------
-// Gather of x into route order for the fc1 B operand, and the combine of the
-// fp32 accumulator.
+// Gather of x into the tiled token layout (fc1 B operand), and the combine of
+// the fp32 accumulator.
 // ----------------------------------------------------------------------------
-__global__ void __launch_bounds__(256) gather_rows_kernel(const void* __restrict__ x, const int* __restrict__ perm,
-                                                          int k, int R, int H, void* __restrict__ xg) {
+// One CTA per GEMM-class item: rows c < rows of the item, 16-byte chunks of
+// 8 values; chunks past H (K padding up to 64) are written as zeros.  Rows
+// past the item's count are left as they are: they only feed token columns
+// that the epilogue never stores.
+__global__ void __launch_bounds__(256) gather_tiles_kernel(const void* __restrict__ x, const int* __restrict__ perm,
+                                                           int k, int H, const Item* __restrict__ items,
+                                                           const int* __restrict__ n_items, uint8_t* __restrict__ xt) {
   pdl_wait();
-  const int vec = H / 8;  // 16-byte vectors per row
-  const size_t n = (size_t)R * vec;
+  if ((int)blockIdx.x >= *n_items) return;
+  const Item it = items[blockIdx.x];
+  const int ksteps = (H + 63) / 64;
+  const int cpr = ksteps * 8;                 // chunks per row (padded)
+  const int hv = H / 8;                       // real chunks per row
   const uint4* src = static_cast<const uint4*>(x);
-  uint4* dst = static_cast<uint4*>(xg);
-  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x) {
-    const int p = (int)(i / vec), v = (int)(i % vec);
-    const int t = perm[p] / k;
-    dst[i] = src[(size_t)t * vec + v];
+  const int n = it.rows * cpr;
+  constexpr int U = 4;
+  for (int base = threadIdx.x; base < n; base += U * blockDim.x) {
+    uint4 v[U];
+    int cc[U], ch[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int i = base + u * blockDim.x;
+      cc[u] = -1;
+      if (i < n) {
+        cc[u] = i / cpr;
+        ch[u] = i % cpr;
+        v[u] = make_uint4(0u, 0u, 0u, 0u);
+        if (ch[u] < hv) {
+          const int t = perm[it.start + cc[u]] / k;
+          v[u] = src[(size_t)t * hv + ch[u]];
+        }
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      if (cc[u] < 0) continue;
+      uint8_t* dst = xt + tok_tile_offset(blockIdx.x, ksteps, ch[u] >> 3) + cc[u] * 128 +
+                     (((ch[u] & 7) ^ (cc[u] & 7)) << 4);
+      *reinterpret_cast<uint4*>(dst) = v[u];
+    }
   }
   pdl_launch_dependents();
 }
 
-cudaError_t launch_gather(const void* x, const int* perm, int k, int R, int H, void* xg, cudaStream_t s) {
-  const size_t n = (size_t)R * (H / 8);
-  int grid = (int)((n + 255) / 256);
-  if (grid > 152 * 16) grid = 152 * 16;
-  if (grid < 1) grid = 1;
+cudaError_t launch_gather_tiles(const void* x, const int* perm, int k, int H, const Item* items,
+                                const int* n_items, int max_items, uint8_t* xt, cudaStream_t s) {
+  if (max_items <= 0) return cudaSuccess;
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.gridDim = dim3(grid);
+  cfg.gridDim = dim3(max_items);
   cfg.blockDim = dim3(256);
   cfg.stream = s;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, gather_rows_kernel, x, perm, k, R, H, xg);
+  return cudaLaunchKernelEx(&cfg, gather_tiles_kernel, x, perm, k, H, items, n_items, xt);
 }
 
 template <int DT>
@@ -234,23 +261,26 @@ __device__ __forceinline__ void tc_commit(uint64_t* bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
                : "memory");
 }
-// D[tmem] (+)= A[tmem] * B[smem desc]
-__device__ __forceinline__ void umma_ts(uint32_t d, uint32_t a, uint64_t bdesc, uint32_t idesc, uint32_t acc) {
+// Four K=16 MMAs of one 64-deep k-step from one asm block: A columns a0 + 8j,
+// B descriptor start advanced 32 bytes per MMA; the first accumulates into D
+// only when `acc` is set, the rest always do.
+__device__ __forceinline__ void umma_ts_x4(uint32_t d, uint32_t a0, uint64_t b0, uint32_t idesc, uint32_t acc) {
+  const uint64_t b1 = b0 + 2, b2 = b0 + 4, b3 = b0 + 6;   // +32 bytes in 16-byte units
   asm volatile(
-      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d),
-      "r"(a), "l"(bdesc), "r"(idesc), "r"(acc)
+      "{\n\t.reg .pred p0, p1;\n\t"
+      "setp.ne.b32 p0, %9, 0;\n\t"
+      "setp.eq.b32 p1, %9, %9;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %5, %8, p0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%2], %6, %8, p1;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%3], %7, %8, p1;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%4], %10, %8, p1;\n\t}" ::"r"(d),
+      "r"(a0), "r"(a0 + 8), "r"(a0 + 16), "r"(a0 + 24), "l"(b0), "l"(b1), "l"(b2), "r"(idesc), "r"(acc),
+      "l"(b3)
       : "memory");
 }
+
 __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
-}
-__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
-          smem_u32(dst)),
-      "l"(map), "r"(x), "r"(y), "r"(smem_u32(bar))
-      : "memory");
 }
 __device__ __forceinline__ void red_add_f32(float* p, float v) {
   asm volatile("red.global.add.f32 [%0], %1;" ::"l"(p), "f"(v) : "memory");
@@ -316,25 +346,53 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, co
   return false;
 }
 
+// The same with non-blocking polls: for the MMA-issuing thread, whose loop
+// paces the whole pipeline (a parked poll costs ~250 cycles even when the
+// phase has already completed).
+__device__ __forceinline__ bool spin_or_abort(uint64_t* bar, uint32_t parity, const WaitCfg& w,
+                                              volatile int* abort_flag) {
+  const long long limit = w.limit * 64;
+  for (long long i = 0; i < limit; ++i) {
+    if (mbar_test_wait(bar, parity)) return true;
+    if ((i & 255) == 255 && *abort_flag) return false;
+  }
+  atomicExch(w.status, DEV_TIMEOUT);
+  *abort_flag = 1;
+  return false;
+}
+
 // ----------------------------------------------------------------------------
 // The grouped GEMM kernel
 // ----------------------------------------------------------------------------
 constexpr int kStagesB = 8;       // token tiles: 128 x 64 x 2 B = 16 KB each
 constexpr int kStagesW = 8;       // packed weight stages
 constexpr int kStagesA = 8;       // dequantised A stages in TMEM (32 columns each)
+// One commit per k-step frees both the token stage and the A stage of that
+// step (step_empty), so both rings have the same depth.
+static_assert(kStagesA == kStagesB, "B and A rings advance together");
 constexpr int kTileN = 128;       // token rows per tile (MMA N <= 128)
 constexpr int kBBytes = kTileN * 128;
 constexpr int kTmemCols = 512;
 constexpr int kAccCols = 128;     // two accumulators: columns [0,128) and [128,256)
 constexpr int kAcol0 = 256;       // first TMEM column of the A ring
-constexpr int kGemmThreads = 512; // 16 warps, see the role map in the kernel
+constexpr int kDeqGroups = 3;     // dequant warp groups (4 warps each), k-step kc -> group kc % 3
+constexpr int kEpiWarp0 = 4 + 4 * kDeqGroups;
+constexpr int kGemmThreads = (kEpiWarp0 + 4) * 32;  // see the role map in the kernel
+constexpr int kEpiPitch = 36;     // fp32 words per row of an epilogue transpose tile (pad: banks)
+constexpr int kEpiBytes = 4 * 32 * kEpiPitch * 4;   // one 32x32 tile per epilogue warp
 
 struct GemmSmem {
   static constexpr int b_off = 0;
   static constexpr int w_off = kStagesB * kBBytes;
-  __host__ __device__ static int bar_off(int wstage) { return w_off + kStagesW * ((wstage + 127) / 128 * 128); }
+  __host__ __device__ static int epi_off(int wstage) { return w_off + kStagesW * ((wstage + 127) / 128 * 128); }
+  __host__ __device__ static int bar_off(int wstage) { return epi_off(wstage) + kEpiBytes; }
   __host__ __device__ static int total(int wstage) { return bar_off(wstage) + 1024; }
 };
+
+__device__ __forceinline__ void red_add_v4_f32(float* p, float a, float b, float c, float d) {
+  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(a), "f"(b), "f"(c), "f"(d)
+               : "memory");
+}
 
 template <int BITS, int ZPM, bool BF16>
 __device__ __forceinline__ void dequant_row(const uint8_t* stage, const GemmLayout& L, int r, uint32_t zoff2,
@@ -396,16 +454,16 @@ __device__ __forceinline__ float glu_fast(int act, float g, float u) {
   return 0.5f * g * (1.f + t) * u;
 }
 
-// Warp roles (16 warps):
+// Warp roles (8 + 4 * kDeqGroups warps):
 //   0      TMA / bulk-copy producer (one thread)
 //   1      MMA issuer (one thread) and TMEM owner
 //   2..3   idle
-//   4..7   dequant group 0 (even k-steps), warp w owns TMEM lanes 32*(w%4)
-//   8..11  dequant group 1 (odd k-steps)
-//   12..15 epilogue (TMEM lanes 32*(w%4))
+//   4 ..   dequant groups of 4 warps; group g takes k-steps kc % kDeqGroups == g,
+//          warp w owns TMEM lanes 32*(w%4)
+//   last 4 epilogue (TMEM lanes 32*(w%4))
 template <int BITS, int ZPM, bool BF16, bool GLU>
 __global__ void __launch_bounds__(kGemmThreads, 1)
-    gemm_kernel(const __grid_constant__ CUtensorMap tmB, const GemmArgs a) {
+    gemm_kernel(const GemmArgs a) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   // 1024-byte alignment for the swizzled B tiles
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -415,12 +473,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   uint8_t* wring = smem + GemmSmem::w_off;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + GemmSmem::bar_off(wstage));
   uint64_t* b_full = bars;
-  uint64_t* b_empty = b_full + kStagesB;
+  uint64_t* b_empty = b_full + kStagesB;      // step_empty: B and A stage of a k-step
   uint64_t* w_full = b_empty + kStagesB;
   uint64_t* w_empty = w_full + kStagesW;
   uint64_t* a_full = w_empty + kStagesW;
-  uint64_t* a_empty = a_full + kStagesA;
-  uint64_t* acc_full = a_empty + kStagesA;   // [2]
+  uint64_t* acc_full = a_full + kStagesA;    // [2]
   uint64_t* acc_empty = acc_full + 2;        // [2]
   uint64_t* drain_bar = acc_empty + 2;
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain_bar + 1);
@@ -431,7 +488,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < kStagesB; ++i) { mbar_init(&b_full[i], 1); mbar_init(&b_empty[i], 1); }
     for (int i = 0; i < kStagesW; ++i) { mbar_init(&w_full[i], 1); mbar_init(&w_empty[i], 4); }
-    for (int i = 0; i < kStagesA; ++i) { mbar_init(&a_full[i], 4); mbar_init(&a_empty[i], 1); }
+    for (int i = 0; i < kStagesA; ++i) mbar_init(&a_full[i], 4);
     for (int i = 0; i < 2; ++i) { mbar_init(&acc_full[i], 1); mbar_init(&acc_empty[i], 4); }
     mbar_init(drain_bar, 1);
     *abort_flag = 0;
@@ -459,17 +516,25 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       const Item it = a.items[tile / L.ntiles];
       const int nt = tile % L.ntiles;
       const uint8_t* wsrc = a.wq + (size_t)it.e * L.expert_bytes + (size_t)nt * L.tile_bytes;
+      // The weight tiles of one token tile run on neighbouring CTAs at the
+      // same time; starting each at a different k-step spreads their reads
+      // of the shared token tile over the L2 instead of hitting the same
+      // lines together.  The MMA sums the k-steps in any order.
+      const int rot = (int)(((long long)nt * L.ksteps) / L.ntiles);
       for (int ks = 0; ks < L.ksteps && ok; ++ks, ++kc) {
         const int sb = kc % kStagesB, sw = kc % kStagesW;
+        int kr = ks + rot;
+        if (kr >= L.ksteps) kr -= L.ksteps;
         ok = wait_or_abort(&w_empty[sw], ((kc / kStagesW) & 1) ^ 1, a.wait, abort_flag);
         if (!ok) break;
         mbar_arrive_expect_tx(&w_full[sw], L.stage_bytes);
-        bulk_g2s(wring + sw * wstage, wsrc + (size_t)ks * L.stage_bytes, L.stage_bytes, &w_full[sw]);
+        bulk_g2s(wring + sw * wstage, wsrc + (size_t)kr * L.stage_bytes, L.stage_bytes, &w_full[sw]);
         nw_issued = kc + 1;
         ok = wait_or_abort(&b_empty[sb], ((kc / kStagesB) & 1) ^ 1, a.wait, abort_flag);
         if (!ok) break;
         mbar_arrive_expect_tx(&b_full[sb], kBBytes);
-        tma_load_2d(bring + sb * kBBytes, &tmB, ks * 64, it.start, &b_full[sb]);
+        bulk_g2s(bring + sb * kBBytes, a.btiles + tok_tile_offset(tile / L.ntiles, L.ksteps, kr), kBBytes,
+                 &b_full[sb]);
         nb_issued = kc + 1;
       }
     }
@@ -491,45 +556,64 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       const int N = (it.rows + 15) & ~15;
       const uint32_t idesc = idesc_f16(BF16, 128, N);
       const int ab = tc & 1;
-      ok = wait_or_abort(&acc_empty[ab], ((tc >> 1) & 1) ^ 1, a.wait, abort_flag);
+      ok = spin_or_abort(&acc_empty[ab], ((tc >> 1) & 1) ^ 1, a.wait, abort_flag);
       if (!ok) break;
       tc_fence_after();
       const uint32_t dacc = tmem + ab * kAccCols;
-      for (int ks = 0; ks < L.ksteps; ++ks, ++kc) {
-        const int sb = kc % kStagesB, sa = kc % kStagesA;
-        ok = wait_or_abort(&b_full[sb], (kc / kStagesB) & 1, a.wait, abort_flag);
-        if (ok) ok = wait_or_abort(&a_full[sa], (kc / kStagesA) & 1, a.wait, abort_flag);
-        if (!ok) break;
+      // Two k-steps per round: one poll of all four barriers, then eight MMAs
+      // back to back (a poll costs a few hundred cycles of the issuing
+      // thread, during which the tensor pipe would otherwise idle).
+      for (int ks = 0; ks < L.ksteps; ks += 2, kc += 2) {
+        const bool two = ks + 1 < L.ksteps;
+        const int s0 = kc % kStagesB, s1 = (kc + 1) % kStagesB;   // same index in both rings
+        const uint32_t p0 = (kc / kStagesB) & 1, p1 = ((kc + 1) / kStagesB) & 1;
+        uint64_t* b1 = two ? &b_full[s1] : &b_full[s0];
+        uint64_t* a1 = two ? &a_full[s1] : &a_full[s0];
+        const uint32_t q1 = two ? p1 : p0;
+        const long long limit = a.wait.limit * 64;
+        long long i = 0;
+        for (; i < limit; ++i) {
+          if (mbar_test_wait4(&b_full[s0], p0, &a_full[s0], p0, b1, q1, a1, q1)) break;
+          if ((i & 255) == 255 && *abort_flag) break;
+        }
+        if (i >= limit) {
+          atomicExch(a.wait.status, DEV_TIMEOUT);
+          *abort_flag = 1;
+        }
+        if (i >= limit || *abort_flag) {
+          ok = false;
+          break;
+        }
         tc_fence_after();
-        const uint32_t baddr = smem_u32(bring + sb * kBBytes);
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
-          umma_ts(dacc, tmem + kAcol0 + sa * 32 + kk * 8, smem_desc_sw128(baddr + kk * 32), idesc,
-                  (ks | kk) != 0 ? 1u : 0u);
-        tc_commit(&b_empty[sb]);
-        tc_commit(&a_empty[sa]);
-        counters[0] = kc + 1;
+        umma_ts_x4(dacc, tmem + kAcol0 + s0 * 32, smem_desc_sw128(smem_u32(bring + s0 * kBBytes)), idesc,
+                   ks != 0 ? 1u : 0u);
+        if (two)
+          umma_ts_x4(dacc, tmem + kAcol0 + s1 * 32, smem_desc_sw128(smem_u32(bring + s1 * kBBytes)), idesc, 1u);
+        tc_commit(&b_empty[s0]);
+        if (two) tc_commit(&b_empty[s1]);
+        counters[0] = kc + (two ? 2 : 1);
       }
+      kc -= (L.ksteps & 1);   // the last round of an odd count covered one step
       if (ok) tc_commit(&acc_full[ab]);
     }
     // All MMAs issued by this thread have completed once drain_bar flips.
     tc_commit(drain_bar);
     const WaitCfg drain{a.wait.status, kDrainWaitLimit};
     mbar_wait_bounded(drain_bar, 0, drain);
-  } else if (warp >= 4 && warp < 12) {
+  } else if (warp >= 4 && warp < kEpiWarp0) {
     // ---------------- dequant: packed weights -> 16-bit pairs in TMEM ----------------
     const int q = warp & 3;
-    const int grp = (warp - 4) >> 2;      // 0: even k-steps, 1: odd k-steps
+    const int grp = (warp - 4) >> 2;      // this group takes k-steps kc % kDeqGroups == grp
     const int r = q * 32 + lane;          // TMEM lane = weight row of the tile
     const uint32_t zoff2 = ZPM == QMOE_ZP_OFFSET ? half_magic_offset<BF16>(a.zp_offset) : 0u;
     int kc = 0;
     bool ok = true;
     for (int tile = blockIdx.x; tile < total_tiles && ok; tile += gridDim.x) {
       for (int ks = 0; ks < L.ksteps; ++ks, ++kc) {
-        if ((kc & 1) != grp) continue;
+        if (kc % kDeqGroups != grp) continue;
         const int sw = kc % kStagesW, sa = kc % kStagesA;
         ok = wait_or_abort(&w_full[sw], (kc / kStagesW) & 1, a.wait, abort_flag);
-        if (ok) ok = wait_or_abort(&a_empty[sa], ((kc / kStagesA) & 1) ^ 1, a.wait, abort_flag);
+        if (ok) ok = wait_or_abort(&b_empty[sa], ((kc / kStagesA) & 1) ^ 1, a.wait, abort_flag);
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
         tc_fence_after();
@@ -547,10 +631,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         }
       }
     }
-  } else if (warp >= 12) {
+  } else if (warp >= kEpiWarp0) {
     // ---------------- epilogue: TMEM -> GLU -> h (fc1) | weighted scatter (fc2) ----------------
+    // Each warp owns TMEM lanes 32q..32q+31 (its 32 weight rows) and a 32x32
+    // shared tile in which it turns its (row, token) values around, so that
+    // global memory sees 16-byte stores (fc1) / 16-byte reductions (fc2)
+    // along the contiguous feature axis.
     const int q = warp & 3;
-    const int r = q * 32 + lane;
+    float* tile32 = reinterpret_cast<float*>(smem + GemmSmem::epi_off(wstage)) + q * 32 * kEpiPitch;
     int tc = 0;
     bool ok = true;
     for (int tile = blockIdx.x; tile < total_tiles && ok; tile += gridDim.x, ++tc) {
@@ -564,43 +652,66 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       for (int c0 = 0; c0 < it.rows; c0 += 32) {
         uint32_t v[32];
         TC_LD32(tmem + ((uint32_t)(q * 32) << 16) + ab * kAccCols + c0, v);
-        // route of column c0 + lane (one load per lane, broadcast below)
+        // route of token column c0 + lane
         int my_tok = 0;
         float my_w = 0.f;
-        if (!GLU && c0 + lane < it.rows) {
+        const bool col_ok = c0 + lane < it.rows;
+        if (!GLU && col_ok) {
           const int route = a.perm[it.start + c0 + lane];
           my_tok = route / a.k;
           my_w = a.w[route];
         }
         tc_wait_ld();
         if (GLU) {
-          const int n = nt * 64 + (r >> 1);
+          // lanes 2p / 2p+1 hold gate / up of feature n = nt*64 + q*16 + p
           const bool odd = lane & 1;
           const int jbeg = odd ? 16 : 0;
+          uint16_t* t16 = reinterpret_cast<uint16_t*>(tile32);   // [32 tokens][16 features]
 #pragma unroll
           for (int j = 0; j < 32; ++j) {
             const float mine = __uint_as_float(v[j]);
             const float other = __shfl_xor_sync(0xffffffffu, mine, 1);
             if (j >= jbeg && j < jbeg + 16) {
-              const int c = c0 + j;
-              if (c < it.rows && n < a.N_out) {
-                const float g = odd ? other : mine, u = odd ? mine : other;
-                const float h = glu_fast(a.act, g, u);
-                const size_t o = (size_t)(it.start + c) * a.N_out + n;
-                if (BF16) static_cast<__nv_bfloat16*>(a.hout)[o] = __float2bfloat16_rn(h);
-                else static_cast<__half*>(a.hout)[o] = __float2half_rn(h);
-              }
+              const float g = odd ? other : mine, u = odd ? mine : other;
+              const float h = glu_fast(a.act, g, u);
+              t16[j * 16 + (lane >> 1)] = BF16 ? __bfloat16_as_ushort(__float2bfloat16_rn(h))
+                                               : __half_as_ushort(__float2half_rn(h));
             }
           }
-        } else {
-          const int m = nt * 128 + r;
+          __syncwarp();
+          // h chunk (token c0+tok, features nbase + 8*hv .. +7) -> tiled token
+          // layout of fc2's B operand; chunks past I are the K padding: zeros.
+          const int nbase = nt * 64 + q * 16;
+          const int item = tile / L.ntiles;
 #pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            const int tok = __shfl_sync(0xffffffffu, my_tok, j);
-            const float wr = __shfl_sync(0xffffffffu, my_w, j);
-            if (c0 + j < it.rows && m < a.N_out)
-              red_add_f32(a.out_acc + (size_t)tok * a.N_out + m, wr * __uint_as_float(v[j]));
+          for (int u2 = 0; u2 < 2; ++u2) {
+            const int vec = lane + 32 * u2, tok = vec >> 1, hv = vec & 1;
+            const int c = c0 + tok, n = nbase + 8 * hv;
+            if (c < it.rows && n < a.h_ksteps * 64) {
+              uint4 val = make_uint4(0u, 0u, 0u, 0u);
+              if (n < a.N_out) val = *reinterpret_cast<const uint4*>(t16 + tok * 16 + hv * 8);
+              uint8_t* dst = a.htiles + tok_tile_offset(item, a.h_ksteps, n >> 6) + c * 128 +
+                             ((((n & 63) >> 3) ^ (c & 7)) << 4);
+              *reinterpret_cast<uint4*>(dst) = val;
+            }
           }
+          __syncwarp();
+        } else {
+          // transpose: tile32[token j][row] = D[row][c0 + j]
+#pragma unroll
+          for (int j = 0; j < 32; ++j) tile32[j * kEpiPitch + lane] = __uint_as_float(v[j]);
+          __syncwarp();
+          const int mbase = nt * 128 + q * 32;
+          if (col_ok && mbase < a.N_out) {
+            float* dst = a.out_acc + (size_t)my_tok * a.N_out + mbase;
+            const float* src = tile32 + lane * kEpiPitch;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              const float4 y = *reinterpret_cast<const float4*>(src + 4 * i);
+              red_add_v4_f32(dst + 4 * i, my_w * y.x, my_w * y.y, my_w * y.z, my_w * y.w);
+            }
+          }
+          __syncwarp();
         }
       }
       tc_fence_before();
@@ -618,35 +729,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 // ----------------------------------------------------------------------------
 // Host side
 // ----------------------------------------------------------------------------
-static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  if (!fn) {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-  }
-  return fn;
-}
-
-cudaError_t make_token_map(CUtensorMap* map, const void* base, int rows, int K, bool bf16) {
-  auto fn = encode_fn();
-  if (!fn) return cudaErrorNotSupported;
-  cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
-  cuuint64_t strides[1] = {(cuuint64_t)K * 2};
-  cuuint32_t box[2] = {64, (cuuint32_t)kTileN};
-  cuuint32_t estr[2] = {1, 1};
-  CUresult r = fn(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
-                  const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
-}
-
 template <int BITS, int ZPM, bool BF16, bool GLU>
-static cudaError_t launch_g(const CUtensorMap& map, const GemmArgs& a, cudaStream_t s) {
+static cudaError_t launch_g(const GemmArgs& a, cudaStream_t s) {
   const int wstage = (a.L.stage_bytes + 127) / 128 * 128;
   const int smem = GemmSmem::total(wstage) + 1024;  // + alignment slack
   auto kern = gemm_kernel<BITS, ZPM, BF16, GLU>;
@@ -662,30 +746,30 @@ static cudaError_t launch_g(const CUtensorMap& map, const GemmArgs& a, cudaStrea
   cfg.stream = s;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, map, a);
+  return cudaLaunchKernelEx(&cfg, kern, a);
 }
 
 template <int BITS, int ZPM, bool BF16>
-static cudaError_t launch_g_glu(const CUtensorMap& m, const GemmArgs& a, cudaStream_t s) {
-  return a.fc == 1 ? launch_g<BITS, ZPM, BF16, true>(m, a, s) : launch_g<BITS, ZPM, BF16, false>(m, a, s);
+static cudaError_t launch_g_glu(const GemmArgs& a, cudaStream_t s) {
+  return a.fc == 1 ? launch_g<BITS, ZPM, BF16, true>(a, s) : launch_g<BITS, ZPM, BF16, false>(a, s);
 }
 template <int BITS, int ZPM>
-static cudaError_t launch_g_dt(const CUtensorMap& m, const GemmArgs& a, cudaStream_t s) {
-  return a.bf16 ? launch_g_glu<BITS, ZPM, true>(m, a, s) : launch_g_glu<BITS, ZPM, false>(m, a, s);
+static cudaError_t launch_g_dt(const GemmArgs& a, cudaStream_t s) {
+  return a.bf16 ? launch_g_glu<BITS, ZPM, true>(a, s) : launch_g_glu<BITS, ZPM, false>(a, s);
 }
 template <int BITS>
-static cudaError_t launch_g_zp(const CUtensorMap& m, const GemmArgs& a, cudaStream_t s) {
-  if (a.zp_mode == QMOE_ZP_UINT8) return launch_g_dt<BITS, QMOE_ZP_UINT8>(m, a, s);
-  if (a.zp_mode == QMOE_ZP_OFFSET) return launch_g_dt<BITS, QMOE_ZP_OFFSET>(m, a, s);
-  return launch_g_dt<BITS, QMOE_ZP_SYMMETRIC>(m, a, s);
+static cudaError_t launch_g_zp(const GemmArgs& a, cudaStream_t s) {
+  if (a.zp_mode == QMOE_ZP_UINT8) return launch_g_dt<BITS, QMOE_ZP_UINT8>(a, s);
+  if (a.zp_mode == QMOE_ZP_OFFSET) return launch_g_dt<BITS, QMOE_ZP_OFFSET>(a, s);
+  return launch_g_dt<BITS, QMOE_ZP_SYMMETRIC>(a, s);
 }
 
-cudaError_t launch_gemm(const CUtensorMap& map, const GemmArgs& a, cudaStream_t s) {
+cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t s) {
   if (a.max_items <= 0 || a.grid <= 0) return cudaSuccess;
   switch (a.L.bits) {
-    case 2: return launch_g_zp<2>(map, a, s);
-    case 3: return launch_g_zp<3>(map, a, s);
-    case 4: return launch_g_zp<4>(map, a, s);
+    case 2: return launch_g_zp<2>(a, s);
+    case 3: return launch_g_zp<3>(a, s);
+    case 4: return launch_g_zp<4>(a, s);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -1,6 +1,5 @@
 // Tensor-core grouped GEMM path (prefill): declarations.
 #pragma once
-#include <cuda.h>
 
 #include "qmoe_internal.cuh"
 
@@ -35,16 +34,28 @@ struct GemmRepackArgs {
 };
 cudaError_t launch_repack_gemm(const GemmRepackArgs& a, cudaStream_t s);
 
+// Tiled token layout (the B operand of the grouped GEMM).  Work item i of the
+// GEMM class owns block i: for each k-step s of 64 values, 128 token rows of
+// 128 bytes, the 16-byte chunk c of row r stored at chunk position
+// c ^ (r & 7) -- the K-major 128-byte-swizzle layout the MMA reads -- so one
+// (item, k-step) operand tile is one contiguous 16 KB bulk copy.
+constexpr int kTokTileBytes = 128 * 128;
+__host__ __device__ inline size_t tok_tile_offset(int item, int ksteps, int s) {
+  return ((size_t)item * ksteps + s) * kTokTileBytes;
+}
+
 struct GemmArgs {
   const uint8_t* wq;       // GEMM layout
   GemmLayout L;
-  const Item* items;       // class-1 work-list (e, start, rows <= 256)
+  const Item* items;       // class-1 work-list (e, start, rows <= 128)
   const int* n_items;
   int max_items;
   int grid;                // persistent CTAs
   int fc, act, zp_mode, bf16;
   float zp_offset;
-  void* hout;              // fc1: h [R, I] D (route order)
+  const uint8_t* btiles;   // B operand in the tiled token layout (L.ksteps steps per item)
+  uint8_t* htiles;         // fc1: h written in the tiled token layout for fc2
+  int h_ksteps;            // fc1: k-steps of h (ceil(I / 64))
   float* out_acc;          // fc2: fp32 [T, H] combine accumulator
   const int* perm;
   const float* w;
@@ -53,9 +64,11 @@ struct GemmArgs {
   WaitCfg wait;
 };
 
-cudaError_t make_token_map(CUtensorMap* map, const void* base, int rows, int K, bool bf16);
-cudaError_t launch_gemm(const CUtensorMap& map, const GemmArgs& a, cudaStream_t s);
-cudaError_t launch_gather(const void* x, const int* perm, int k, int R, int H, void* xg, cudaStream_t s);
+cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t s);
+// x rows of every GEMM-class item into the tiled token layout (K = H padded
+// to 64 with zeros).
+cudaError_t launch_gather_tiles(const void* x, const int* perm, int k, int H, const Item* items,
+                                const int* n_items, int max_items, uint8_t* xt, cudaStream_t s);
 cudaError_t launch_finalize_acc(float* acc, void* out, size_t n, int dtype, cudaStream_t s);
 
 }  // namespace qmoe
