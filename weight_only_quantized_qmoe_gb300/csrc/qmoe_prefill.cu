@@ -21,7 +21,7 @@
 //     arrive);
 //   * tcgen05.mma.cta_group::1.kind::f16, fp32 accumulators in TMEM, two of
 //     128 columns so the epilogue of one tile overlaps the next tile's MMAs;
-//     N = the tile's rows rounded up to 16 (no padded work);
+//     N = the tile's rows rounded up to 16, at least 64;
 //   * warp roles: 0 = bulk-copy producer, 1 = MMA issuer (one thread) and
 //     TMEM owner, then the dequant groups, then 4 epilogue warps (tcgen05.ld);
 //   * persistent CTAs stride over the (item, weight-tile) list; fc1 rows are
@@ -364,12 +364,16 @@ __device__ __forceinline__ bool spin_or_abort(uint64_t* bar, uint32_t parity, co
 // ----------------------------------------------------------------------------
 // The grouped GEMM kernel
 // ----------------------------------------------------------------------------
-constexpr int kStagesB = 8;       // token tiles: 128 x 64 x 2 B = 16 KB each
-constexpr int kStagesW = 8;       // packed weight stages
-constexpr int kStagesA = 8;       // dequantised A stages in TMEM (32 columns each)
-// One commit per k-step frees both the token stage and the A stage of that
-// step (step_empty), so both rings have the same depth.
-static_assert(kStagesA == kStagesB, "B and A rings advance together");
+// One ring of kStages k-steps: stage s holds the token tile (B, shared
+// memory), the packed weights (W, shared memory) and the dequantised weights
+// (A, 32 TMEM columns) of one k-step.  Three barriers per stage, one wait per
+// role and k-step:
+//   full[s]  the producer's copies of W and B have landed (transaction count)
+//   ready[s] the 4 dequant warps of the step have written A   (4 arrivals)
+//   empty[s] the MMAs of the step have completed                (tcgen05.commit)
+// producer: empty -> copies -> full;  dequant: full -> A -> ready;
+// MMA: ready -> MMAs -> commit empty.
+constexpr int kStages = 8;
 constexpr int kTileN = 128;       // token rows per tile (MMA N <= 128)
 constexpr int kBBytes = kTileN * 128;
 constexpr int kTmemCols = 512;
@@ -383,8 +387,8 @@ constexpr int kEpiBytes = 4 * 32 * kEpiPitch * 4;   // one 32x32 tile per epilog
 
 struct GemmSmem {
   static constexpr int b_off = 0;
-  static constexpr int w_off = kStagesB * kBBytes;
-  __host__ __device__ static int epi_off(int wstage) { return w_off + kStagesW * ((wstage + 127) / 128 * 128); }
+  static constexpr int w_off = kStages * kBBytes;
+  __host__ __device__ static int epi_off(int wstage) { return w_off + kStages * ((wstage + 127) / 128 * 128); }
   __host__ __device__ static int bar_off(int wstage) { return epi_off(wstage) + kEpiBytes; }
   __host__ __device__ static int total(int wstage) { return bar_off(wstage) + 1024; }
 };
@@ -454,13 +458,40 @@ __device__ __forceinline__ float glu_fast(int act, float g, float u) {
   return 0.5f * g * (1.f + t) * u;
 }
 
+// Source of k-step ks of a tile: the weight stage and the token tile.  The
+// weight tiles of one token tile run on neighbouring CTAs at the same time;
+// starting each at a different k-step (rotation by nt) spreads their reads of
+// the shared token tile over the L2 instead of hitting the same lines
+// together.  The MMA sums the k-steps in any order.
+struct StepSrc {
+  const uint8_t* w;
+  const uint8_t* b;
+  uint32_t b_bytes;
+};
+__device__ __forceinline__ StepSrc step_src(const GemmArgs& a, int tile, int ks) {
+  const GemmLayout& L = a.L;
+  const int item = tile / L.ntiles, nt = tile % L.ntiles;
+  const Item it = a.items[item];
+  int kr = ks + (int)(((long long)nt * L.ksteps) / L.ntiles);
+  if (kr >= L.ksteps) kr -= L.ksteps;
+  StepSrc r;
+  r.w = a.wq + (size_t)it.e * L.expert_bytes + (size_t)nt * L.tile_bytes + (size_t)kr * L.stage_bytes;
+  r.b = a.btiles + tok_tile_offset(item, L.ksteps, kr);
+  // only the 8-row groups that hold the item's rows (the MMA reads stale
+  // rows past them into columns that are never stored)
+  r.b_bytes = (uint32_t)min(kBBytes, ((it.rows + 7) / 8) * 1024);
+  return r;
+}
+
 // Warp roles (8 + 4 * kDeqGroups warps):
-//   0      TMA / bulk-copy producer (one thread)
+//   0      bulk-copy producer (one thread): W + B of a k-step into stage s
 //   1      MMA issuer (one thread) and TMEM owner
 //   2..3   idle
 //   4 ..   dequant groups of 4 warps; group g takes k-steps kc % kDeqGroups == g,
 //          warp w owns TMEM lanes 32*(w%4)
 //   last 4 epilogue (TMEM lanes 32*(w%4))
+// The producer and the MMA issuer poll without suspending (they pace the
+// ring); the dequant and epilogue warps park on their barriers.
 template <int BITS, int ZPM, bool BF16, bool GLU>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     gemm_kernel(const GemmArgs a) {
@@ -472,27 +503,25 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   uint8_t* bring = smem + GemmSmem::b_off;
   uint8_t* wring = smem + GemmSmem::w_off;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + GemmSmem::bar_off(wstage));
-  uint64_t* b_full = bars;
-  uint64_t* b_empty = b_full + kStagesB;      // step_empty: B and A stage of a k-step
-  uint64_t* w_full = b_empty + kStagesB;
-  uint64_t* w_empty = w_full + kStagesW;
-  uint64_t* a_full = w_empty + kStagesW;
-  uint64_t* acc_full = a_full + kStagesA;    // [2]
+  uint64_t* full = bars;
+  uint64_t* ready = full + kStages;
+  uint64_t* empty = ready + kStages;
+  uint64_t* acc_full = empty + kStages;      // [2]
   uint64_t* acc_empty = acc_full + 2;        // [2]
   uint64_t* drain_bar = acc_empty + 2;
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain_bar + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
-  volatile int* counters = abort_flag + 1;   // [0] = B steps consumed, [1] = W steps consumed
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
-    for (int i = 0; i < kStagesB; ++i) { mbar_init(&b_full[i], 1); mbar_init(&b_empty[i], 1); }
-    for (int i = 0; i < kStagesW; ++i) { mbar_init(&w_full[i], 1); mbar_init(&w_empty[i], 4); }
-    for (int i = 0; i < kStagesA; ++i) mbar_init(&a_full[i], 4);
+    for (int i = 0; i < kStages; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&ready[i], 4);
+      mbar_init(&empty[i], 1);
+    }
     for (int i = 0; i < 2; ++i) { mbar_init(&acc_full[i], 1); mbar_init(&acc_empty[i], 4); }
     mbar_init(drain_bar, 1);
     *abort_flag = 0;
-    counters[0] = counters[1] = 0;
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -509,43 +538,30 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   const int total_tiles = n_items * L.ntiles;
 
   if (warp == 0 && lane == 0) {
-    // ---------------- producer: token tiles (TMA) + weight stages (bulk) ----------------
-    int kc = 0, nb_issued = 0, nw_issued = 0;
+    // ---------------- producer ----------------
+    int kc = 0, issued = 0;
     bool ok = true;
     for (int tile = blockIdx.x; tile < total_tiles && ok; tile += gridDim.x) {
-      const Item it = a.items[tile / L.ntiles];
-      const int nt = tile % L.ntiles;
-      const uint8_t* wsrc = a.wq + (size_t)it.e * L.expert_bytes + (size_t)nt * L.tile_bytes;
-      // The weight tiles of one token tile run on neighbouring CTAs at the
-      // same time; starting each at a different k-step spreads their reads
-      // of the shared token tile over the L2 instead of hitting the same
-      // lines together.  The MMA sums the k-steps in any order.
-      const int rot = (int)(((long long)nt * L.ksteps) / L.ntiles);
-      for (int ks = 0; ks < L.ksteps && ok; ++ks, ++kc) {
-        const int sb = kc % kStagesB, sw = kc % kStagesW;
-        int kr = ks + rot;
-        if (kr >= L.ksteps) kr -= L.ksteps;
-        ok = wait_or_abort(&w_empty[sw], ((kc / kStagesW) & 1) ^ 1, a.wait, abort_flag);
+      // (An L2 bulk prefetch a ring's depth ahead of each copy made the
+      // kernel twice as slow: the copies queue behind the prefetches.)
+      for (int ks = 0; ks < L.ksteps; ++ks, ++kc) {
+        const StepSrc src = step_src(a, tile, ks);
+        const int s = kc % kStages;
+        ok = spin_or_abort(&empty[s], ((kc / kStages) & 1) ^ 1, a.wait, abort_flag);
         if (!ok) break;
-        mbar_arrive_expect_tx(&w_full[sw], L.stage_bytes);
-        bulk_g2s(wring + sw * wstage, wsrc + (size_t)kr * L.stage_bytes, L.stage_bytes, &w_full[sw]);
-        nw_issued = kc + 1;
-        ok = wait_or_abort(&b_empty[sb], ((kc / kStagesB) & 1) ^ 1, a.wait, abort_flag);
-        if (!ok) break;
-        mbar_arrive_expect_tx(&b_full[sb], kBBytes);
-        bulk_g2s(bring + sb * kBBytes, a.btiles + tok_tile_offset(tile / L.ntiles, L.ksteps, kr), kBBytes,
-                 &b_full[sb]);
-        nb_issued = kc + 1;
+        mbar_arrive_expect_tx(&full[s], (uint32_t)L.stage_bytes + src.b_bytes);
+        bulk_g2s(wring + s * wstage, src.w, (uint32_t)L.stage_bytes, &full[s]);
+        bulk_g2s(bring + s * kBBytes, src.b, src.b_bytes, &full[s]);
+        issued = kc + 1;
       }
     }
     if (!ok) {
-      // Drain: wait for every copy issued but not consumed (fixed large bound)
-      // so that none lands in shared memory after the CTA has left.
+      // Drain: the last copy issued into each stage must land before the CTA
+      // leaves (fixed large bound).  A stage's phase completes on the bytes
+      // alone, whatever the consumers did.
       const WaitCfg drain{a.wait.status, kDrainWaitLimit};
-      for (int i = counters[0]; i < nb_issued; ++i)
-        mbar_wait_bounded(&b_full[i % kStagesB], (i / kStagesB) & 1, drain);
-      for (int i = counters[1]; i < nw_issued; ++i)
-        mbar_wait_bounded(&w_full[i % kStagesW], (i / kStagesW) & 1, drain);
+      for (int i = issued > kStages ? issued - kStages : 0; i < issued; ++i)
+        mbar_wait_bounded(&full[i % kStages], (i / kStages) & 1, drain);
     }
   } else if (warp == 1 && lane == 0) {
     // ---------------- MMA issuer ----------------
@@ -553,47 +569,24 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     bool ok = true;
     for (int tile = blockIdx.x; tile < total_tiles && ok; tile += gridDim.x, ++tc) {
       const Item it = a.items[tile / L.ntiles];
-      const int N = (it.rows + 15) & ~15;
+      // N >= 64: below that the MMA takes as long as at 64 (measured) and
+      // the extra columns are never stored
+      const int N = max(64, (it.rows + 15) & ~15);
       const uint32_t idesc = idesc_f16(BF16, 128, N);
       const int ab = tc & 1;
       ok = spin_or_abort(&acc_empty[ab], ((tc >> 1) & 1) ^ 1, a.wait, abort_flag);
       if (!ok) break;
       tc_fence_after();
       const uint32_t dacc = tmem + ab * kAccCols;
-      // Two k-steps per round: one poll of all four barriers, then eight MMAs
-      // back to back (a poll costs a few hundred cycles of the issuing
-      // thread, during which the tensor pipe would otherwise idle).
-      for (int ks = 0; ks < L.ksteps; ks += 2, kc += 2) {
-        const bool two = ks + 1 < L.ksteps;
-        const int s0 = kc % kStagesB, s1 = (kc + 1) % kStagesB;   // same index in both rings
-        const uint32_t p0 = (kc / kStagesB) & 1, p1 = ((kc + 1) / kStagesB) & 1;
-        uint64_t* b1 = two ? &b_full[s1] : &b_full[s0];
-        uint64_t* a1 = two ? &a_full[s1] : &a_full[s0];
-        const uint32_t q1 = two ? p1 : p0;
-        const long long limit = a.wait.limit * 64;
-        long long i = 0;
-        for (; i < limit; ++i) {
-          if (mbar_test_wait4(&b_full[s0], p0, &a_full[s0], p0, b1, q1, a1, q1)) break;
-          if ((i & 255) == 255 && *abort_flag) break;
-        }
-        if (i >= limit) {
-          atomicExch(a.wait.status, DEV_TIMEOUT);
-          *abort_flag = 1;
-        }
-        if (i >= limit || *abort_flag) {
-          ok = false;
-          break;
-        }
+      for (int ks = 0; ks < L.ksteps; ++ks, ++kc) {
+        const int s = kc % kStages;
+        ok = spin_or_abort(&ready[s], (kc / kStages) & 1, a.wait, abort_flag);
+        if (!ok) break;
         tc_fence_after();
-        umma_ts_x4(dacc, tmem + kAcol0 + s0 * 32, smem_desc_sw128(smem_u32(bring + s0 * kBBytes)), idesc,
+        umma_ts_x4(dacc, tmem + kAcol0 + s * 32, smem_desc_sw128(smem_u32(bring + s * kBBytes)), idesc,
                    ks != 0 ? 1u : 0u);
-        if (two)
-          umma_ts_x4(dacc, tmem + kAcol0 + s1 * 32, smem_desc_sw128(smem_u32(bring + s1 * kBBytes)), idesc, 1u);
-        tc_commit(&b_empty[s0]);
-        if (two) tc_commit(&b_empty[s1]);
-        counters[0] = kc + (two ? 2 : 1);
+        tc_commit(&empty[s]);
       }
-      kc -= (L.ksteps & 1);   // the last round of an odd count covered one step
       if (ok) tc_commit(&acc_full[ab]);
     }
     // All MMAs issued by this thread have completed once drain_bar flips.
@@ -602,6 +595,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     mbar_wait_bounded(drain_bar, 0, drain);
   } else if (warp >= 4 && warp < kEpiWarp0) {
     // ---------------- dequant: packed weights -> 16-bit pairs in TMEM ----------------
+    // full[s] also means the A slot is free: the producer refilled stage s
+    // only after the MMAs that read it had completed (empty[s]).
     const int q = warp & 3;
     const int grp = (warp - 4) >> 2;      // this group takes k-steps kc % kDeqGroups == grp
     const int r = q * 32 + lane;          // TMEM lane = weight row of the tile
@@ -611,24 +606,19 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     for (int tile = blockIdx.x; tile < total_tiles && ok; tile += gridDim.x) {
       for (int ks = 0; ks < L.ksteps; ++ks, ++kc) {
         if (kc % kDeqGroups != grp) continue;
-        const int sw = kc % kStagesW, sa = kc % kStagesA;
-        ok = wait_or_abort(&w_full[sw], (kc / kStagesW) & 1, a.wait, abort_flag);
-        if (ok) ok = wait_or_abort(&b_empty[sa], ((kc / kStagesA) & 1) ^ 1, a.wait, abort_flag);
+        const int s = kc % kStages;
+        ok = wait_or_abort(&full[s], (kc / kStages) & 1, a.wait, abort_flag);
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
         tc_fence_after();
         uint32_t v[32];
-        dequant_row<BITS, ZPM, BF16>(wring + sw * wstage, L, r, zoff2, v);
-        const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + kAcol0 + sa * 32;
+        dequant_row<BITS, ZPM, BF16>(wring + s * wstage, L, r, zoff2, v);
+        const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + kAcol0 + s * 32;
         TC_ST32(taddr, v);
         tc_wait_st();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) {
-          mbar_arrive(&a_full[sa]);
-          mbar_arrive(&w_empty[sw]);
-          if (q == 0) counters[1] = kc + 1;
-        }
+        if (lane == 0) mbar_arrive(&ready[s]);
       }
     }
   } else if (warp >= kEpiWarp0) {
