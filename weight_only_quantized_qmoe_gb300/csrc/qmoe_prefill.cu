@@ -468,33 +468,48 @@ __device__ __forceinline__ float glu_fast(int act, float g, float u) {
   return 0.5f * g * (1.f + t) * u;
 }
 
-// Source of k-step ks of a tile: the weight stage and the token tile.  The
-// weight tiles of one token tile run on neighbouring CTAs at the same time;
-// starting each at a different k-step (rotation by nt) spreads their reads of
-// the shared token tile over the L2 instead of hitting the same lines
+// Sources of one tile: its weight tile, its token tile and the first k-step.
+// The weight tiles of one token tile run on neighbouring CTAs at the same
+// time; starting each at a different k-step (rotation by nt) spreads their
+// reads of the shared token tile over the L2 instead of hitting the same lines
 // together.  The MMA sums the k-steps in any order.
-struct StepSrc {
-  const uint8_t* w;
-  const uint8_t* b;
-  uint32_t b_bytes;
+struct TileSrc {
+  const uint8_t* w;     // k-step kr at w + kr * stage_bytes
+  const uint8_t* b;     // k-step kr at b + kr * kTokTileBytes
+  uint32_t b_bytes;     // token bytes copied per k-step
+  int rot;              // first k-step
 };
-__device__ __forceinline__ StepSrc step_src(const GemmArgs& a, int tile, int ks) {
+__device__ __forceinline__ TileSrc tile_src(const GemmArgs& a, int tile) {
   const GemmLayout& L = a.L;
-  const int item = tile / L.ntiles, nt = tile % L.ntiles;
+  const int item = tile / L.ntiles, nt = tile - item * L.ntiles;
   const Item it = a.items[item];
-  int kr = ks + (int)(((long long)nt * L.ksteps) / L.ntiles);
-  if (kr >= L.ksteps) kr -= L.ksteps;
-  StepSrc r;
-  r.w = a.wq + (size_t)it.e * L.expert_bytes + (size_t)nt * L.tile_bytes + (size_t)kr * L.stage_bytes;
-  r.b = a.btiles + tok_tile_offset(item, L.ksteps, kr);
+  TileSrc r;
+  r.w = a.wq + (size_t)it.e * L.expert_bytes + (size_t)nt * L.tile_bytes;
+  r.b = a.btiles + tok_tile_offset(item, L.ksteps, 0);
   // only the 8-row groups that hold the item's rows (the MMA reads stale
   // rows past them into columns that are never stored)
   r.b_bytes = (uint32_t)min(kBBytes, ((it.rows + 7) / 8) * 1024);
+  r.rot = (int)(((long long)nt * L.ksteps) / L.ntiles);
   return r;
 }
 
+__device__ __forceinline__ void mbar_arrive_expect_tx_elect(uint64_t* bar, uint32_t bytes) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+      "@e mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n\t}" ::"r"(smem_u32(bar)), "r"(bytes)
+      : "memory");
+}
+__device__ __forceinline__ void bulk_g2s_elect(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+      "@e cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n\t}" ::"r"(
+          smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
 // Warp roles (8 + 4 * kDeqGroups warps):
-//   0      bulk-copy producer (one thread): W + B of a k-step into stage s
+//   0      bulk-copy producer (whole warp, elect.sync): W + B of a k-step into stage s
 //   1      MMA issuer (whole warp, elect.sync) and TMEM owner
 //   2..3   idle
 //   4 ..   dequant groups of 4 warps; group g takes k-steps kc % kDeqGroups == g,
@@ -547,22 +562,29 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   const int n_items = *a.n_items;
   const int total_tiles = n_items * L.ntiles;
 
-  if (warp == 0 && lane == 0) {
-    // ---------------- producer ----------------
+  if (warp == 0) {
+    // ---------------- producer: the whole warp, one elected lane copies ----------------
     int kc = 0, issued = 0;
     bool ok = true;
     for (int tile = blockIdx.x; tile < total_tiles && ok; tile += gridDim.x) {
       // (An L2 bulk prefetch a ring's depth ahead of each copy made the
       // kernel twice as slow: the copies queue behind the prefetches.)
+      const TileSrc src = tile_src(a, tile);
+      const uint32_t tx = (uint32_t)L.stage_bytes + src.b_bytes;
+      int kr = src.rot;
       for (int ks = 0; ks < L.ksteps; ++ks, ++kc) {
-        const StepSrc src = step_src(a, tile, ks);
-        const int s = kc % kStages;
-        ok = spin_or_abort(&empty[s], ((kc / kStages) & 1) ^ 1, a.wait, abort_flag);
-        if (!ok) break;
-        mbar_arrive_expect_tx(&full[s], (uint32_t)L.stage_bytes + src.b_bytes);
-        bulk_g2s(wring + s * wstage, src.w, (uint32_t)L.stage_bytes, &full[s]);
-        bulk_g2s(bring + s * kBBytes, src.b, src.b_bytes, &full[s]);
+        const int s = kc & (kStages - 1);
+        const uint32_t par = ((uint32_t)(kc / kStages) & 1u) ^ 1u;
+        if (!mbar_test_wait(&empty[s], par)) {
+          ok = spin_or_abort(&empty[s], par, a.wait, abort_flag);
+          ok = __shfl_sync(0xffffffffu, ok, 0);
+          if (!ok) break;
+        }
+        mbar_arrive_expect_tx_elect(&full[s], tx);
+        bulk_g2s_elect(wring + s * wstage, src.w + (size_t)kr * L.stage_bytes, (uint32_t)L.stage_bytes, &full[s]);
+        bulk_g2s_elect(bring + s * kBBytes, src.b + (size_t)kr * kTokTileBytes, src.b_bytes, &full[s]);
         issued = kc + 1;
+        if (++kr == L.ksteps) kr = 0;
       }
     }
     if (!ok) {
@@ -575,6 +597,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
   } else if (warp == 1) {
     // ---------------- MMA issuer: the whole warp, one elected lane issues ----------------
+    static_assert((kStages & (kStages - 1)) == 0, "ring depth is a power of two");
+    const uint32_t a0 = tmem + kAcol0;
+    const uint64_t bdesc0 = smem_desc_sw128(smem_u32(bring));
     int kc = 0, tc = 0;
     bool ok = true;
     for (int tile = blockIdx.x; tile < total_tiles && ok; tile += gridDim.x, ++tc) {
@@ -589,15 +614,31 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       if (!ok) break;
       tc_fence_after();
       const uint32_t dacc = tmem + ab * kAccCols;
-      for (int ks = 0; ks < L.ksteps; ++ks, ++kc) {
-        const int s = kc % kStages;
-        ok = spin_or_abort(&ready[s], (kc / kStages) & 1, a.wait, abort_flag);
-        ok = __shfl_sync(0xffffffffu, ok, 0);
-        if (!ok) break;
-        tc_fence_after();
-        umma_ts_x4_elect(dacc, tmem + kAcol0 + s * 32, smem_desc_sw128(smem_u32(bring + s * kBBytes)), idesc,
-                         ks != 0 ? 1u : 0u);
-        tc_commit_elect(&empty[s]);
+      // The k-step loop is unrolled over the ring stage u, so every stage's
+      // operands are compile-time offsets from a0 / bdesc0 and the code
+      // between two MMA batches is a single barrier poll and a commit: with
+      // more work there (index arithmetic, a general wait loop) the tensor
+      // pipe idled between batches (measured: 257 vs 700 cycles per k-step).
+      int ks = 0;
+      while (ks < L.ksteps && ok) {
+#pragma unroll
+        for (int u = 0; u < kStages; ++u) {
+          if (u == (kc & (kStages - 1)) && ks < L.ksteps && ok) {
+            const uint32_t par = (uint32_t)(kc / kStages) & 1u;
+            if (!mbar_test_wait(&ready[u], par)) {
+              ok = spin_or_abort(&ready[u], par, a.wait, abort_flag);
+              ok = __shfl_sync(0xffffffffu, ok, 0);
+            }
+            if (ok) {
+              tc_fence_after();
+              umma_ts_x4_elect(dacc, a0 + 32 * u, bdesc0 + (uint64_t)(u * (kBBytes >> 4)), idesc,
+                               ks != 0 ? 1u : 0u);
+              tc_commit_elect(&empty[u]);
+              ++kc;
+              ++ks;
+            }
+          }
+        }
       }
       if (ok) tc_commit_elect(&acc_full[ab]);
     }
