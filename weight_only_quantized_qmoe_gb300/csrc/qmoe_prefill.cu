@@ -575,8 +575,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       for (int ks = 0; ks < L.ksteps; ++ks, ++kc) {
         const int s = kc & (kStages - 1);
         const uint32_t par = ((uint32_t)(kc / kStages) & 1u) ^ 1u;
+        // Parked (not spinning) wait: the producer runs a ring's depth ahead
+        // of the MMAs, and a spinning poll competes with them for the
+        // barrier unit.
         if (!mbar_test_wait(&empty[s], par)) {
-          ok = spin_or_abort(&empty[s], par, a.wait, abort_flag);
+          ok = wait_or_abort(&empty[s], par, a.wait, abort_flag);
           ok = __shfl_sync(0xffffffffu, ok, 0);
           if (!ok) break;
         }
@@ -651,28 +654,27 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     // full[s] also means the A slot is free: the producer refilled stage s
     // only after the MMAs that read it had completed (empty[s]).
     const int q = warp & 3;
-    const int grp = (warp - 4) >> 2;      // this group takes k-steps kc % kDeqGroups == grp
+    const int grp = (warp - 4) >> 2;      // dequant group
     const int r = q * 32 + lane;          // TMEM lane = weight row of the tile
     const uint32_t zoff2 = ZPM == QMOE_ZP_OFFSET ? half_magic_offset<BF16>(a.zp_offset) : 0u;
-    int kc = 0;
+    // k-steps are numbered across tiles (kc); this group takes kc = grp,
+    // grp + kDeqGroups, ...
+    const int n_steps = ((total_tiles - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x) * L.ksteps;
     bool ok = true;
-    for (int tile = blockIdx.x; tile < total_tiles && ok; tile += gridDim.x) {
-      for (int ks = 0; ks < L.ksteps; ++ks, ++kc) {
-        if (kc % kDeqGroups != grp) continue;
-        const int s = kc % kStages;
-        ok = wait_or_abort(&full[s], (kc / kStages) & 1, a.wait, abort_flag);
-        ok = __all_sync(0xffffffffu, ok);
-        if (!ok) break;
-        tc_fence_after();
-        uint32_t v[32];
-        dequant_row<BITS, ZPM, BF16>(wring + s * wstage, L, r, zoff2, v);
-        const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + kAcol0 + s * 32;
-        TC_ST32(taddr, v);
-        tc_wait_st();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&ready[s]);
-      }
+    for (int kc = grp; kc < n_steps && ok; kc += kDeqGroups) {
+      const int s = kc & (kStages - 1);
+      ok = wait_or_abort(&full[s], (kc / kStages) & 1, a.wait, abort_flag);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      tc_fence_after();
+      uint32_t v[32];
+      dequant_row<BITS, ZPM, BF16>(wring + s * wstage, L, r, zoff2, v);
+      const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + kAcol0 + s * 32;
+      TC_ST32(taddr, v);
+      tc_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&ready[s]);
     }
   } else if (warp >= kEpiWarp0) {
     // ---------------- epilogue: TMEM -> GLU -> h (fc1) | weighted scatter (fc2) ----------------
@@ -710,16 +712,16 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           const bool odd = lane & 1;
           const int jbeg = odd ? 16 : 0;
           uint16_t* t16 = reinterpret_cast<uint16_t*>(tile32);   // [32 tokens][16 features]
+          // Even lanes take tokens 0..15 of the chunk (own gate, partner's
+          // up), odd lanes tokens 16..31 (partner's gate, own up): one
+          // exchange and one activation per lane and token pair, no divergence.
 #pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            const float mine = __uint_as_float(v[j]);
-            const float other = __shfl_xor_sync(0xffffffffu, mine, 1);
-            if (j >= jbeg && j < jbeg + 16) {
-              const float g = odd ? other : mine, u = odd ? mine : other;
-              const float h = glu_fast(a.act, g, u);
-              t16[j * 16 + (lane >> 1)] = BF16 ? __bfloat16_as_ushort(__float2bfloat16_rn(h))
-                                               : __half_as_ushort(__float2half_rn(h));
-            }
+          for (int j = 0; j < 16; ++j) {
+            const float lo = __uint_as_float(v[j]), hi = __uint_as_float(v[16 + j]);
+            const float other = __shfl_xor_sync(0xffffffffu, odd ? lo : hi, 1);
+            const float h = glu_fast(a.act, odd ? other : lo, odd ? hi : other);
+            t16[(jbeg + j) * 16 + (lane >> 1)] = BF16 ? __bfloat16_as_ushort(__float2bfloat16_rn(h))
+                                                      : __half_as_ushort(__float2half_rn(h));
           }
           __syncwarp();
           // h chunk (token c0+tok, features nbase + 8*hv .. +7) -> tiled token
