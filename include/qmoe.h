@@ -122,8 +122,10 @@ qmoe_status qmoe_set_routing(qmoe_layer* layer, int normalize);
 qmoe_status qmoe_set_zero_point_offset(qmoe_layer* layer, float offset);
 
 /* Experts with more than `min_rows` routed rows take the tensor-core grouped
- * GEMM; the others the weight-streaming decode kernel.  Any value gives the
- * same result within tolerance.  Default 32.  [qmoe.rs prefill_min_tokens;
+ * GEMM; the others the mma.sync weight-streaming decode kernel.  Any value
+ * gives the same result within tolerance.  Default 0: every expert takes the
+ * tensor-core path (the faster one at every measured shape, decode included);
+ * fp32 activations always take the SIMT kernel.  [qmoe.rs prefill_min_tokens;
  * PR "fast INT3" kMaxProfiledExpandedRows] */
 qmoe_status qmoe_set_gemm_min_rows(qmoe_layer* layer, int min_rows);
 
@@ -251,11 +253,13 @@ qmoe_status qmoe_set_wait_limit(qmoe_layer* layer, int64_t iterations);
 qmoe_status qmoe_forward_noalloc(qmoe_layer* layer, const void* x_dev, const float* logits_dev,
                                  void* out_dev, int64_t num_tokens, void* stream);
 
-/* Test hook for failure detection without a GPU fault: while enabled, every
- * warp of the decode projection kernels arms its first copy-stage barrier but
- * never issues that copy, so its bounded wait runs out; the kernel records
+/* Test hook for failure detection without a GPU fault: while enabled, the
+ * projection kernels arm their first copy-stage barrier but never issue that
+ * copy (every warp of the decode kernel; the producer of every grouped-GEMM
+ * CTA), so the bounded waits on it run out; the kernel records
  * QMOE_ERR_TIMEOUT (see qmoe_poll_device_status), waits for its other copies
- * and returns.  Results of such forwards are meaningless.  0 disables. */
+ * (and MMAs), frees its tensor memory and returns.  Results of such forwards
+ * are meaningless.  0 disables. */
 qmoe_status qmoe_debug_inject_stall(qmoe_layer* layer, int enable);
 
 /* Message of the last failed call on `layer` ("" if none); static strings

@@ -35,7 +35,7 @@ def run_layer(qm, inp, reserve=None, min_rows=None):
     return layer, out
 
 
-def check_routing(layer, inp, min_rows=32):
+def check_routing(layer, inp, min_rows=0):
     cfg = inp["cfg"]
     ids, w, perm, offs = layer.routing(cfg.T)
     torch.cuda.synchronize()
@@ -70,11 +70,17 @@ def check_out(out, ref, dtype, tokens=None):
     return err, tol
 
 
+# Both projection paths: the default (tensor-core grouped GEMM for every
+# expert) and the mma.sync decode kernel (threshold above any expert's rows).
+PATHS = {"gemm": 0, "decode": 10 ** 6}
+
+
+@pytest.mark.parametrize("path", sorted(PATHS))
 @pytest.mark.parametrize("name", ["tiny", "decode_int2", "decode_many_expert_int4", "mixed_int3_int4"])
-def test_config_parity(qm, name):
+def test_config_parity(qm, name, path):
     inp = make_inputs(CONFIGS[name])
-    layer, out = run_layer(qm, inp)
-    check_routing(layer, inp)
+    layer, out = run_layer(qm, inp, min_rows=PATHS[path])
+    check_routing(layer, inp, min_rows=PATHS[path])
     check_out(out, O.forward(inp), inp["cfg"].dtype)
 
 
@@ -163,10 +169,12 @@ def test_zero_tokens_and_growth(qm):
     check_out(out, O.forward(inp), cfg.dtype)
 
 
-def test_graph_capture_replay_matches_eager(qm):
+@pytest.mark.parametrize("path", sorted(PATHS))
+def test_graph_capture_replay_matches_eager(qm, path):
     cfg = CONFIGS["decode_int2"]
     inp = make_inputs(cfg)
     layer = qm.QMoELayer.from_config(cfg)
+    layer.set_gemm_min_rows(PATHS[path])
     layer.reserve(cfg.T)
     x, logits = qm.load_inputs(layer, inp)
     eager = layer.forward(x, logits).clone()
@@ -182,7 +190,13 @@ def test_graph_capture_replay_matches_eager(qm):
     out.zero_()
     g.replay()
     torch.cuda.synchronize()
-    assert torch.equal(out, eager)                   # deterministic
+    if path == "decode":
+        assert torch.equal(out, eager)               # slot-ordered combine: bitwise deterministic
+    else:
+        # fp32 reductions into the combine accumulator: the order of the k
+        # slot additions may differ run to run (a last-bit difference at most
+        # after rounding to D).
+        torch.testing.assert_close(out.float(), eager.float(), rtol=1e-2, atol=1e-2)
     check_out(out, O.forward(inp), cfg.dtype)
 
 
@@ -200,10 +214,12 @@ def test_capture_beyond_reservation_is_refused(qm):
     assert ei.value.status == qm.QMOE_ERR_STATE
 
 
-def test_forward_host_matches_device(qm):
+@pytest.mark.parametrize("path", sorted(PATHS))
+def test_forward_host_matches_device(qm, path):
     cfg = CONFIGS["decode_many_expert_int4"]
     inp = make_inputs(cfg)
     layer = qm.QMoELayer.from_config(cfg)
+    layer.set_gemm_min_rows(PATHS[path])
     layer.reserve(cfg.T)
     x, logits = qm.load_inputs(layer, inp)
     dev = layer.forward(x, logits)
@@ -212,17 +228,25 @@ def test_forward_host_matches_device(qm):
     oh = torch.empty_like(xh).pin_memory()
     layer.forward_host(xh, lh, oh)
     torch.cuda.synchronize()
-    assert torch.equal(oh, dev.cpu())
+    if path == "decode":
+        assert torch.equal(oh, dev.cpu())            # slot-ordered combine: bitwise deterministic
+    else:
+        # fp32 reductions into the combine accumulator: slot order may differ
+        torch.testing.assert_close(oh.float(), dev.cpu().float(), rtol=1e-2, atol=1e-2)
+    check_out(oh, O.forward(inp), cfg.dtype)
 
 
-def test_bounded_wait_reports_timeout_and_context_survives(qm):
-    # Host-injected failure: the first copy stage of every decode warp is armed
-    # but never issued, so its bounded wait runs out.  The kernel records
-    # QMOE_ERR_TIMEOUT, drains its real copies and returns; the context stays
-    # usable and the next forward is correct.
+@pytest.mark.parametrize("path", sorted(PATHS))
+def test_bounded_wait_reports_timeout_and_context_survives(qm, path):
+    # Host-injected failure: the first copy stage of every decode warp (or of
+    # every grouped-GEMM CTA) is armed but never issued, so the bounded waits
+    # on it run out.  The kernel records QMOE_ERR_TIMEOUT, drains its real
+    # copies and returns; the context stays usable and the next forward is
+    # correct.
     cfg = BASE.with_(T=4)
     inp = make_inputs(cfg)
     layer = qm.QMoELayer.from_config(cfg)
+    layer.set_gemm_min_rows(PATHS[path])
     x, logits = qm.load_inputs(layer, inp)
     layer.set_wait_limit(2000)
     layer.inject_stall(True)

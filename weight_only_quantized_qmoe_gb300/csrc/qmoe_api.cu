@@ -51,7 +51,7 @@ struct qmoe_layer {
   int normalize = 1;
   float zp_offset = NAN;
   bool offset_set = false;
-  int gemm_min_rows = 32;
+  int gemm_min_rows = 0;
   int device = -1;
   long long wait_limit = kDefaultWaitLimit;
   int inject_stall = 0;
@@ -547,6 +547,7 @@ qmoe_status qmoe_forward(qmoe_layer* l, const void* x, const float* logits, void
         ga.k = l->k;
         ga.N_out = f == 0 ? l->I : l->H;
         ga.wait = wait;
+        ga.inject_stall = l->inject_stall;
         QMOE_CUDA(l, launch_gemm(ga, s), "launch grouped GEMM");
       }
     }

@@ -146,10 +146,13 @@ cudaError_t launch_repack_gemm(const GemmRepackArgs& a, cudaStream_t s) {
 // Gather of x into the tiled token layout (fc1 B operand), and the combine of
 // the fp32 accumulator.
 // ----------------------------------------------------------------------------
-// One CTA per GEMM-class item: rows c < rows of the item, 16-byte chunks of
-// 8 values; chunks past H (K padding up to 64) are written as zeros.  Rows
-// past the item's count are left as they are: they only feed token columns
-// that the epilogue never stores.
+// kGatherParts CTAs per GEMM-class item (grid y), each taking every
+// kGatherParts-th group of 16-byte chunks (8 values) of the item's rows;
+// chunks past H (K padding up to 64) and rows past the item's count up to the
+// next multiple of 8 (copied with the tile) are written as zeros, so the MMA
+// never reads undefined values.
+constexpr int kGatherParts = 8;
+
 __global__ void __launch_bounds__(256) gather_tiles_kernel(const void* __restrict__ x, const int* __restrict__ perm,
                                                            int k, int H, const Item* __restrict__ items,
                                                            const int* __restrict__ n_items, uint8_t* __restrict__ xt) {
@@ -160,20 +163,21 @@ __global__ void __launch_bounds__(256) gather_tiles_kernel(const void* __restric
   const int cpr = ksteps * 8;                 // chunks per row (padded)
   const int hv = H / 8;                       // real chunks per row
   const uint4* src = static_cast<const uint4*>(x);
-  const int n = it.rows * cpr;
+  const int n = ((it.rows + 7) & ~7) * cpr;   // rows up to a multiple of 8 (the copy unit)
   constexpr int U = 4;
-  for (int base = threadIdx.x; base < n; base += U * blockDim.x) {
+  const int stride = (int)(gridDim.y * blockDim.x);
+  for (int base = (int)(blockIdx.y * blockDim.x + threadIdx.x); base < n; base += U * stride) {
     uint4 v[U];
     int cc[U], ch[U];
 #pragma unroll
     for (int u = 0; u < U; ++u) {
-      const int i = base + u * blockDim.x;
+      const int i = base + u * stride;
       cc[u] = -1;
       if (i < n) {
         cc[u] = i / cpr;
         ch[u] = i % cpr;
         v[u] = make_uint4(0u, 0u, 0u, 0u);
-        if (ch[u] < hv) {
+        if (ch[u] < hv && cc[u] < it.rows) {
           const int t = perm[it.start + cc[u]] / k;
           v[u] = src[(size_t)t * hv + ch[u]];
         }
@@ -197,7 +201,7 @@ cudaError_t launch_gather_tiles(const void* x, const int* perm, int k, int H, co
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.gridDim = dim3(max_items);
+  cfg.gridDim = dim3(max_items, kGatherParts);
   cfg.blockDim = dim3(256);
   cfg.stream = s;
   cfg.attrs = attr;
@@ -553,6 +557,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     tmem_alloc(tmem_holder, kTmemCols);
     tmem_relinquish();
   }
+  // The MMA reads N >= 64 token rows of a stage, more than a small item
+  // copies; the rows past the copy must hold finite values (zero here, or
+  // rows of an earlier copy), never undefined shared memory.
+  for (int i = threadIdx.x; i < kStages * kBBytes / 16; i += blockDim.x)
+    reinterpret_cast<uint4*>(bring)[i] = make_uint4(0u, 0u, 0u, 0u);
+  fence_proxy_async_smem();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -584,8 +594,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           if (!ok) break;
         }
         mbar_arrive_expect_tx_elect(&full[s], tx);
-        bulk_g2s_elect(wring + s * wstage, src.w + (size_t)kr * L.stage_bytes, (uint32_t)L.stage_bytes, &full[s]);
-        bulk_g2s_elect(bring + s * kBBytes, src.b + (size_t)kr * kTokTileBytes, src.b_bytes, &full[s]);
+        // Test hook: stage 0's barrier is armed but its copies are never
+        // issued, so the waits on it can only run out (host-injected failure).
+        if (!(a.inject_stall && kc == 0)) {
+          bulk_g2s_elect(wring + s * wstage, src.w + (size_t)kr * L.stage_bytes, (uint32_t)L.stage_bytes, &full[s]);
+          bulk_g2s_elect(bring + s * kBBytes, src.b + (size_t)kr * kTokTileBytes, src.b_bytes, &full[s]);
+        }
         issued = kc + 1;
         if (++kr == L.ksteps) kr = 0;
       }
@@ -595,8 +609,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       // leaves (fixed large bound).  A stage's phase completes on the bytes
       // alone, whatever the consumers did.
       const WaitCfg drain{a.wait.status, kDrainWaitLimit};
-      for (int i = issued > kStages ? issued - kStages : 0; i < issued; ++i)
+      for (int i = issued > kStages ? issued - kStages : 0; i < issued; ++i) {
+        if (a.inject_stall && i == 0) continue;   // no copy was issued for it
         mbar_wait_bounded(&full[i % kStages], (i / kStages) & 1, drain);
+      }
     }
   } else if (warp == 1) {
     // ---------------- MMA issuer: the whole warp, one elected lane issues ----------------
@@ -732,9 +748,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           for (int u2 = 0; u2 < 2; ++u2) {
             const int vec = lane + 32 * u2, tok = vec >> 1, hv = vec & 1;
             const int c = c0 + tok, n = nbase + 8 * hv;
-            if (c < it.rows && n < a.h_ksteps * 64) {
+            // rows up to the next multiple of 8 are copied with the tile:
+            // the ones past the item's count are written as zeros
+            if (c < ((it.rows + 7) & ~7) && n < a.h_ksteps * 64) {
               uint4 val = make_uint4(0u, 0u, 0u, 0u);
-              if (n < a.N_out) val = *reinterpret_cast<const uint4*>(t16 + tok * 16 + hv * 8);
+              if (c < it.rows && n < a.N_out) val = *reinterpret_cast<const uint4*>(t16 + tok * 16 + hv * 8);
               uint8_t* dst = a.htiles + tok_tile_offset(item, a.h_ksteps, n >> 6) + c * 128 +
                              ((((n & 63) >> 3) ^ (c & 7)) << 4);
               *reinterpret_cast<uint4*>(dst) = val;

@@ -62,6 +62,7 @@ struct GemmArgs {
   int k;
   int N_out;               // I (fc1) or H (fc2)
   WaitCfg wait;
+  int inject_stall;         // test hook: arm the first stage's barrier, never issue its copies
 };
 
 cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t s);

@@ -147,14 +147,24 @@ __global__ void __launch_bounds__(1024) group_kernel(const RouteArgs a, int do_r
   __syncthreads();
 
   // Pass 1: each warp counts its contiguous segment of routes per expert.
+  // Loads are issued kU 32-route groups at a time so their latencies overlap.
+  constexpr int kU = 8;
   const int seg = (((R + 31) / 32) + 31) & ~31;
   const int beg = warp * seg, end = min(R, beg + seg);
-  for (int base = beg; base < end; base += 32) {
-    const int r = base + lane;
-    const int e = r < end ? a.ids[r] : -1;
-    const unsigned peers = __match_any_sync(0xffffffffu, e);
-    if (e >= 0 && lane == __ffs(peers) - 1) cnt[warp * E + e] += __popc(peers);
-    __syncwarp();
+  for (int base = beg; base < end; base += 32 * kU) {
+    int ev[kU];
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      const int r = base + 32 * u + lane;
+      ev[u] = r < end ? a.ids[r] : -1;
+    }
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      const int e = ev[u];
+      const unsigned peers = __match_any_sync(0xffffffffu, e);
+      if (e >= 0 && lane == __ffs(peers) - 1) cnt[warp * E + e] += __popc(peers);
+      __syncwarp();
+    }
   }
   __syncthreads();
 
@@ -181,18 +191,27 @@ __global__ void __launch_bounds__(1024) group_kernel(const RouteArgs a, int do_r
 
   // Pass 2: stable placement, walking each segment in route order.
   const unsigned lt = (1u << lane) - 1u;
-  for (int base = beg; base < end; base += 32) {
-    const int r = base + lane;
-    const int e = r < end ? a.ids[r] : -1;
-    const unsigned peers = __match_any_sync(0xffffffffu, e);
-    if (e >= 0) {
-      const int p = cnt[warp * E + e] + __popc(peers & lt);
-      a.perm[p] = r;
-      a.pos[r] = p;
+  for (int base = beg; base < end; base += 32 * kU) {
+    int ev[kU];
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      const int r = base + 32 * u + lane;
+      ev[u] = r < end ? a.ids[r] : -1;
     }
-    __syncwarp();
-    if (e >= 0 && lane == __ffs(peers) - 1) cnt[warp * E + e] += __popc(peers);
-    __syncwarp();
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      const int r = base + 32 * u + lane;
+      const int e = ev[u];
+      const unsigned peers = __match_any_sync(0xffffffffu, e);
+      if (e >= 0) {
+        const int p = cnt[warp * E + e] + __popc(peers & lt);
+        a.perm[p] = r;
+        a.pos[r] = p;
+      }
+      __syncwarp();
+      if (e >= 0 && lane == __ffs(peers) - 1) cnt[warp * E + e] += __popc(peers);
+      __syncwarp();
+    }
   }
 
   // Work-lists: class 0 (decode kernel) for experts with 1..threshold rows,
