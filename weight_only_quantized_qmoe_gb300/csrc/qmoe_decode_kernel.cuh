@@ -171,7 +171,8 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
   int i = 0;
   for (; i < nst; ++i) {
     const int slot = i % stages;
-    if (!mbar_wait_bounded(&bar[slot], (uint32_t)((i / stages) & 1), a.wait)) {
+    // every lane polls; the warp continues (or gives up) as one
+    if (!__all_sync(0xffffffffu, mbar_wait_bounded(&bar[slot], (uint32_t)((i / stages) & 1), a.wait))) {
       ok = false;
       break;
     }

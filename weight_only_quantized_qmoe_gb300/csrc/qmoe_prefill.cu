@@ -348,6 +348,15 @@ __device__ __forceinline__ uint32_t idesc_f16(bool bf16, int M, int N) {
   return d;
 }
 
+// One poll of a phase whose answer is the same for the whole warp: every lane
+// polls, lane 0's answer is broadcast.  (Each lane acting on its own answer
+// can split the warp when the phase completes during the poll; the split
+// halves would then reach different warp-synchronous instructions.)
+__device__ __forceinline__ bool warp_test_wait(uint64_t* bar, uint32_t parity) {
+  const int done = mbar_test_wait(bar, parity) ? 1 : 0;
+  return __shfl_sync(0xffffffffu, done, 0) != 0;
+}
+
 // Bounded wait that also gives up when another role has aborted.
 __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, const WaitCfg& w,
                                               volatile int* abort_flag) {
@@ -387,13 +396,17 @@ __device__ __forceinline__ bool spin_or_abort(uint64_t* bar, uint32_t parity, co
 //   empty[s] the MMAs of the step have completed                (tcgen05.commit)
 // producer: empty -> copies -> full;  dequant: full -> A -> ready;
 // MMA: ready -> MMAs -> commit empty.
-constexpr int kStages = 8;
+constexpr int kStages = 6;
 constexpr int kTileN = 128;       // token rows per tile (MMA N <= 128)
 constexpr int kBBytes = kTileN * 128;
 constexpr int kTmemCols = 512;
 constexpr int kAccCols = 128;     // two accumulators: columns [0,128) and [128,256)
 constexpr int kAcol0 = 256;       // first TMEM column of the A ring
 constexpr int kDeqGroups = 3;     // dequant warp groups (4 warps each), k-step kc -> group kc % 3
+// Each stage is always dequantised by the same group (stage s -> group s % 3),
+// so a group consumes its stages' phases in order and never runs a ring ahead
+// of a fill that has not landed (a parity test could not tell those apart).
+static_assert(kStages % kDeqGroups == 0, "a stage belongs to one dequant group");
 constexpr int kEpiWarp0 = 4 + 4 * kDeqGroups;
 constexpr int kGemmThreads = (kEpiWarp0 + 4) * 32;  // see the role map in the kernel
 constexpr int kEpiPitch = 36;     // fp32 words per row of an epilogue transpose tile (pad: banks)
@@ -583,12 +596,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       const uint32_t tx = (uint32_t)L.stage_bytes + src.b_bytes;
       int kr = src.rot;
       for (int ks = 0; ks < L.ksteps; ++ks, ++kc) {
-        const int s = kc & (kStages - 1);
+        const int s = kc % kStages;
         const uint32_t par = ((uint32_t)(kc / kStages) & 1u) ^ 1u;
         // Parked (not spinning) wait: the producer runs a ring's depth ahead
         // of the MMAs, and a spinning poll competes with them for the
         // barrier unit.
-        if (!mbar_test_wait(&empty[s], par)) {
+        if (!warp_test_wait(&empty[s], par)) {
           ok = wait_or_abort(&empty[s], par, a.wait, abort_flag);
           ok = __shfl_sync(0xffffffffu, ok, 0);
           if (!ok) break;
@@ -616,10 +629,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
   } else if (warp == 1) {
     // ---------------- MMA issuer: the whole warp, one elected lane issues ----------------
-    static_assert((kStages & (kStages - 1)) == 0, "ring depth is a power of two");
     const uint32_t a0 = tmem + kAcol0;
     const uint64_t bdesc0 = smem_desc_sw128(smem_u32(bring));
-    int kc = 0, tc = 0;
+    int st = 0, tc = 0;       // ring stage of the next k-step, tile count
+    uint32_t ph = 0;          // phase parity of that stage's current use
     bool ok = true;
     for (int tile = blockIdx.x; tile < total_tiles && ok; tile += gridDim.x, ++tc) {
       const Item it = a.items[tile / L.ntiles];
@@ -642,10 +655,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       while (ks < L.ksteps && ok) {
 #pragma unroll
         for (int u = 0; u < kStages; ++u) {
-          if (u == (kc & (kStages - 1)) && ks < L.ksteps && ok) {
-            const uint32_t par = (uint32_t)(kc / kStages) & 1u;
-            if (!mbar_test_wait(&ready[u], par)) {
-              ok = spin_or_abort(&ready[u], par, a.wait, abort_flag);
+          if (u == st && ks < L.ksteps && ok) {
+            if (!warp_test_wait(&ready[u], ph)) {
+              ok = spin_or_abort(&ready[u], ph, a.wait, abort_flag);
               ok = __shfl_sync(0xffffffffu, ok, 0);
             }
             if (ok) {
@@ -653,8 +665,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
               umma_ts_x4_elect(dacc, a0 + 32 * u, bdesc0 + (uint64_t)(u * (kBBytes >> 4)), idesc,
                                ks != 0 ? 1u : 0u);
               tc_commit_elect(&empty[u]);
-              ++kc;
               ++ks;
+              if (++st == kStages) {
+                st = 0;
+                ph ^= 1u;
+              }
             }
           }
         }
@@ -678,7 +693,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const int n_steps = ((total_tiles - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x) * L.ksteps;
     bool ok = true;
     for (int kc = grp; kc < n_steps && ok; kc += kDeqGroups) {
-      const int s = kc & (kStages - 1);
+      // kStages is a multiple of kDeqGroups, so every use of stage s falls
+      // to this one group, in order: the parity of full[s] names one phase.
+      const int s = kc % kStages;
       ok = wait_or_abort(&full[s], (kc / kStages) & 1, a.wait, abort_flag);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
@@ -722,6 +739,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           my_tok = route / a.k;
           my_w = a.w[route];
         }
+        __syncwarp();   // converged again before the warp-wide tcgen05.wait
         tc_wait_ld();
         if (GLU) {
           // lanes 2p / 2p+1 hold gate / up of feature n = nt*64 + q*16 + p
