@@ -600,8 +600,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         const uint32_t par = ((uint32_t)(kc / kStages) & 1u) ^ 1u;
         // Parked (not spinning) wait: the producer runs a ring's depth ahead
         // of the MMAs, and a spinning poll competes with them for the
-        // barrier unit.
-        if (!warp_test_wait(&empty[s], par)) {
+        // barrier unit.  The first poll is one warp-wide instruction (a
+        // lane-0 broadcast here cost 4-9 % of the kernel time).
+        if (!mbar_test_wait(&empty[s], par)) {
           ok = wait_or_abort(&empty[s], par, a.wait, abort_flag);
           ok = __shfl_sync(0xffffffffu, ok, 0);
           if (!ok) break;
