@@ -26,7 +26,8 @@ in float64, written from these pages:
 Readings where the pages leave a step open (also listed in the design notes):
 selection is on the fp32 logits (equal to selection on the exact softmax,
 which is strictly increasing); fc1 rows are concatenated ``[gate | up]``;
-scales are stored in the activation type D; intermediates (fc1 output,
+scales are stored in the activation type D; biases are fp32 (qmoe.rs);
+the SwiGLU attributes do not apply to GeGLU; intermediates (fc1 output,
 activation, fc2 output) stay unrounded in float64; the int3 stream is one
 LSB-first bit stream per row.
 
@@ -218,13 +219,34 @@ def gelu_tanh(g):
     return 0.5 * g * (1.0 + np.tanh(0.7978845608028654 * (g + 0.044715 * g * g * g)))
 
 
-def glu(a, inter: int, act: str):
-    """Concatenated gate/up GLU: gate = a[:, :I], up = a[:, I:2I]
-    (qmoe.rs ``qmoe_activate`` with swiglu_fusion == 2; GeGLU replaces the
-    SiLU gate by tanh-GELU, PR "fused int2 ...")."""
-    gate, up = a[:, :inter], a[:, inter:2 * inter]
-    f = silu if act == "swiglu" else gelu_tanh
-    return f(gate) * up
+def swiglu(g, u, alpha: float = 1.0, beta: float = 0.0, limit: float = float("inf")):
+    """qmoe.rs ``swiglu_value``: the gate is bounded above by ``limit``, the
+    linear half clamped to [-limit, limit]; then
+    ``g' * sigmoid(alpha * g') * (u' + beta)``.  With the attribute defaults
+    (alpha 1, beta 0, no limit) this is ``silu(g) * u``."""
+    g = np.minimum(np.asarray(g, dtype=np.float64), limit)
+    u = np.clip(np.asarray(u, dtype=np.float64), -limit, limit)
+    return g / (1.0 + np.exp(-alpha * g)) * (u + beta)
+
+
+def split_gate_up(a, inter: int, layout: str = "concat"):
+    """Gate and up halves of fc1's output (qmoe.rs ``qmoe_activate``):
+    swiglu_fusion == 2 concatenates them (gate = a[:, :I], up = a[:, I:]),
+    swiglu_fusion == 1 interleaves them (gate = a[:, 2f], up = a[:, 2f+1])."""
+    if layout == "interleaved":
+        return a[:, 0:2 * inter:2], a[:, 1:2 * inter:2]
+    return a[:, :inter], a[:, inter:2 * inter]
+
+
+def glu(a, inter: int, act: str, layout: str = "concat", alpha: float = 1.0, beta: float = 0.0,
+        limit: float = float("inf")):
+    """Gated activation of fc1's output: SwiGLU with the qmoe.rs attributes,
+    or GeGLU (tanh-GELU gate times up; PR "fused int2 ..."; the SwiGLU
+    attributes do not apply to it)."""
+    gate, up = split_gate_up(a, inter, layout)
+    if act == "swiglu":
+        return swiglu(gate, up, alpha, beta, limit)
+    return gelu_tanh(gate) * up
 
 
 # ----------------------------------------------------------------------------
@@ -249,6 +271,14 @@ def expert_weights(inputs: dict, fc: int, e: int) -> np.ndarray:
         None if zp is None else np.asarray(zp[e]), cfg.zp_offset)
 
 
+def projection_bias(inputs: dict, fc: int, e: int):
+    """fp32 bias row of expert e added to the projection output (qmoe.rs
+    ``qmoe_linear_impl``: ``output = value + bias[expert * out + feature]``),
+    or 0 without biases."""
+    b = inputs.get("fc1_bias" if fc == 1 else "fc2_bias")
+    return 0.0 if b is None else to_f64(b[e])
+
+
 def routing(inputs: dict):
     """Selection, weights, grouping for all tokens."""
     cfg = inputs["cfg"]
@@ -264,8 +294,8 @@ def forward(inputs: dict, tokens=None, round_h: bool = False, return_parts: bool
     """The QMoE layer forward on float64 data.
 
     ``out[t, m] = R_D( sum_j w[t, j] * y[t*k + j, m] )`` (slot order j) with
-    ``y[r] = W2_e @ act_glu(W1_e @ x[t])`` for route r = t*k + j of expert
-    e = ids[t, j].  ``tokens`` restricts the output to a subset of token rows
+    ``y[r] = W2_e @ act_glu(W1_e @ x[t] + b1_e) + b2_e`` for route r = t*k + j
+    of expert e = ids[t, j] (biases zero unless given).  ``tokens`` restricts the output to a subset of token rows
     (routing is still computed for all tokens).  ``round_h`` rounds the
     activation to D before fc2 (only to measure that gap; off by default).
     """
@@ -282,11 +312,11 @@ def forward(inputs: dict, tokens=None, round_h: bool = False, return_parts: bool
     for e in sorted(need):
         rows = need[e]
         xe = x[[t for t, _ in rows]]                       # [M_e, H]
-        a = xe @ expert_weights(inputs, 1, e).T            # [M_e, 2I]
-        h = glu(a, cfg.I, cfg.act)
+        a = xe @ expert_weights(inputs, 1, e).T + projection_bias(inputs, 1, e)   # [M_e, 2I]
+        h = glu(a, cfg.I, cfg.act, cfg.fc1_layout, cfg.swiglu_alpha, cfg.swiglu_beta, cfg.swiglu_limit)
         if round_h:
             h = round_to_dtype(h, cfg.dtype)
-        ye = h @ expert_weights(inputs, 2, e).T            # [M_e, H]
+        ye = h @ expert_weights(inputs, 2, e).T + projection_bias(inputs, 2, e)  # [M_e, H]
         for (t, j), row in zip(rows, ye):
             y[(t, j)] = row
     out = np.zeros((len(tokens), cfg.H))

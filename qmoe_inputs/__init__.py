@@ -25,7 +25,9 @@ and ``decode_affine_weight``):
 * ``zp``     uint8 ``[E, N, ceil((K/B)*bits/8)]``: LSB-first bit stream of the
   K/B per-block zero points, at the weight bit width (only in ``uint8`` mode).
 
-fc1 rows are ``[gate (I rows) | up (I rows)]`` (concatenated gate/up).
+fc1 rows are ``[gate (I rows) | up (I rows)]`` (concatenated gate/up), or
+interleaved (row 2f = gate f, row 2f+1 = up f) when ``fc1_layout`` says so.
+Optional projection biases are float32 ``[E, N]`` in the same row order.
 """
 from __future__ import annotations
 
@@ -63,6 +65,16 @@ class QMoEConfig:
     zp_hi: int = 0
     logit_sigma: float = 1.0
     zipf_bias: float = 0.0  # logits[t, e] += zipf_bias * log(1 / (e + 1))
+    # fc1 row order: "concat" ([gate (I rows) | up (I rows)]) or "interleaved"
+    # (row 2f = gate f, row 2f+1 = up f)
+    fc1_layout: str = "concat"
+    # SwiGLU attributes: h = min(g, L) * sigmoid(alpha * min(g, L)) * (clamp(u, -L, L) + beta)
+    swiglu_alpha: float = 1.0
+    swiglu_beta: float = 0.0
+    swiglu_limit: float = float("inf")
+    # fp32 projection biases ([E, 2I] for fc1 in its row order, [E, H] for fc2)
+    bias: bool = False
+    bias_sigma: float = 0.05
 
     def with_(self, **kw) -> "QMoEConfig":
         return dataclasses.replace(self, **kw)
@@ -154,12 +166,17 @@ def make_inputs(cfg: QMoEConfig, T: Optional[int] = None) -> dict:
     x = _cast(rng.standard_normal((T, cfg.H), dtype=np.float32), cfg.dtype)
     fc1 = _projection(rng, cfg, 2 * cfg.I, cfg.H, cfg.bits1)
     fc2 = _projection(rng, cfg, cfg.H, cfg.I, cfg.bits2)
+    b1 = b2 = None
+    if cfg.bias:   # drawn after everything else: the other streams do not move
+        b1 = torch.from_numpy((rng.standard_normal((cfg.E, 2 * cfg.I)) * cfg.bias_sigma).astype(np.float32))
+        b2 = torch.from_numpy((rng.standard_normal((cfg.E, cfg.H)) * cfg.bias_sigma).astype(np.float32))
     return {
         "cfg": cfg.with_(T=T),
         "logits": torch.from_numpy(np.ascontiguousarray(logits)),
         "x": x,
         "fc1_codes": fc1[0], "fc1_scales": fc1[1], "fc1_zp": fc1[2],
         "fc2_codes": fc2[0], "fc2_scales": fc2[1], "fc2_zp": fc2[2],
+        "fc1_bias": b1, "fc2_bias": b2,
     }
 
 

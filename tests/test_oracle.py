@@ -208,6 +208,33 @@ def test_dequant_block_indexing_and_rounding():
             assert W[n, d] == ref
 
 
+def test_swiglu_attributes_match_a_torch_restatement():
+    # g' sigmoid(alpha g') == silu(alpha g') / alpha, computed by torch
+    g = torch.linspace(-9, 9, 181, dtype=torch.float64)[:, None]
+    u = torch.linspace(-5, 5, 41, dtype=torch.float64)[None, :]
+    for alpha, beta, limit in [(1.0, 0.0, float("inf")), (1.702, 1.0, 7.0), (0.5, -0.25, 1.5), (3.0, 2.0, 0.1)]:
+        gb = torch.clamp(g, max=limit)
+        ref = torch.nn.functional.silu(alpha * gb) / alpha * (torch.clamp(u, -limit, limit) + beta)
+        np.testing.assert_allclose(O.swiglu(g.numpy(), u.numpy(), alpha, beta, limit), ref.numpy(),
+                                   rtol=1e-13, atol=1e-300)
+    # attribute defaults: plain silu(g) * u
+    np.testing.assert_allclose(O.swiglu(g.numpy(), u.numpy()),
+                               (torch.nn.functional.silu(g) * u).numpy(), rtol=1e-15, atol=1e-300)
+
+
+def test_interleaved_layout_is_a_row_permutation_of_concat():
+    # Interleaved rows (2f = gate f, 2f+1 = up f) moved to [gate | up] give the
+    # same layer.
+    cfg = CONFIGS["tiny"].with_(fc1_layout="interleaved", bias=True, H=64, I=32, E=3, k=2)
+    inp = make_inputs(cfg)
+    order = np.concatenate([np.arange(0, 64, 2), np.arange(1, 64, 2)])
+    cat = dict(inp)
+    cat["cfg"] = cfg.with_(fc1_layout="concat")
+    for key in ("fc1_codes", "fc1_scales", "fc1_bias"):
+        cat[key] = inp[key][:, order]
+    np.testing.assert_array_equal(O.forward(inp), O.forward(cat))
+
+
 def test_activations_match_torch():
     g = torch.linspace(-12, 12, 2001, dtype=torch.float64)
     np.testing.assert_allclose(O.silu(g.numpy()), torch.nn.functional.silu(g).numpy(), rtol=1e-15, atol=1e-300)
@@ -263,16 +290,24 @@ def _brute_layer(inp):
             if e not in W1:
                 W1[e] = [[weight(1, e, n, d) for d in range(cfg.H)] for n in range(2 * cfg.I)]
                 W2[e] = [[weight(2, e, n, d) for d in range(cfg.I)] for n in range(cfg.H)]
-            a = [sum(W1[e][n][d] * x[t][d] for d in range(cfg.H)) for n in range(2 * cfg.I)]
+            b1 = inp["fc1_bias"][e].tolist() if inp.get("fc1_bias") is not None else [0.0] * (2 * cfg.I)
+            b2 = inp["fc2_bias"][e].tolist() if inp.get("fc2_bias") is not None else [0.0] * cfg.H
+            a = [sum(W1[e][n][d] * x[t][d] for d in range(cfg.H)) + b1[n] for n in range(2 * cfg.I)]
             h = []
             for n in range(cfg.I):
-                g, u = a[n], a[cfg.I + n]
+                if cfg.fc1_layout == "interleaved":
+                    g, u = a[2 * n], a[2 * n + 1]
+                else:
+                    g, u = a[n], a[cfg.I + n]
                 if cfg.act == "swiglu":
-                    h.append(g / (1 + math.exp(-g)) * u)
+                    L = cfg.swiglu_limit
+                    g = min(g, L)
+                    u = max(-L, min(L, u))
+                    h.append(g / (1 + math.exp(-cfg.swiglu_alpha * g)) * (u + cfg.swiglu_beta))
                 else:
                     h.append(0.5 * g * (1 + math.tanh(math.sqrt(2 / math.pi) * (g + 0.044715 * g ** 3))) * u)
             for mm in range(cfg.H):
-                acc[mm] += p[e] / den * sum(W2[e][mm][n] * h[n] for n in range(cfg.I))
+                acc[mm] += p[e] / den * (sum(W2[e][mm][n] * h[n] for n in range(cfg.I)) + b2[mm])
         out.append([_bf_round(v, cfg.dtype) for v in acc])
     return np.array(out)
 
@@ -285,6 +320,13 @@ SMALL_VARIANTS = {
     "int3_int4_unnorm": dict(bits1=3, bits2=4, normalize=False, dtype="bf16", H=64, I=64, E=5, k=2),
     "int3_uint8_int2": dict(bits1=3, bits2=2, zp_mode="uint8", zp_lo=0, zp_hi=3, dtype="bf16",
                             H=64, I=64, E=3, k=3),
+    # qmoe.rs swiglu_fusion == 1 (interleaved gate/up), SwiGLU alpha / beta /
+    # limit (the limit clamps a good share of the gates here), fp32 biases
+    "interleaved_bias_swiglu_params": dict(fc1_layout="interleaved", bias=True, swiglu_alpha=1.702,
+                                           swiglu_beta=1.0, swiglu_limit=0.3, dtype="bf16",
+                                           H=64, I=64, E=4, k=2),
+    "bias_geglu_f16": dict(act="geglu", bias=True, bits1=2, bits2=2, zp_mode="offset", zp_offset=1.5,
+                           dtype="f16", H=64, I=64, B=64, scale_lo=0.01, scale_hi=0.05),
 }
 
 
@@ -367,7 +409,33 @@ def _layer_pin_fails(monkeypatch, name, fake):
 def test_planted_swapped_gate_up_is_caught(monkeypatch):
     real = O.glu
     assert _layer_pin_fails(monkeypatch, "glu",
-                            lambda a, inter, act: real(np.concatenate([a[:, inter:], a[:, :inter]], 1), inter, act))
+                            lambda a, inter, act, *r: real(np.concatenate([a[:, inter:], a[:, :inter]], 1),
+                                                           inter, act, *r))
+
+
+def _variant_pin_fails(monkeypatch, variant, name, fake):
+    monkeypatch.setattr(O, name, fake)
+    cfg = CONFIGS["tiny"].with_(**SMALL_VARIANTS[variant])
+    inp = make_inputs(cfg)
+    ulp = {"f32": 2.0 ** -23, "f16": 2.0 ** -10, "bf16": 2.0 ** -7}[cfg.dtype]
+    return not np.allclose(O.forward(inp), _brute_layer(inp), rtol=ulp, atol=1e-30)
+
+
+def test_planted_dropped_bias_is_caught(monkeypatch):
+    assert _variant_pin_fails(monkeypatch, "interleaved_bias_swiglu_params", "projection_bias",
+                              lambda inputs, fc, e: 0.0)
+
+
+def test_planted_ignored_interleave_is_caught(monkeypatch):
+    real = O.split_gate_up
+    assert _variant_pin_fails(monkeypatch, "interleaved_bias_swiglu_params", "split_gate_up",
+                              lambda a, inter, layout="concat": real(a, inter, "concat"))
+
+
+def test_planted_ignored_limit_is_caught(monkeypatch):
+    real = O.swiglu
+    assert _variant_pin_fails(monkeypatch, "interleaved_bias_swiglu_params", "swiglu",
+                              lambda g, u, alpha=1.0, beta=0.0, limit=float("inf"): real(g, u, alpha, beta))
 
 
 def test_planted_wrong_zero_point_is_caught(monkeypatch):
