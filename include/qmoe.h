@@ -121,6 +121,29 @@ qmoe_status qmoe_set_routing(qmoe_layer* layer, int normalize);
  * in that mode. */
 qmoe_status qmoe_set_zero_point_offset(qmoe_layer* layer, float offset);
 
+/* SwiGLU attributes [qmoe.rs swiglu_value]: with g = gate, u = up,
+ *   h = min(g, limit) * sigmoid(alpha * min(g, limit)) * (clamp(u, -limit, limit) + beta)
+ * (a NaN in u is kept).  Defaults alpha = 1, beta = 0, limit = +inf: plain
+ * silu(g) * u.  GeGLU ignores them.  alpha must be finite and nonzero, beta
+ * finite, limit > 0 (+inf allowed); otherwise INVALID_ARG.  May be called at
+ * any time; it applies to later forwards. */
+qmoe_status qmoe_set_swiglu_params(qmoe_layer* layer, float alpha, float beta, float limit);
+
+/* Row order of fc1's canonical codes / scales / zero points / bias
+ * [qmoe.rs qmoe_activate, swiglu_fusion]: 0 = concatenated [gate (I rows) |
+ * up (I rows)] (default, swiglu_fusion 2), 1 = interleaved (row 2f = gate f,
+ * row 2f+1 = up f; swiglu_fusion 1).  Must precede qmoe_prepack(fc = 1) and
+ * qmoe_set_bias(fc = 1); STATE otherwise. */
+qmoe_status qmoe_set_fc1_layout(qmoe_layer* layer, int interleaved);
+
+/* Projection biases [qmoe.rs qmoe_linear_impl: output = sum + bias[e*N + n]]:
+ * bias_dev is a float32 device array [E, N] (fc1: N = 2*inter in the fc1 row
+ * order; fc2: N = hidden), added to the projection output (fc1 before the
+ * gated activation, fc2 before the weighted combine).  The layer keeps its own
+ * copy (the caller may free bias_dev once `stream` has been synchronised).
+ * NULL removes the bias (synchronises `stream` first). */
+qmoe_status qmoe_set_bias(qmoe_layer* layer, int fc, const float* bias_dev, void* stream);
+
 /* Experts with more than `min_rows` routed rows take the tensor-core grouped
  * GEMM; the others the mma.sync weight-streaming decode kernel.  Any value
  * gives the same result within tolerance.  Default 0: every expert takes the

@@ -85,6 +85,24 @@ def test_prepack_and_forward_state_checks(lib):
     b.qmoe_destroy(h)
 
 
+def test_activation_layout_and_bias_argument_checks(lib):
+    st, h = _create()
+    inf = float("inf")
+    assert b.qmoe_set_swiglu_params(h, 1.702, 1.0, 7.0) == b.QMOE_OK
+    assert b.qmoe_set_swiglu_params(h, 1.0, 0.0, inf) == b.QMOE_OK         # the defaults
+    assert b.qmoe_set_swiglu_params(h, float("nan"), 0.0, 1.0) == b.QMOE_ERR_INVALID_ARG
+    assert b.qmoe_set_swiglu_params(h, 0.0, 0.0, 1.0) == b.QMOE_ERR_INVALID_ARG
+    assert b.qmoe_set_swiglu_params(h, 1.0, inf, 1.0) == b.QMOE_ERR_INVALID_ARG
+    assert b.qmoe_set_swiglu_params(h, 1.0, 0.0, 0.0) == b.QMOE_ERR_INVALID_ARG
+    assert b.qmoe_set_swiglu_params(h, 1.0, 0.0, -1.0) == b.QMOE_ERR_INVALID_ARG
+    assert b.qmoe_set_fc1_layout(h, 1) == b.QMOE_OK
+    assert b.qmoe_set_fc1_layout(h, 0) == b.QMOE_OK
+    assert b.qmoe_set_fc1_layout(h, 2) == b.QMOE_ERR_INVALID_ARG
+    assert b.qmoe_set_bias(h, 3, 16, 0) == b.QMOE_ERR_INVALID_ARG
+    assert b.qmoe_set_bias(h, 1, 0, 0) == b.QMOE_OK                       # removing none is fine
+    b.qmoe_destroy(h)
+
+
 def test_status_strings(lib):
     assert b.qmoe_status_string(b.QMOE_OK) == "QMOE_OK"
     assert b.qmoe_status_string(b.QMOE_ERR_TIMEOUT) == "QMOE_ERR_TIMEOUT"

@@ -121,6 +121,31 @@ VARIANTS = {
 }
 
 
+# qmoe.rs swiglu_fusion 1 (interleaved gate/up), SwiGLU alpha / beta / limit
+# (the limit clamps many gates and up values at these sizes) and fp32 biases,
+# on both projection paths and the fp32 SIMT path.
+FEATURE_VARIANTS = {
+    "interleaved_bias_swiglu_params": dict(fc1_layout="interleaved", bias=True, swiglu_alpha=1.702,
+                                           swiglu_beta=1.0, swiglu_limit=0.3, T=13),
+    "bias_geglu_int2_offset_f16": dict(act="geglu", bias=True, bits1=2, bits2=2, zp_mode="offset",
+                                       zp_offset=1.5, dtype="f16", B=128, T=9),
+    "interleaved_uint8_T150": dict(fc1_layout="interleaved", zp_mode="uint8", zp_lo=5, zp_hi=11,
+                                   E=4, T=150),
+    "f32_interleaved_bias_params": dict(dtype="f32", fc1_layout="interleaved", bias=True,
+                                        swiglu_alpha=1.702, swiglu_beta=1.0, swiglu_limit=0.3, T=7),
+}
+
+
+@pytest.mark.parametrize("path", sorted(PATHS))
+@pytest.mark.parametrize("name", list(FEATURE_VARIANTS))
+def test_feature_parity(qm, name, path):
+    cfg = BASE.with_(**FEATURE_VARIANTS[name])
+    inp = make_inputs(cfg)
+    layer, out = run_layer(qm, inp, min_rows=PATHS[path])
+    check_routing(layer, inp, min_rows=PATHS[path])
+    check_out(out, O.forward(inp), cfg.dtype)
+
+
 @pytest.mark.parametrize("name", list(VARIANTS))
 def test_variant_parity(qm, name):
     cfg = BASE.with_(**VARIANTS[name])

@@ -59,9 +59,25 @@ class QMoELayer:
 
     @classmethod
     def from_config(cls, cfg):
-        return cls(cfg.H, cfg.I, cfg.E, cfg.k, cfg.bits1, cfg.bits2, cfg.B, cfg.zp_mode,
-                   cfg.act, cfg.dtype, cfg.normalize,
-                   cfg.zp_offset if cfg.zp_mode == "offset" else None)
+        layer = cls(cfg.H, cfg.I, cfg.E, cfg.k, cfg.bits1, cfg.bits2, cfg.B, cfg.zp_mode,
+                    cfg.act, cfg.dtype, cfg.normalize,
+                    cfg.zp_offset if cfg.zp_mode == "offset" else None)
+        if getattr(cfg, "fc1_layout", "concat") == "interleaved":
+            layer.set_fc1_layout(True)
+        if (getattr(cfg, "swiglu_alpha", 1.0), getattr(cfg, "swiglu_beta", 0.0),
+                getattr(cfg, "swiglu_limit", float("inf"))) != (1.0, 0.0, float("inf")):
+            layer.set_swiglu_params(cfg.swiglu_alpha, cfg.swiglu_beta, cfg.swiglu_limit)
+        return layer
+
+    def set_swiglu_params(self, alpha, beta, limit):
+        self._check(binding.qmoe_set_swiglu_params(self.handle, alpha, beta, limit))
+
+    def set_fc1_layout(self, interleaved):
+        self._check(binding.qmoe_set_fc1_layout(self.handle, 1 if interleaved else 0))
+
+    def set_bias(self, fc, bias, stream=None):
+        """fp32 [E, N] device tensor, or None to remove."""
+        self._check(binding.qmoe_set_bias(self.handle, fc, _ptr(bias), _stream(stream)))
 
     def _check(self, st):
         if st != binding.QMOE_OK:
@@ -152,6 +168,9 @@ def load_inputs(layer: QMoELayer, inp: dict, device="cuda"):
         zp = inp[pre + "zp"]
         zp = zp.to(device) if zp is not None else None
         layer.prepack(fc, codes, scales, zp)
+        b = inp.get(pre + "bias")
+        if b is not None:
+            layer.set_bias(fc, b.to(device))
     import torch
     torch.cuda.synchronize()
     return inp["x"].to(device), inp["logits"].to(device)

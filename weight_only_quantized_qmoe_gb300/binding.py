@@ -32,6 +32,9 @@ _SIGS = {
     "qmoe_set_routing": (_i, [_p, _i]),
     "qmoe_set_zero_point_offset": (_i, [_p, ctypes.c_float]),
     "qmoe_set_gemm_min_rows": (_i, [_p, _i]),
+    "qmoe_set_swiglu_params": (_i, [_p, ctypes.c_float, ctypes.c_float, ctypes.c_float]),
+    "qmoe_set_fc1_layout": (_i, [_p, _i]),
+    "qmoe_set_bias": (_i, [_p, _i, _p, _p]),
     "qmoe_reserve": (_i, [_p, _i64]),
     "qmoe_prepack": (_i, [_p, _i, _p, _p, _p, _p]),
     "qmoe_forward": (_i, [_p, _p, _p, _p, _i64, _p]),
@@ -96,6 +99,18 @@ def qmoe_set_zero_point_offset(layer, offset):
 
 def qmoe_set_gemm_min_rows(layer, min_rows):
     return load().qmoe_set_gemm_min_rows(layer, int(min_rows))
+
+
+def qmoe_set_swiglu_params(layer, alpha, beta, limit):
+    return load().qmoe_set_swiglu_params(layer, float(alpha), float(beta), float(limit))
+
+
+def qmoe_set_fc1_layout(layer, interleaved):
+    return load().qmoe_set_fc1_layout(layer, int(interleaved))
+
+
+def qmoe_set_bias(layer, fc, bias_dev, stream=None):
+    return load().qmoe_set_bias(layer, int(fc), bias_dev, stream)
 
 
 def qmoe_reserve(layer, max_tokens):

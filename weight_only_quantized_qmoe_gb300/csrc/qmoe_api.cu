@@ -48,6 +48,10 @@ constexpr long long kDefaultWaitLimit = 1LL << 21;
 struct qmoe_layer {
   int H, I, E, k, B, zp_mode, act, dtype, dsize;
   int bits[2];
+  // SwiGLU attributes (qmoe.rs swiglu_value defaults: alpha 1, beta 0, no limit)
+  float sw_alpha = 1.f, sw_beta = 0.f, sw_limit = INFINITY;
+  int fc1_interleaved = 0;                 // fc1 canonical rows: [gate | up] or (gate, up) pairs
+  float* bias[2] = {nullptr, nullptr};     // fc1: [E, I, 2] (gate, up) pairs ; fc2: [E, H]
   int normalize = 1;
   float zp_offset = NAN;
   bool offset_set = false;
@@ -125,6 +129,34 @@ cudaError_t dalloc(T** p, size_t bytes) {
   *p = nullptr;
   if (bytes == 0) bytes = 16;
   return cudaMalloc(reinterpret_cast<void**>(p), bytes);
+}
+
+ActParams act_params(const qmoe_layer* l) {
+  ActParams p;
+  p.act = l->act;
+  p.alpha = l->sw_alpha;
+  p.beta = l->sw_beta;
+  p.limit = l->sw_limit;
+  return p;
+}
+
+// fc1 bias [E, 2I] in the canonical row order -> (gate, up) pairs [E, I, 2].
+__global__ void pair_bias_kernel(const float* __restrict__ src, float* __restrict__ dst, int E, int I,
+                                 int interleaved) {
+  const size_t n = (size_t)E * I;
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x) {
+    const size_t e = i / I, f = i % I;
+    const float* row = src + e * 2 * I;
+    dst[2 * i] = interleaved ? row[2 * f] : row[f];
+    dst[2 * i + 1] = interleaved ? row[2 * f + 1] : row[I + f];
+  }
+}
+
+cudaError_t launch_pair_bias(const float* src, float* dst, int E, int I, int interleaved, cudaStream_t s) {
+  const size_t n = (size_t)E * I;
+  const int grid = (int)std::min<size_t>((n + 255) / 256, 4096);
+  pair_bias_kernel<<<grid, 256, 0, s>>>(src, dst, E, I, interleaved);
+  return cudaGetLastError();
 }
 
 void free_workspace(qmoe_layer* l) {
@@ -295,6 +327,46 @@ qmoe_status qmoe_set_zero_point_offset(qmoe_layer* l, float offset) {
   return QMOE_OK;
 }
 
+qmoe_status qmoe_set_swiglu_params(qmoe_layer* l, float alpha, float beta, float limit) {
+  if (!l) return QMOE_ERR_INVALID_ARG;
+  if (!std::isfinite(alpha) || alpha == 0.f || !std::isfinite(beta) || std::isnan(limit) || !(limit > 0.f))
+    return fail(l, QMOE_ERR_INVALID_ARG, "swiglu: alpha finite and nonzero, beta finite, limit > 0 (or +inf)");
+  l->sw_alpha = alpha;
+  l->sw_beta = beta;
+  l->sw_limit = limit;
+  return QMOE_OK;
+}
+
+qmoe_status qmoe_set_fc1_layout(qmoe_layer* l, int interleaved) {
+  if (!l || (interleaved != 0 && interleaved != 1)) return QMOE_ERR_INVALID_ARG;
+  if (l->proj[0].ready || l->bias[0])
+    return fail(l, QMOE_ERR_STATE, "set the fc1 layout before qmoe_prepack(fc=1) and qmoe_set_bias(fc=1)");
+  l->fc1_interleaved = interleaved;
+  return QMOE_OK;
+}
+
+qmoe_status qmoe_set_bias(qmoe_layer* l, int fc, const float* bias, void* stream) {
+  if (!l) return QMOE_ERR_INVALID_ARG;
+  if (fc != 1 && fc != 2) return fail(l, QMOE_ERR_INVALID_ARG, "fc must be 1 or 2");
+  float*& dst = l->bias[fc - 1];
+  if (!bias) {
+    if (dst) {
+      QMOE_CUDA(l, cudaStreamSynchronize(static_cast<cudaStream_t>(stream)), "synchronise");
+      cudaFree(dst);
+    }
+    dst = nullptr;
+    return QMOE_OK;
+  }
+  const size_t n = (size_t)l->E * (fc == 1 ? 2 * l->I : l->H);
+  if (!dst) QMOE_CUDA(l, dalloc(&dst, n * sizeof(float)), "allocate bias");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (fc == 2)
+    QMOE_CUDA(l, cudaMemcpyAsync(dst, bias, n * sizeof(float), cudaMemcpyDeviceToDevice, s), "copy bias");
+  else
+    QMOE_CUDA(l, launch_pair_bias(bias, dst, l->E, l->I, l->fc1_interleaved, s), "re-lay fc1 bias");
+  return QMOE_OK;
+}
+
 qmoe_status qmoe_set_gemm_min_rows(qmoe_layer* l, int min_rows) {
   if (!l || min_rows < 0) return QMOE_ERR_INVALID_ARG;
   l->gemm_min_rows = min_rows;
@@ -382,6 +454,7 @@ qmoe_status qmoe_prepack(qmoe_layer* l, int fc, const uint8_t* codes, const void
     ra.N = p.N;
     ra.K = p.K;
     ra.I_or_0 = fc == 1 ? l->I : 0;
+    ra.interleaved = l->fc1_interleaved;
     ra.dsize = l->dsize;
     ra.L = p.L;
     QMOE_CUDA(l, launch_repack_decode(ra, s), "repack weights");
@@ -402,6 +475,7 @@ qmoe_status qmoe_prepack(qmoe_layer* l, int fc, const uint8_t* codes, const void
     ga.K = p.K;
     ga.I = l->I;
     ga.fc = fc;
+    ga.interleaved = l->fc1_interleaved;
     ga.L = p.GL;
     QMOE_CUDA(l, launch_repack_gemm(ga, s), "repack weights (GEMM layout)");
   }
@@ -492,7 +566,9 @@ qmoe_status qmoe_forward(qmoe_layer* l, const void* x, const float* logits, void
       sa.k = l->k;
       sa.fc = f + 1;
       sa.dtype = l->dtype;
-      sa.act = l->act;
+      sa.act = act_params(l);
+      sa.bias = l->bias[f];
+      sa.interleaved = l->fc1_interleaved;
       sa.zp_mode = l->zp_mode;
       sa.zp_offset = l->zp_offset;
       sa.dst = f == 0 ? l->hbuf : (void*)l->ybuf;
@@ -513,7 +589,8 @@ qmoe_status qmoe_forward(qmoe_layer* l, const void* x, const float* logits, void
       da.fc = f + 1;
       da.ng = tb0 / 8;
       da.dst = f == 0 ? l->hbuf : (void*)l->ybuf;
-      da.act = l->act;
+      da.act = act_params(l);
+      da.bias = l->bias[f];
       da.zp_mode = l->zp_mode;
       da.zp_offset = l->zp_offset;
       da.bf16 = l->dtype == QMOE_BF16;
@@ -534,7 +611,8 @@ qmoe_status qmoe_forward(qmoe_layer* l, const void* x, const float* logits, void
         const int64_t max_tiles = (int64_t)ra.cap[1] * p.GL.ntiles;
         ga.grid = (int)(max_tiles < l->num_sms ? max_tiles : l->num_sms);
         ga.fc = f + 1;
-        ga.act = l->act;
+        ga.act = act_params(l);
+        ga.bias = l->bias[f];
         ga.zp_mode = l->zp_mode;
         ga.bf16 = l->dtype == QMOE_BF16;
         ga.zp_offset = l->zp_offset;
@@ -672,6 +750,8 @@ void qmoe_destroy(qmoe_layer* l) {
   if (!l) return;
   if (l->device >= 0 || l->cap_T > 0) cudaDeviceSynchronize();
   free_workspace(l);
+  for (float* b : l->bias)
+    if (b) cudaFree(b);
   for (Proj& p : l->proj) {
     if (p.codes) cudaFree(p.codes);
     if (p.scales) cudaFree(p.scales);
@@ -829,7 +909,9 @@ extern "C" qmoe_status qmoe_forward_noalloc(qmoe_layer* l, const void* x, const 
       sa.k = l->k;
       sa.fc = f + 1;
       sa.dtype = l->dtype;
-      sa.act = l->act;
+      sa.act = act_params(l);
+      sa.bias = l->bias[f];
+      sa.interleaved = l->fc1_interleaved;
       sa.zp_mode = l->zp_mode;
       sa.zp_offset = l->zp_offset;
       sa.dst = f == 0 ? hbuf : (void*)ybuf;
@@ -850,7 +932,8 @@ extern "C" qmoe_status qmoe_forward_noalloc(qmoe_layer* l, const void* x, const 
       da.fc = f + 1;
       da.ng = tb0 / 8;
       da.dst = f == 0 ? hbuf : (void*)ybuf;
-      da.act = l->act;
+      da.act = act_params(l);
+      da.bias = l->bias[f];
       da.zp_mode = l->zp_mode;
       da.zp_offset = l->zp_offset;
       da.bf16 = l->dtype == QMOE_BF16;

@@ -75,7 +75,14 @@ __global__ void repack_decode_kernel(const RepackArgs a) {
   const int ktiles = L.SC / 16;
 
   for (int s = 0; s < L.nsub; ++s) {
-    const int rowbase = tile * 16 + (s == 1 ? a.I_or_0 : 0);
+    // canonical row of local row `off` of this 16-row sub-tile: fc1 gate
+    // (s = 0) / up (s = 1) row of feature f = tile*16 + off, concatenated
+    // ([gate | up]) or interleaved (gate f = 2f, up f = 2f+1); fc2 row f.
+    auto crow = [&](int off) {
+      const int f = tile * 16 + off;
+      if (a.I_or_0 == 0) return f;
+      return a.interleaved ? 2 * f + s : f + s * a.I_or_0;
+    };
     auto code = [&](int row, int d) {
       const uint8_t* rp = a.codes + ((size_t)e * a.N + row) * row_bytes;
       return canon_code(rp, row_bytes, bits, d, a.K);
@@ -92,7 +99,7 @@ __global__ void repack_decode_kernel(const RepackArgs a) {
         uint32_t w = 0;
         for (int r = 0; r < 4; ++r)
           for (int e2 = 0; e2 < 2; ++e2) {
-            const int row = rowbase + g + ((r & 1) ? 8 : 0);
+            const int row = crow(g + ((r & 1) ? 8 : 0));
             w |= (uint32_t)code(row, kidx(j, t, r, e2)) << (4 * (r + 4 * e2));
           }
         cw[lane * W + j] = w;
@@ -105,7 +112,7 @@ __global__ void repack_decode_kernel(const RepackArgs a) {
         uint32_t w = 0;
         for (int pi = 0; pi < 8; ++pi) {
           const int j = 2 * wj + pi / 4, r = pi % 4;
-          const int row = rowbase + g + ((r & 1) ? 8 : 0);
+          const int row = crow(g + ((r & 1) ? 8 : 0));
           for (int e2 = 0; e2 < 2; ++e2)
             w |= (uint32_t)(code(row, kidx(j, t, r, e2)) & 3) << (2 * (pi + 8 * e2));
         }
@@ -120,7 +127,7 @@ __global__ void repack_decode_kernel(const RepackArgs a) {
           uint32_t w = 0;
           for (int pi = 0; pi < 16; ++pi) {
             const int j = 4 * wj + pi / 4, r = pi % 4;
-            const int row = rowbase + g + ((r & 1) ? 8 : 0);
+            const int row = crow(g + ((r & 1) ? 8 : 0));
             for (int e2 = 0; e2 < 2; ++e2)
               w |= (uint32_t)((code(row, kidx(j, t, r, e2)) >> 2) & 1) << (pi + 16 * e2);
           }
@@ -133,7 +140,7 @@ __global__ void repack_decode_kernel(const RepackArgs a) {
     uint8_t* sp = out + L.nsub * L.code_bytes + s * L.scale_bytes;
     for (int i = threadIdx.x; i < nb * 16; i += blockDim.x) {
       const int blk = i / 16, g = (i % 16) / 2, hi = i % 2;
-      const int row = rowbase + g + 8 * hi;
+      const int row = crow(g + 8 * hi);
       const int kb = kc * nb + blk;
       uint16_t v = 0;
       if (kb < nblk_row)
@@ -147,8 +154,8 @@ __global__ void repack_decode_kernel(const RepackArgs a) {
         if (i < nb * 8) {
           const int blk = i / 8, g = i % 8, kb = kc * nb + blk;
           if (kb < nblk_row) {
-            const uint8_t* z0 = a.zp + ((size_t)e * a.N + rowbase + g) * zrow_bytes;
-            const uint8_t* z1 = a.zp + ((size_t)e * a.N + rowbase + g + 8) * zrow_bytes;
+            const uint8_t* z0 = a.zp + ((size_t)e * a.N + crow(g)) * zrow_bytes;
+            const uint8_t* z1 = a.zp + ((size_t)e * a.N + crow(g + 8)) * zrow_bytes;
             const int lo = canon_code(z0, zrow_bytes, bits, kb, nblk_row);
             const int hi = canon_code(z1, zrow_bytes, bits, kb, nblk_row);
             v = (uint8_t)(lo | (hi << 4));
@@ -233,9 +240,12 @@ __global__ void __launch_bounds__(256) simt_kernel(const SimtArgs a) {
   if (n >= a.N_out) return;
   const bool glu_fc = a.fc == 1;
   float ag[kSimtRows] = {0.f, 0.f, 0.f, 0.f}, au[kSimtRows] = {0.f, 0.f, 0.f, 0.f};
+  // fc1 rows of feature n: concatenated [gate | up] or interleaved pairs
+  const int grow = glu_fc && a.interleaved ? 2 * n : n;
+  const int urow = glu_fc ? (a.interleaved ? 2 * n + 1 : a.I_or_0 + n) : 0;
   for (int d = lane; d < K; d += 32) {
-    const float wg = simt_weight<DT>(a, it.e, n, d);
-    const float wu = glu_fc ? simt_weight<DT>(a, it.e, a.I_or_0 + n, d) : 0.f;
+    const float wg = simt_weight<DT>(a, it.e, grow, d);
+    const float wu = glu_fc ? simt_weight<DT>(a, it.e, urow, d) : 0.f;
 #pragma unroll
     for (int r = 0; r < kSimtRows; ++r) {
       ag[r] = fmaf(wg, xs[r * K + d], ag[r]);
@@ -251,10 +261,20 @@ __global__ void __launch_bounds__(256) simt_kernel(const SimtArgs a) {
     }
   }
   if (lane == 0) {
+    // fp32 projection bias [qmoe.rs qmoe_linear_impl]: fc1 (gate, up) pairs, fc2 rows
+    float bg = 0.f, bu = 0.f;
+    if (a.bias) {
+      if (glu_fc) {
+        bg = a.bias[((size_t)it.e * a.N_out + n) * 2];
+        bu = a.bias[((size_t)it.e * a.N_out + n) * 2 + 1];
+      } else {
+        bg = a.bias[(size_t)it.e * a.N_out + n];
+      }
+    }
     for (int r = 0; r < it.rows && r < kSimtRows; ++r) {
       const size_t o = (size_t)(it.start + r) * a.N_out + n;
-      if (glu_fc) store_d<DT>(a.dst, o, glu(a.act, ag[r], au[r]));
-      else static_cast<float*>(a.dst)[o] = ag[r];
+      if (glu_fc) store_d<DT>(a.dst, o, glu(a.act, ag[r] + bg, au[r] + bu));
+      else static_cast<float*>(a.dst)[o] = ag[r] + bg;
     }
   }
 }

@@ -307,12 +307,29 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
   if (!active || ks != 0) return;
 
   // Epilogue.  acc[s][n][q]: row g + 8*(q>>1), token n*8 + 2t + (q&1).
+  // fp32 projection biases [qmoe.rs qmoe_linear_impl]: fc1 (gate, up) pairs
+  // per feature, fc2 per row.
+  float bias_g[2] = {0.f, 0.f}, bias_u[2] = {0.f, 0.f};
+  if (a.bias) {
+#pragma unroll
+    for (int hi = 0; hi < 2; ++hi) {
+      const int row = tile * 16 + g + 8 * hi;
+      if (GLU) {
+        bias_g[hi] = a.bias[((size_t)it.e * a.N_out + row) * 2];
+        bias_u[hi] = a.bias[((size_t)it.e * a.N_out + row) * 2 + 1];
+      } else {
+        bias_g[hi] = a.bias[(size_t)it.e * a.N_out + row];
+      }
+    }
+  }
 #pragma unroll
   for (int n = 0; n < NGM; ++n) {
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
       const int tok = n * 8 + 2 * t + (q & 1);
       const int row = tile * 16 + g + 8 * (q >> 1);
+      acc[0][n][q] += bias_g[q >> 1];
+      if (GLU) acc[NSUB - 1][n][q] += bias_u[q >> 1];
       if (tok < it.rows) {
         const size_t o = (size_t)(it.start + tok) * a.N_out + row;
         if (GLU) {

@@ -80,12 +80,19 @@ struct RouteArgs {
 
 cudaError_t launch_route_group(const RouteArgs& a, bool fused, cudaStream_t s);
 
+// Gated activation of fc1's output: SwiGLU (with its attributes) or GeGLU.
+struct ActParams {
+  int act;                  // QMOE_ACT_SWIGLU | QMOE_ACT_GEGLU_TANH
+  float alpha, beta, limit; // SwiGLU only
+};
+
 struct RepackArgs {
   const uint8_t* codes;     // canonical [E, N, K*bits/8]
   const void* scales;       // canonical [E, N, K/B], D
   const uint8_t* zp;        // canonical packed zp or null
   uint8_t* out;             // decode layout
   int E, N, K, I_or_0;      // I_or_0 = inter for fc1 (gate/up pairing), 0 for fc2
+  int interleaved;          // fc1 canonical rows: 0 = [gate | up], 1 = (gate f, up f) pairs
   int dsize;
   DecodeLayout L;
 };
@@ -106,7 +113,8 @@ struct DecodeArgs {
   int fc;                   // 1 or 2
   int ng;                   // token groups of 8 per item (1, 2 or 4)
   void* dst;                // fc1: h [R, I] D ; fc2: y [R, H] f32
-  int act;
+  ActParams act;
+  const float* bias;        // fc1: [E, I, 2] (gate, up) pairs ; fc2: [E, H] ; or null
   int zp_mode;
   float zp_offset;
   int bf16;
@@ -133,7 +141,10 @@ struct SimtArgs {
   int max_items;
   const void* src;
   const int* perm;
-  int k, fc, dtype, act, zp_mode;
+  int k, fc, dtype, zp_mode;
+  ActParams act;
+  const float* bias;        // fc1: [E, I, 2] (gate, up) pairs ; fc2: [E, H] ; or null
+  int interleaved;          // fc1 canonical rows interleaved (gate f = row 2f, up f = row 2f+1)
   float zp_offset;
   void* dst;                // fc1: h [R, I] f32 ; fc2: y [R, H] f32
   int E;
@@ -407,8 +418,19 @@ __device__ __forceinline__ float act_silu(float g) {
 __device__ __forceinline__ float act_gelu_tanh(float g) {
   return 0.5f * g * (1.f + tanhf(0.7978845608028654f * (g + 0.044715f * g * g * g)));
 }
-__device__ __forceinline__ float glu(int act, float g, float u) {
-  return (act == QMOE_ACT_SWIGLU ? act_silu(g) : act_gelu_tanh(g)) * u;
+// SwiGLU with the qmoe.rs swiglu_value attributes: the gate bounded above by
+// `limit`, the linear half clamped to [-limit, limit] (NaN kept), then
+// g' * sigmoid(alpha * g') * (u' + beta).  alpha = 1, beta = 0, limit = +inf
+// is plain silu(g) * u.
+__device__ __forceinline__ float act_swiglu(float g, float u, float alpha, float beta, float limit) {
+  g = fminf(g, limit);
+  if (!isnan(u)) u = fminf(fmaxf(u, -limit), limit);
+  const float z = alpha * g;
+  const float sig = z >= 0.f ? 1.f / (1.f + expf(-z)) : expf(z) / (1.f + expf(z));
+  return g * sig * (u + beta);
+}
+__device__ __forceinline__ float glu(const ActParams& p, float g, float u) {
+  return p.act == QMOE_ACT_SWIGLU ? act_swiglu(g, u, p.alpha, p.beta, p.limit) : act_gelu_tanh(g) * u;
 }
 
 }  // namespace qmoe

@@ -58,9 +58,11 @@ __global__ void repack_gemm_kernel(const GemmRepackArgs a) {
   int row;
   bool valid;
   if (a.fc == 1) {
+    // tile row 2p = gate of feature n, 2p+1 = its up row; canonical rows
+    // concatenated ([gate | up]) or interleaved (gate n = 2n, up n = 2n+1)
     const int n = nt * 64 + r / 2;
     valid = n < a.I;
-    row = (r & 1) ? a.I + n : n;
+    row = a.interleaved ? 2 * n + (r & 1) : ((r & 1) ? a.I + n : n);
   } else {
     row = nt * 128 + r;
     valid = row < a.N;
@@ -477,9 +479,15 @@ __device__ __forceinline__ void dequant_row(const uint8_t* stage, const GemmLayo
 }
 
 // Gated activations for the GEMM epilogue, from exp (CUDA's __expf):
-// silu(g) = g / (1 + e^-g); tanh(y) = 1 - 2 / (e^{2y} + 1).
-__device__ __forceinline__ float glu_fast(int act, float g, float u) {
-  if (act == QMOE_ACT_SWIGLU) return __fdividef(g, 1.f + __expf(-g)) * u;
+// SwiGLU with its attributes (gate bounded by limit, linear half clamped to
+// [-limit, limit], g * sigmoid(alpha g) = g / (1 + e^{-alpha g}), times
+// (u + beta)); tanh(y) = 1 - 2 / (e^{2y} + 1) for GeGLU.
+__device__ __forceinline__ float glu_fast(const ActParams& p, float g, float u) {
+  if (p.act == QMOE_ACT_SWIGLU) {
+    g = fminf(g, p.limit);
+    if (!isnan(u)) u = fminf(fmaxf(u, -p.limit), p.limit);
+    return __fdividef(g, 1.f + __expf(-p.alpha * g)) * (u + p.beta);
+  }
   const float y = 0.7978845608028654f * (g + 0.044715f * g * g * g);
   const float t = 1.f - __fdividef(2.f, __expf(2.f * y) + 1.f);
   return 0.5f * g * (1.f + t) * u;
@@ -746,6 +754,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           // lanes 2p / 2p+1 hold gate / up of feature n = nt*64 + q*16 + p
           const bool odd = lane & 1;
           const int jbeg = odd ? 16 : 0;
+          if (a.bias) {   // fp32 projection bias of this lane's row (gate or up of n)
+            const int n = nt * 64 + q * 16 + (lane >> 1);
+            const float b = n < a.N_out ? a.bias[((size_t)it.e * a.N_out + n) * 2 + (lane & 1)] : 0.f;
+#pragma unroll
+            for (int j = 0; j < 32; ++j) v[j] = __float_as_uint(__uint_as_float(v[j]) + b);
+          }
           uint16_t* t16 = reinterpret_cast<uint16_t*>(tile32);   // [32 tokens][16 features]
           // Even lanes take tokens 0..15 of the chunk (own gate, partner's
           // up), odd lanes tokens 16..31 (partner's gate, own up): one
@@ -779,9 +793,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           }
           __syncwarp();
         } else {
-          // transpose: tile32[token j][row] = D[row][c0 + j]
+          // transpose: tile32[token j][row] = D[row][c0 + j] (+ the row's fp32 bias)
+          const int mrow = nt * 128 + q * 32 + lane;
+          const float b = a.bias && mrow < a.N_out ? a.bias[(size_t)it.e * a.N_out + mrow] : 0.f;
 #pragma unroll
-          for (int j = 0; j < 32; ++j) tile32[j * kEpiPitch + lane] = __uint_as_float(v[j]);
+          for (int j = 0; j < 32; ++j) tile32[j * kEpiPitch + lane] = __uint_as_float(v[j]) + b;
           __syncwarp();
           const int mbase = nt * 128 + q * 32;
           if (col_ok && mbase < a.N_out) {

@@ -30,6 +30,7 @@ struct GemmRepackArgs {
   const uint8_t* zp;
   uint8_t* out;
   int E, N, K, I, fc;
+  int interleaved;          // fc1 canonical rows: 0 = [gate | up], 1 = (gate f, up f) pairs
   GemmLayout L;
 };
 cudaError_t launch_repack_gemm(const GemmRepackArgs& a, cudaStream_t s);
@@ -51,7 +52,9 @@ struct GemmArgs {
   const int* n_items;
   int max_items;
   int grid;                // persistent CTAs
-  int fc, act, zp_mode, bf16;
+  int fc, zp_mode, bf16;
+  ActParams act;
+  const float* bias;       // fc1: [E, I, 2] (gate, up) pairs ; fc2: [E, H] ; or null
   float zp_offset;
   const uint8_t* btiles;   // B operand in the tiled token layout (L.ksteps steps per item)
   uint8_t* htiles;         // fc1: h written in the tiled token layout for fc2
