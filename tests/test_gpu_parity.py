@@ -133,6 +133,8 @@ FEATURE_VARIANTS = {
                                    E=4, T=150),
     "f32_interleaved_bias_params": dict(dtype="f32", fc1_layout="interleaved", bias=True,
                                         swiglu_alpha=1.702, swiglu_beta=1.0, swiglu_limit=0.3, T=7),
+    # a long fc2 reduction (K = 1024) with biases
+    "bias_long_fc2_k": dict(bias=True, I=1024, E=4, T=6),
 }
 
 
