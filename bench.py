@@ -30,6 +30,12 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "QMoE layer µs & tokens/s; % HBM roofline (decode), % tensor peak (prefill)"
+
+# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one fc1
+# gemm_kernel launch, from one ncu capture of the current kernel
+# (profiles/gemm_kernel_decode_int2_fc1.md, profiles/gemm_kernel_prefill_fc1.md);
+# None where no capture of the current kernel exists for the workload.
+FC1_TRAFFIC = {"decode_int2": 19_199_744, "prefill_int4": 803_444_992}
 L2_BYTES = 129 * 1024 * 1024
 
 
@@ -323,16 +329,18 @@ def run_ours(args):
     # measured copy bandwidth) and its tensor time (2 * R * H * 2I FLOPs at
     # the measured bf16 peak) decides what bounds it.
     fc1_flops = 2.0 * cfg.T * cfg.k * cfg.H * 2 * cfg.I
+    # counters taken on the default path only (every expert on the GEMM)
+    traffic = FC1_TRAFFIC.get(cfg.name) if (min_rows == 0 and cfg.dtype != "f32") else None
     if fc1_flops / (bf16_peak * 1e12) > fc1_bytes / (hbm_peak * 1e9):
         achieved_t = fc1_flops / (fc1_stage * 1e-3) / 1e12
         roofline = {"bound": "tensor", "achieved": achieved_t, "peak": bf16_peak, "unit": "TFLOP/s",
-                    "frac": achieved_t / bf16_peak, "traffic": None,
+                    "frac": achieved_t / bf16_peak, "traffic": traffic,
                     "kernel": "fc1 (gemm_kernel, tcgen05 grouped GEMM)", "flops_per_launch": fc1_flops,
                     "peak_kind": peak_kind + " bf16 burst"}
     else:
         achieved = fc1_bytes / (fc1_stage * 1e-3) / 1e9
         roofline = {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
-                    "frac": achieved / hbm_peak, "traffic": None,
+                    "frac": achieved / hbm_peak, "traffic": traffic,
                     "kernel": "fc1 (gemm_kernel)" if cfg.T > min_rows and cfg.dtype != "f32"
                     else "fc1 (decode_mma_kernel)", "bytes_per_launch": fc1_bytes,
                     "peak_kind": peak_kind}
@@ -355,11 +363,13 @@ def run_ours(args):
     e2e = max_over_ranks(statistics.mean(e2e_ms), dev)
 
     # Kernels one forward launches (the library's launch sequence): routing
-    # (fused with grouping for T <= 64, else route + group), the x gather
-    # when the grouped GEMM runs, per projection the decode-class kernel plus
-    # the GEMM when it runs, and the combine.
+    # (fused with grouping for T <= 64, else route + group), the x gather and
+    # one GEMM per projection when the grouped GEMM runs, one decode-class
+    # kernel per projection when any expert can take that class (a positive
+    # threshold, or fp32 / T below it), and the combine.
     gemm_on = cfg.dtype != "f32" and cfg.T > min_rows
-    launches_per_step = (1 if cfg.T <= 64 else 2) + (1 if gemm_on else 0) + 2 * (1 + (1 if gemm_on else 0)) + 1
+    decode_on = not gemm_on or min_rows > 0
+    launches_per_step = ((1 if cfg.T <= 64 else 2) + (3 if gemm_on else 0) + (2 if decode_on else 0) + 1)
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
