@@ -148,6 +148,39 @@ def test_feature_parity(qm, name, path):
     check_out(out, O.forward(inp), cfg.dtype)
 
 
+# Every (fc1, fc2) code width in {2,3,4}^2 at every block size, on both
+# projection paths; the zero-point mode and activation dtype rotate through
+# the matrix so each appears with every width and block size.
+def _width_cases():
+    cases = []
+    zps = ["sym", "uint8", "offset"]
+    for b1 in (2, 3, 4):
+        for b2 in (2, 3, 4):
+            for blk in (32, 64, 128):
+                i = len(cases)
+                zp = zps[(b1 + b2 + blk // 32) % 3]
+                kw = dict(bits1=b1, bits2=b2, B=blk, zp_mode=zp, dtype=("bf16", "f16")[i % 2], T=12)
+                if zp == "uint8":
+                    kw.update(zp_lo=0, zp_hi=(1 << min(b1, b2)) - 1)
+                if zp == "offset":
+                    kw.update(zp_offset=1.5)
+                cases.append((f"w{b1}{b2}_B{blk}_{zp}", kw))
+    return cases
+
+
+WIDTH_CASES = dict(_width_cases())
+
+
+@pytest.mark.parametrize("path", sorted(PATHS))
+@pytest.mark.parametrize("name", list(WIDTH_CASES))
+def test_width_matrix_parity(qm, name, path):
+    cfg = BASE.with_(**WIDTH_CASES[name])
+    inp = make_inputs(cfg)
+    layer, out = run_layer(qm, inp, min_rows=PATHS[path])
+    check_routing(layer, inp, min_rows=PATHS[path])
+    check_out(out, O.forward(inp), cfg.dtype)
+
+
 @pytest.mark.parametrize("name", list(VARIANTS))
 def test_variant_parity(qm, name):
     cfg = BASE.with_(**VARIANTS[name])

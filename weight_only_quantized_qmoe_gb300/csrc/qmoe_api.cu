@@ -610,6 +610,9 @@ qmoe_status qmoe_forward(qmoe_layer* l, const void* x, const float* logits, void
         ga.max_items = ra.cap[1];
         const int64_t max_tiles = (int64_t)ra.cap[1] * p.GL.ntiles;
         ga.grid = (int)(max_tiles < l->num_sms ? max_tiles : l->num_sms);
+        // an expert receives at most T rows: with T <= 64 every item fits
+        // the decode ring shape
+        ga.dec = T <= 64 ? 1 : 0;
         ga.fc = f + 1;
         ga.act = act_params(l);
         ga.bias = l->bias[f];

@@ -389,37 +389,50 @@ __device__ __forceinline__ bool spin_or_abort(uint64_t* bar, uint32_t parity, co
 // ----------------------------------------------------------------------------
 // The grouped GEMM kernel
 // ----------------------------------------------------------------------------
-// One ring of kStages k-steps: stage s holds the token tile (B, shared
-// memory), the packed weights (W, shared memory) and the dequantised weights
-// (A, 32 TMEM columns) of one k-step.  Three barriers per stage, one wait per
-// role and k-step:
+// One ring of Ring<DEC>::stages stages: stage s holds KSUB consecutive 64-deep
+// k-steps -- their token tiles (B, shared memory), their packed weights (W,
+// shared memory, one contiguous copy) and their dequantised weights (A, 32
+// TMEM columns per k-step).  Three barriers per stage, one wait per role and
+// stage:
 //   full[s]  the producer's copies of W and B have landed (transaction count)
-//   ready[s] the 4 dequant warps of the step have written A   (4 arrivals)
-//   empty[s] the MMAs of the step have completed                (tcgen05.commit)
+//   ready[s] the 4 dequant warps of the stage have written A   (4 arrivals)
+//   empty[s] the MMAs of the stage have completed                (tcgen05.commit)
 // producer: empty -> copies -> full;  dequant: full -> A -> ready;
 // MMA: ready -> MMAs -> commit empty.
-constexpr int kStages = 6;
-constexpr int kTileN = 128;       // token rows per tile (MMA N <= 128)
-constexpr int kBBytes = kTileN * 128;
 constexpr int kTmemCols = 512;
-constexpr int kAccCols = 128;     // two accumulators: columns [0,128) and [128,256)
-constexpr int kAcol0 = 256;       // first TMEM column of the A ring
-constexpr int kDeqGroups = 3;     // dequant warp groups (4 warps each), k-step kc -> group kc % 3
-// Each stage is always dequantised by the same group (stage s -> group s % 3),
-// so a group consumes its stages' phases in order and never runs a ring ahead
-// of a fill that has not landed (a parity test could not tell those apart).
-static_assert(kStages % kDeqGroups == 0, "a stage belongs to one dequant group");
+constexpr int kDeqGroups = 3;     // dequant warp groups (4 warps each), stage step kc -> group kc % 3
 constexpr int kEpiWarp0 = 4 + 4 * kDeqGroups;
 constexpr int kGemmThreads = (kEpiWarp0 + 4) * 32;  // see the role map in the kernel
 constexpr int kEpiPitch = 36;     // fp32 words per row of an epilogue transpose tile (pad: banks)
 constexpr int kEpiBytes = 4 * 32 * kEpiPitch * 4;   // one 32x32 tile per epilogue warp
 
-struct GemmSmem {
+// The two ring shapes.  Prefill items carry up to 128 token rows: two
+// 128-column accumulators and one k-step per stage.  Decode items (T <= 64)
+// carry at most 64 rows: two 64-column accumulators, and the TMEM this frees
+// holds 128-deep stages, so each barrier round, copy and commit covers twice
+// the MMA work (the hand-offs, not the MMAs, pace the ring at these shapes).
+template <bool DEC>
+struct Ring {
+  static constexpr int stages = 6;
+  static constexpr int ksub = DEC ? 2 : 1;          // 64-deep k-steps per stage
+  static constexpr int tile_n = DEC ? 64 : 128;     // token rows per item (MMA N <= tile_n)
+  static constexpr int bsub = tile_n * 128;         // shared bytes of one k-step's token tile
+  static constexpr int acc_cols = tile_n;           // accumulators: [0, acc) and [acc, 2 acc)
+  static constexpr int acol0 = 2 * acc_cols;        // first TMEM column of the A ring
+  static constexpr int a_cols = 32 * ksub;          // A columns per stage
+  // Each stage is always dequantised by the same group (stage s -> group
+  // s % 3), so a group consumes its stages' phases in order and never runs a
+  // ring ahead of a fill that has not landed (a parity test could not tell
+  // those apart).
+  static_assert(stages % kDeqGroups == 0, "a stage belongs to one dequant group");
+  static_assert(acol0 + stages * a_cols <= kTmemCols, "TMEM columns");
+  // shared memory: B ring, W ring (128-byte aligned slots), epilogue tiles, barriers
+  __host__ __device__ static int wslot(int stage_bytes) { return (ksub * stage_bytes + 127) / 128 * 128; }
   static constexpr int b_off = 0;
-  static constexpr int w_off = kStages * kBBytes;
-  __host__ __device__ static int epi_off(int wstage) { return w_off + kStages * ((wstage + 127) / 128 * 128); }
-  __host__ __device__ static int bar_off(int wstage) { return epi_off(wstage) + kEpiBytes; }
-  __host__ __device__ static int total(int wstage) { return bar_off(wstage) + 1024; }
+  static constexpr int w_off = stages * ksub * bsub;
+  __host__ __device__ static int epi_off(int sb) { return w_off + stages * wslot(sb); }
+  __host__ __device__ static int bar_off(int sb) { return epi_off(sb) + kEpiBytes; }
+  __host__ __device__ static int total(int sb) { return bar_off(sb) + 1024; }
 };
 
 __device__ __forceinline__ void red_add_v4_f32(float* p, float a, float b, float c, float d) {
@@ -497,13 +510,16 @@ __device__ __forceinline__ float glu_fast(const ActParams& p, float g, float u) 
 // The weight tiles of one token tile run on neighbouring CTAs at the same
 // time; starting each at a different k-step (rotation by nt) spreads their
 // reads of the shared token tile over the L2 instead of hitting the same lines
-// together.  The MMA sums the k-steps in any order.
+// together.  The MMA sums the k-steps in any order.  With two k-steps per
+// stage the pairs stay aligned (no rotation): a stage's k-steps are then one
+// contiguous weight copy.
 struct TileSrc {
   const uint8_t* w;     // k-step kr at w + kr * stage_bytes
   const uint8_t* b;     // k-step kr at b + kr * kTokTileBytes
   uint32_t b_bytes;     // token bytes copied per k-step
   int rot;              // first k-step
 };
+template <bool DEC>
 __device__ __forceinline__ TileSrc tile_src(const GemmArgs& a, int tile) {
   const GemmLayout& L = a.L;
   const int item = tile / L.ntiles, nt = tile - item * L.ntiles;
@@ -513,8 +529,8 @@ __device__ __forceinline__ TileSrc tile_src(const GemmArgs& a, int tile) {
   r.b = a.btiles + tok_tile_offset(item, L.ksteps, 0);
   // only the 8-row groups that hold the item's rows (the MMA reads stale
   // rows past them into columns that are never stored)
-  r.b_bytes = (uint32_t)min(kBBytes, ((it.rows + 7) / 8) * 1024);
-  r.rot = (int)(((long long)nt * L.ksteps) / L.ntiles);
+  r.b_bytes = (uint32_t)min(Ring<DEC>::bsub, ((it.rows + 7) / 8) * 1024);
+  r.rot = DEC ? 0 : (int)(((long long)nt * L.ksteps) / L.ntiles);
   return r;
 }
 
@@ -534,25 +550,28 @@ __device__ __forceinline__ void bulk_g2s_elect(void* dst, const void* src, uint3
 }
 
 // Warp roles (8 + 4 * kDeqGroups warps):
-//   0      bulk-copy producer (whole warp, elect.sync): W + B of a k-step into stage s
+//   0      bulk-copy producer (whole warp, elect.sync): W + B of a stage into slot s
 //   1      MMA issuer (whole warp, elect.sync) and TMEM owner
 //   2..3   idle
-//   4 ..   dequant groups of 4 warps; group g takes k-steps kc % kDeqGroups == g,
+//   4 ..   dequant groups of 4 warps; group g takes stage steps kc % kDeqGroups == g,
 //          warp w owns TMEM lanes 32*(w%4)
 //   last 4 epilogue (TMEM lanes 32*(w%4))
-// The producer and the MMA issuer poll without suspending (they pace the
-// ring); the dequant and epilogue warps park on their barriers.
-template <int BITS, int ZPM, bool BF16, bool GLU>
+// The MMA issuer polls without suspending (it paces the ring); the producer,
+// dequant and epilogue warps park on their barriers.
+template <int BITS, int ZPM, bool BF16, bool GLU, bool DEC>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     gemm_kernel(const GemmArgs a) {
+  using RG = Ring<DEC>;
+  constexpr int kStages = RG::stages;
+  constexpr int KSUB = RG::ksub;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   // 1024-byte alignment for the swizzled B tiles
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const GemmLayout& L = a.L;
-  const int wstage = (L.stage_bytes + 127) / 128 * 128;
-  uint8_t* bring = smem + GemmSmem::b_off;
-  uint8_t* wring = smem + GemmSmem::w_off;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + GemmSmem::bar_off(wstage));
+  const int wslot = RG::wslot(L.stage_bytes);
+  uint8_t* bring = smem + RG::b_off;
+  uint8_t* wring = smem + RG::w_off;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + RG::bar_off(L.stage_bytes));
   uint64_t* full = bars;
   uint64_t* ready = full + kStages;
   uint64_t* empty = ready + kStages;
@@ -561,6 +580,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   uint64_t* drain_bar = acc_empty + 2;
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain_bar + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+  // stage steps per tile; the last one of a tile may hold fewer than KSUB k-steps
+  const int nss = (L.ksteps + KSUB - 1) / KSUB;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
@@ -578,10 +599,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     tmem_alloc(tmem_holder, kTmemCols);
     tmem_relinquish();
   }
-  // The MMA reads N >= 64 token rows of a stage, more than a small item
+  // The MMA reads N >= 64 token rows of a k-step, more than a small item
   // copies; the rows past the copy must hold finite values (zero here, or
   // rows of an earlier copy), never undefined shared memory.
-  for (int i = threadIdx.x; i < kStages * kBBytes / 16; i += blockDim.x)
+  for (int i = threadIdx.x; i < kStages * KSUB * RG::bsub / 16; i += blockDim.x)
     reinterpret_cast<uint4*>(bring)[i] = make_uint4(0u, 0u, 0u, 0u);
   fence_proxy_async_smem();
   tc_fence_before();
@@ -600,12 +621,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     for (int tile = blockIdx.x; tile < total_tiles && ok; tile += gridDim.x) {
       // (An L2 bulk prefetch a ring's depth ahead of each copy made the
       // kernel twice as slow: the copies queue behind the prefetches.)
-      const TileSrc src = tile_src(a, tile);
-      const uint32_t tx = (uint32_t)L.stage_bytes + src.b_bytes;
+      const TileSrc src = tile_src<DEC>(a, tile);
       int kr = src.rot;
-      for (int ks = 0; ks < L.ksteps; ++ks, ++kc) {
+      for (int j = 0; j < nss; ++j, ++kc) {
         const int s = kc % kStages;
         const uint32_t par = ((uint32_t)(kc / kStages) & 1u) ^ 1u;
+        const int nk = KSUB == 1 ? 1 : min(KSUB, L.ksteps - j * KSUB);
         // Parked (not spinning) wait: the producer runs a ring's depth ahead
         // of the MMAs, and a spinning poll competes with them for the
         // barrier unit.  The first poll is one warp-wide instruction (a
@@ -615,15 +636,22 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           ok = __shfl_sync(0xffffffffu, ok, 0);
           if (!ok) break;
         }
-        mbar_arrive_expect_tx_elect(&full[s], tx);
+        mbar_arrive_expect_tx_elect(&full[s], (uint32_t)nk * ((uint32_t)L.stage_bytes + src.b_bytes));
         // Test hook: stage 0's barrier is armed but its copies are never
         // issued, so the waits on it can only run out (host-injected failure).
         if (!(a.inject_stall && kc == 0)) {
-          bulk_g2s_elect(wring + s * wstage, src.w + (size_t)kr * L.stage_bytes, (uint32_t)L.stage_bytes, &full[s]);
-          bulk_g2s_elect(bring + s * kBBytes, src.b + (size_t)kr * kTokTileBytes, src.b_bytes, &full[s]);
+          // the stage's k-steps are consecutive in the weight tile: one copy
+          bulk_g2s_elect(wring + s * wslot, src.w + (size_t)kr * L.stage_bytes, (uint32_t)(nk * L.stage_bytes),
+                         &full[s]);
+#pragma unroll
+          for (int h = 0; h < KSUB; ++h)
+            if (h < nk)
+              bulk_g2s_elect(bring + (s * KSUB + h) * RG::bsub, src.b + (size_t)(kr + h) * kTokTileBytes,
+                             src.b_bytes, &full[s]);
         }
         issued = kc + 1;
-        if (++kr == L.ksteps) kr = 0;
+        kr += nk;
+        if (kr == L.ksteps) kr = 0;
       }
     }
     if (!ok) {
@@ -638,9 +666,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
   } else if (warp == 1) {
     // ---------------- MMA issuer: the whole warp, one elected lane issues ----------------
-    const uint32_t a0 = tmem + kAcol0;
+    const uint32_t a0 = tmem + RG::acol0;
     const uint64_t bdesc0 = smem_desc_sw128(smem_u32(bring));
-    int st = 0, tc = 0;       // ring stage of the next k-step, tile count
+    int st = 0, tc = 0;       // ring stage of the next stage step, tile count
     uint32_t ph = 0;          // phase parity of that stage's current use
     bool ok = true;
     for (int tile = blockIdx.x; tile < total_tiles && ok; tile += gridDim.x, ++tc) {
@@ -654,27 +682,33 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) break;
       tc_fence_after();
-      const uint32_t dacc = tmem + ab * kAccCols;
-      // The k-step loop is unrolled over the ring stage u, so every stage's
-      // operands are compile-time offsets from a0 / bdesc0 and the code
-      // between two MMA batches is a single barrier poll and a commit: with
-      // more work there (index arithmetic, a general wait loop) the tensor
-      // pipe idled between batches (measured: 257 vs 700 cycles per k-step).
-      int ks = 0;
-      while (ks < L.ksteps && ok) {
+      const uint32_t dacc = tmem + ab * RG::acc_cols;
+      // The stage-step loop is unrolled over the ring stage u, so every
+      // stage's operands are compile-time offsets from a0 / bdesc0 and the
+      // code between two MMA batches is a single barrier poll and a commit:
+      // with more work there (index arithmetic, a general wait loop) the
+      // tensor pipe idled between batches (measured: 257 vs 700 cycles per
+      // k-step).
+      int j = 0;
+      while (j < nss && ok) {
 #pragma unroll
         for (int u = 0; u < kStages; ++u) {
-          if (u == st && ks < L.ksteps && ok) {
+          if (u == st && j < nss && ok) {
             if (!warp_test_wait(&ready[u], ph)) {
               ok = spin_or_abort(&ready[u], ph, a.wait, abort_flag);
               ok = __shfl_sync(0xffffffffu, ok, 0);
             }
             if (ok) {
               tc_fence_after();
-              umma_ts_x4_elect(dacc, a0 + 32 * u, bdesc0 + (uint64_t)(u * (kBBytes >> 4)), idesc,
-                               ks != 0 ? 1u : 0u);
+              const int nk = KSUB == 1 ? 1 : min(KSUB, L.ksteps - j * KSUB);
+#pragma unroll
+              for (int h = 0; h < KSUB; ++h)
+                if (h < nk)
+                  umma_ts_x4_elect(dacc, a0 + RG::a_cols * u + 32 * h,
+                                   bdesc0 + (uint64_t)(((u * KSUB + h) * RG::bsub) >> 4), idesc,
+                                   (j != 0 || h != 0) ? 1u : 0u);
               tc_commit_elect(&empty[u]);
-              ++ks;
+              ++j;
               if (++st == kStages) {
                 st = 0;
                 ph ^= 1u;
@@ -697,9 +731,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const int grp = (warp - 4) >> 2;      // dequant group
     const int r = q * 32 + lane;          // TMEM lane = weight row of the tile
     const uint32_t zoff2 = ZPM == QMOE_ZP_OFFSET ? half_magic_offset<BF16>(a.zp_offset) : 0u;
-    // k-steps are numbered across tiles (kc); this group takes kc = grp,
+    // stage steps are numbered across tiles (kc); this group takes kc = grp,
     // grp + kDeqGroups, ...
-    const int n_steps = ((total_tiles - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x) * L.ksteps;
+    const int n_steps = ((total_tiles - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x) * nss;
     bool ok = true;
     for (int kc = grp; kc < n_steps && ok; kc += kDeqGroups) {
       // kStages is a multiple of kDeqGroups, so every use of stage s falls
@@ -709,11 +743,18 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after();
-      uint32_t v[32];
-      dequant_row<BITS, ZPM, BF16>(wring + s * wstage, L, r, zoff2, v);
-      const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + kAcol0 + s * 32;
-      TC_ST32(taddr, v);
-      tc_wait_st();
+      const int jj = KSUB == 1 ? 0 : kc % nss;
+      const int nk = KSUB == 1 ? 1 : min(KSUB, L.ksteps - jj * KSUB);
+      const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + RG::acol0 + s * RG::a_cols;
+#pragma unroll
+      for (int h = 0; h < KSUB; ++h) {
+        if (h < nk) {
+          uint32_t v[32];
+          dequant_row<BITS, ZPM, BF16>(wring + s * wslot + h * L.stage_bytes, L, r, zoff2, v);
+          TC_ST32(taddr + 32 * h, v);
+          tc_wait_st();   // v is reused by the next k-step of the stage
+        }
+      }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&ready[s]);
@@ -725,7 +766,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     // global memory sees 16-byte stores (fc1) / 16-byte reductions (fc2)
     // along the contiguous feature axis.
     const int q = warp & 3;
-    float* tile32 = reinterpret_cast<float*>(smem + GemmSmem::epi_off(wstage)) + q * 32 * kEpiPitch;
+    float* tile32 = reinterpret_cast<float*>(smem + RG::epi_off(L.stage_bytes)) + q * 32 * kEpiPitch;
     int tc = 0;
     bool ok = true;
     for (int tile = blockIdx.x; tile < total_tiles && ok; tile += gridDim.x, ++tc) {
@@ -738,7 +779,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       tc_fence_after();
       for (int c0 = 0; c0 < it.rows; c0 += 32) {
         uint32_t v[32];
-        TC_LD32(tmem + ((uint32_t)(q * 32) << 16) + ab * kAccCols + c0, v);
+        TC_LD32(tmem + ((uint32_t)(q * 32) << 16) + ab * RG::acc_cols + c0, v);
         // route of token column c0 + lane
         int my_tok = 0;
         float my_w = 0.f;
@@ -827,11 +868,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 // ----------------------------------------------------------------------------
 // Host side
 // ----------------------------------------------------------------------------
-template <int BITS, int ZPM, bool BF16, bool GLU>
+template <int BITS, int ZPM, bool BF16, bool GLU, bool DEC>
 static cudaError_t launch_g(const GemmArgs& a, cudaStream_t s) {
-  const int wstage = (a.L.stage_bytes + 127) / 128 * 128;
-  const int smem = GemmSmem::total(wstage) + 1024;  // + alignment slack
-  auto kern = gemm_kernel<BITS, ZPM, BF16, GLU>;
+  const int smem = Ring<DEC>::total(a.L.stage_bytes) + 1024;  // + alignment slack
+  auto kern = gemm_kernel<BITS, ZPM, BF16, GLU, DEC>;
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (err != cudaSuccess) return err;
   cudaLaunchConfig_t cfg = {};
@@ -847,9 +887,13 @@ static cudaError_t launch_g(const GemmArgs& a, cudaStream_t s) {
   return cudaLaunchKernelEx(&cfg, kern, a);
 }
 
+template <int BITS, int ZPM, bool BF16, bool GLU>
+static cudaError_t launch_g_ring(const GemmArgs& a, cudaStream_t s) {
+  return a.dec ? launch_g<BITS, ZPM, BF16, GLU, true>(a, s) : launch_g<BITS, ZPM, BF16, GLU, false>(a, s);
+}
 template <int BITS, int ZPM, bool BF16>
 static cudaError_t launch_g_glu(const GemmArgs& a, cudaStream_t s) {
-  return a.fc == 1 ? launch_g<BITS, ZPM, BF16, true>(a, s) : launch_g<BITS, ZPM, BF16, false>(a, s);
+  return a.fc == 1 ? launch_g_ring<BITS, ZPM, BF16, true>(a, s) : launch_g_ring<BITS, ZPM, BF16, false>(a, s);
 }
 template <int BITS, int ZPM>
 static cudaError_t launch_g_dt(const GemmArgs& a, cudaStream_t s) {

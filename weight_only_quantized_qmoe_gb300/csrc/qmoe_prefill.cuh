@@ -48,10 +48,11 @@ __host__ __device__ inline size_t tok_tile_offset(int item, int ksteps, int s) {
 struct GemmArgs {
   const uint8_t* wq;       // GEMM layout
   GemmLayout L;
-  const Item* items;       // class-1 work-list (e, start, rows <= 128)
+  const Item* items;       // class-1 work-list (e, start, rows <= 128; <= 64 when dec)
   const int* n_items;
   int max_items;
   int grid;                // persistent CTAs
+  int dec;                 // every item has <= 64 rows: the decode ring shape (128-deep stages)
   int fc, zp_mode, bf16;
   ActParams act;
   const float* bias;       // fc1: [E, I, 2] (gate, up) pairs ; fc2: [E, H] ; or null
