@@ -34,9 +34,14 @@ def test_create_validates(lib):
     st, h = _create()
     assert st == b.QMOE_OK and h
     b.qmoe_destroy(h)
+    for widths in ((8, 8), (8, 2), (3, 8)):
+        st, h = _create(bits_fc1=widths[0], bits_fc2=widths[1])
+        assert st == b.QMOE_OK and h, widths
+        b.qmoe_destroy(h)
     for kw, want in [
         (dict(bits_fc1=5), b.QMOE_ERR_UNSUPPORTED),
-        (dict(bits_fc2=8), b.QMOE_ERR_UNSUPPORTED),
+        (dict(bits_fc2=7), b.QMOE_ERR_UNSUPPORTED),
+        (dict(bits_fc1=1), b.QMOE_ERR_UNSUPPORTED),
         (dict(block_size=16), b.QMOE_ERR_UNSUPPORTED),
         (dict(top_k=9), b.QMOE_ERR_INVALID_ARG),
         (dict(top_k=0), b.QMOE_ERR_INVALID_ARG),

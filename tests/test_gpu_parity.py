@@ -169,6 +169,23 @@ def _width_cases():
 
 
 WIDTH_CASES = dict(_width_cases())
+# 8-bit codes (fp16 magic path; bf16 nibble-split path) with every zero-point
+# mode, mixed with narrower widths, and on the fp32 SIMT path; scales sized so
+# that fp16 outputs stay in range with codes up to +-255 from the centre.
+WIDTH_CASES.update({
+    "w88_B32_sym_f16": dict(bits1=8, bits2=8, B=32, dtype="f16", T=12, scale_lo=0.0005, scale_hi=0.002),
+    "w88_B128_sym_bf16": dict(bits1=8, bits2=8, B=128, dtype="bf16", T=12, scale_lo=0.0005, scale_hi=0.002),
+    "w84_B64_uint8_bf16": dict(bits1=8, bits2=4, B=64, zp_mode="uint8", zp_lo=0, zp_hi=15, dtype="bf16",
+                               T=12, scale_lo=0.0005, scale_hi=0.002),
+    "w88_B32_uint8_far_bf16": dict(bits1=8, bits2=8, B=32, zp_mode="uint8", zp_lo=20, zp_hi=240,
+                                   dtype="bf16", T=12, scale_lo=0.0005, scale_hi=0.002),
+    "w28_B64_offset_half_f16": dict(bits1=2, bits2=8, B=64, zp_mode="offset", zp_offset=1.5, dtype="f16",
+                                    T=12, scale_lo=0.01, scale_hi=0.03),
+    "w48_B32_offset_int_bf16": dict(bits1=4, bits2=8, B=32, zp_mode="offset", zp_offset=3.0,
+                                    dtype="bf16", T=12, scale_lo=0.002, scale_hi=0.006),
+    "w88_B64_uint8_f32": dict(bits1=8, bits2=8, B=64, zp_mode="uint8", zp_lo=90, zp_hi=170, dtype="f32",
+                              T=9, scale_lo=0.0005, scale_hi=0.002),
+})
 
 
 @pytest.mark.parametrize("path", sorted(PATHS))

@@ -41,7 +41,9 @@ DecodeLayout make_decode_layout(int bits, int B, int N_rows_per_sub, int K, int 
   L.code_bytes = 16 * L.SC * bits / 8;
   const int nb = L.SC / B;
   L.scale_bytes = nb * 8 * 2 * dsize;
-  L.zp_bytes = zp_mode == QMOE_ZP_UINT8 ? ((nb * 8 + 15) / 16) * 16 : 0;
+  // uint8 zero points of rows g and g+8 per block: two nibbles in one byte,
+  // or two bytes for 8-bit codes
+  L.zp_bytes = zp_mode == QMOE_ZP_UINT8 ? ((nb * (bits == 8 ? 16 : 8) + 15) / 16) * 16 : 0;
   L.scb = nsub * (L.code_bytes + L.scale_bytes + L.zp_bytes);
   L.tile_bytes = (size_t)L.nkc * L.scb;
   L.expert_bytes = L.tile_bytes * L.ntiles;
@@ -92,7 +94,23 @@ __global__ void repack_decode_kernel(const RepackArgs a) {
       return kc * L.SC + j * 16 + 2 * t + ((r & 2) ? 8 : 0) + e2;
     };
     uint32_t* cw = reinterpret_cast<uint32_t*>(out + s * L.code_bytes);
-    if (bits == 4) {
+    if (bits == 8) {
+      // two words per lane and k-tile: word 2j + (r >> 1) holds pair r in
+      // bytes (r & 1) and 2 + (r & 1)
+      const int W = 2 * ktiles;
+      for (int i = threadIdx.x; i < 32 * W; i += blockDim.x) {
+        const int lane = i / W, wj = i % W, g = lane >> 2, t = lane & 3;
+        const int j = wj >> 1;
+        uint32_t w = 0;
+        for (int rr = 0; rr < 2; ++rr) {
+          const int r = 2 * (wj & 1) + rr;
+          const int row = crow(g + ((r & 1) ? 8 : 0));
+          w |= (uint32_t)code(row, kidx(j, t, r, 0)) << (8 * rr);
+          w |= (uint32_t)code(row, kidx(j, t, r, 1)) << (16 + 8 * rr);
+        }
+        cw[lane * W + wj] = w;
+      }
+    } else if (bits == 4) {
       const int W = ktiles;  // words per lane
       for (int i = threadIdx.x; i < 32 * W; i += blockDim.x) {
         const int lane = i / W, j = i % W, g = lane >> 2, t = lane & 3;
@@ -151,7 +169,13 @@ __global__ void repack_decode_kernel(const RepackArgs a) {
       uint8_t* zp = out + L.nsub * (L.code_bytes + L.scale_bytes) + s * L.zp_bytes;
       for (int i = threadIdx.x; i < L.zp_bytes; i += blockDim.x) {
         uint8_t v = 0;
-        if (i < nb * 8) {
+        if (bits == 8 && i < nb * 16) {
+          // [blk][g][row g, row g+8]
+          const int blk = i / 16, g = (i % 16) / 2, hi = i % 2, kb = kc * nb + blk;
+          if (kb < nblk_row)
+            v = (uint8_t)canon_code(a.zp + ((size_t)e * a.N + crow(g + 8 * hi)) * zrow_bytes, zrow_bytes, bits,
+                                    kb, nblk_row);
+        } else if (bits != 8 && i < nb * 8) {
           const int blk = i / 8, g = i % 8, kb = kc * nb + blk;
           if (kb < nblk_row) {
             const uint8_t* z0 = a.zp + ((size_t)e * a.N + crow(g)) * zrow_bytes;
@@ -180,6 +204,7 @@ cudaError_t launch_decode_mma_bits(const DecodeArgs& a, cudaStream_t s);
 extern template cudaError_t launch_decode_mma_bits<2>(const DecodeArgs&, cudaStream_t);
 extern template cudaError_t launch_decode_mma_bits<3>(const DecodeArgs&, cudaStream_t);
 extern template cudaError_t launch_decode_mma_bits<4>(const DecodeArgs&, cudaStream_t);
+extern template cudaError_t launch_decode_mma_bits<8>(const DecodeArgs&, cudaStream_t);
 
 cudaError_t launch_decode_mma(const DecodeArgs& a, cudaStream_t s) {
   if (a.max_items <= 0) return cudaSuccess;
@@ -188,6 +213,7 @@ cudaError_t launch_decode_mma(const DecodeArgs& a, cudaStream_t s) {
     case 2: return launch_decode_mma_bits<2>(a, s);
     case 3: return launch_decode_mma_bits<3>(a, s);
     case 4: return launch_decode_mma_bits<4>(a, s);
+    case 8: return launch_decode_mma_bits<8>(a, s);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -36,7 +36,9 @@ __host__ __device__ inline DecodeSmem decode_smem(const DecodeLayout& L, int NG,
 // 16-bit fields, low element in bits 0.., high element in bits 16..).
 template <int BITS>
 __device__ __forceinline__ uint32_t code_pair(const uint32_t* cw, const uint32_t* hw, int j, int r) {
-  if (BITS == 4) {
+  if (BITS == 8) {
+    return cw[2 * j + (r >> 1)] >> (8 * (r & 1));   // bytes 0 and 2 (bits above ignored)
+  } else if (BITS == 4) {
     return (cw[j] >> (4 * r)) & 0x000F000Fu;
   } else if (BITS == 2) {
     return (cw[j >> 1] >> (2 * ((j & 1) * 4 + r))) & 0x00030003u;
@@ -164,8 +166,13 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
 
   const int ng_act = (it.rows + 7) >> 3;
   constexpr uint32_t MAGIC = Magic<BF16>::v;
-  const uint32_t zoff2 = ZPM == QMOE_ZP_OFFSET ? half_magic_offset<BF16>(a.zp_offset) : 0u;
-  constexpr uint32_t ZSYM = MAGIC | ((1u << (BITS - 1)) * 0x00010001u);
+  // offset zero point: the half-unit magic pair, or for bf16 8-bit codes
+  // (whose accepted offsets are integers) the pair (z, z)
+  uint32_t zoff2 = 0u;
+  if constexpr (ZPM == QMOE_ZP_OFFSET)
+    zoff2 = (BITS == 8 && BF16) ? (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(a.zp_offset)) * 0x00010001u
+                                : half_magic_offset<BF16>(a.zp_offset);
+  const uint32_t ZSYM = BITS == 8 ? code8_zq<BF16>(128u) : MAGIC | ((1u << (BITS - 1)) * 0x00010001u);
 
   bool ok = true;
   int i = 0;
@@ -182,7 +189,7 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
       const uint8_t* ch = st + c * L.scb;
       const int kc = kc0 + i * g_chunks + c;
       // this lane's code words for each sub-tile
-      constexpr int WPL = BITS == 4 ? SC / 16 : SC / 32;   // (low-plane) words per lane
+      constexpr int WPL = BITS == 8 ? SC / 8 : (BITS == 4 ? SC / 16 : SC / 32);   // (low-plane) words per lane
       constexpr int WPH = BITS == 3 ? SC / 64 : 1;
       uint32_t cw[NSUB][WPL];
       uint32_t hw[NSUB][WPH];
@@ -218,9 +225,15 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
           ss[s][0] = __byte_perm(sp, 0, 0x1010);   // (s_g, s_g)
           ss[s][1] = __byte_perm(sp, 0, 0x3232);   // (s_g8, s_g8)
           if (ZPM == QMOE_ZP_UINT8) {
-            const uint32_t zb = ch[NSUB * (L.code_bytes + L.scale_bytes) + s * L.zp_bytes + blk * 8 + g];
-            zz[s][0] = MAGIC | ((zb & 15u) * 0x00010001u);
-            zz[s][1] = MAGIC | ((zb >> 4) * 0x00010001u);
+            const uint8_t* zpp = ch + NSUB * (L.code_bytes + L.scale_bytes) + s * L.zp_bytes;
+            if constexpr (BITS == 8) {
+              zz[s][0] = code8_zq<BF16>(zpp[blk * 16 + 2 * g]);
+              zz[s][1] = code8_zq<BF16>(zpp[blk * 16 + 2 * g + 1]);
+            } else {
+              const uint32_t zb = zpp[blk * 8 + g];
+              zz[s][0] = MAGIC | ((zb & 15u) * 0x00010001u);
+              zz[s][1] = MAGIC | ((zb >> 4) * 0x00010001u);
+            }
           } else {
             zz[s][0] = zz[s][1] = ZSYM;
           }
@@ -234,7 +247,13 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
 #pragma unroll
             for (int r = 0; r < 4; ++r) {
               uint32_t v;
-              if constexpr (ZPM == QMOE_ZP_OFFSET) {
+              if constexpr (BITS == 8) {
+                const uint32_t b = code_pair<BITS>(cw[s], hw[s], j, r);
+                if constexpr (ZPM == QMOE_ZP_OFFSET && !BF16)
+                  v = sub2<false>(((b & 0x00FF00FFu) << 1) | Magic<false>::half, zoff2);
+                else
+                  v = code8_minus_zp<BF16>(b, ZPM == QMOE_ZP_OFFSET ? zoff2 : zz[s][r & 1]);
+              } else if constexpr (ZPM == QMOE_ZP_OFFSET) {
                 // half-unit magic: (M/2 + c) - (M/2 + z) = c - z, exact for
                 // half-integer z (the only centres the API accepts)
                 v = (code_pair<BITS>(cw[s], hw[s], j, r) << 1) | Magic<BF16>::half;

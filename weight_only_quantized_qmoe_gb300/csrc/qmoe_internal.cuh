@@ -343,6 +343,44 @@ __device__ __forceinline__ uint32_t half_magic_offset(float z) {
   return (uint32_t)__half_as_ushort(__float2half_rn(v)) * 0x00010001u;
 }
 
+// 8-bit codes.  The pair of 8-bit codes sits in bits 0-7 and 16-23 of b (the
+// bits above each are ignored); zq is the zero point of each as the kernels'
+// subtrahend: fp16 (M + z, M + z) with M = 1024 (the fp16 significand holds
+// M + c exactly); bf16 (z, z), because its 8-bit significand cannot hold
+// 128 + c for c >= 128: there each code is split into nibbles, each made
+// exact with M = 128, and rejoined as 16 hi + lo (exact below 256) before z
+// is subtracted.  Either way the pair c - z is exact.
+template <bool BF16>
+__device__ __forceinline__ uint32_t fma2(uint32_t a, uint32_t b, uint32_t c);
+template <>
+__device__ __forceinline__ uint32_t fma2<true>(uint32_t a, uint32_t b, uint32_t c) {
+  uint32_t d;
+  asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+template <>
+__device__ __forceinline__ uint32_t fma2<false>(uint32_t a, uint32_t b, uint32_t c) {
+  uint32_t d;
+  asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+template <bool BF16>
+__device__ __forceinline__ uint32_t code8_minus_zp(uint32_t b, uint32_t zq) {
+  if constexpr (!BF16) {
+    return sub2<false>((b & 0x00FF00FFu) | Magic<false>::v, zq);
+  } else {
+    const uint32_t lo = sub2<true>((b & 0x000F000Fu) | Magic<true>::v, Magic<true>::v);
+    const uint32_t hi = sub2<true>(((b >> 4) & 0x000F000Fu) | Magic<true>::v, Magic<true>::v);
+    return sub2<true>(fma2<true>(hi, 0x41804180u /* (16, 16) */, lo), zq);
+  }
+}
+// The subtrahend pair of code8_minus_zp for an integer zero point z in [0, 255].
+template <bool BF16>
+__device__ __forceinline__ uint32_t code8_zq(uint32_t z) {
+  if constexpr (BF16) return (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn((float)z)) * 0x00010001u;
+  else return Magic<false>::v | (z * 0x00010001u);
+}
+
 // D = A(16x16, row) * B(16x8, col) + C, fp32 accumulate.
 template <bool BF16>
 __device__ __forceinline__ void mma16816(float* c, const uint32_t* a, uint32_t b0, uint32_t b1);

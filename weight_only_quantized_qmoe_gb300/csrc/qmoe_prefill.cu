@@ -76,7 +76,14 @@ __global__ void repack_gemm_kernel(const GemmRepackArgs a) {
   uint8_t* stage = a.out + ((((size_t)e * L.ntiles + nt) * L.ksteps) + ks) * L.stage_bytes;
   uint32_t* cw = reinterpret_cast<uint32_t*>(stage + (size_t)r * L.code_row);
   const int k0 = ks * 64;
-  if (bits == 4) {
+  if (bits == 8) {
+    // word i: k pairs 2i (bytes 0 and 2) and 2i+1 (bytes 1 and 3)
+    for (int i = 0; i < 16; ++i) {
+      const int kk = k0 + 4 * i;
+      cw[i] = (uint32_t)code(kk) | ((uint32_t)code(kk + 2) << 8) | ((uint32_t)code(kk + 1) << 16) |
+              ((uint32_t)code(kk + 3) << 24);
+    }
+  } else if (bits == 4) {
     for (int i = 0; i < 8; ++i) {
       uint32_t w = 0;
       for (int m = 0; m < 4; ++m) {
@@ -445,9 +452,15 @@ __device__ __forceinline__ void dequant_row(const uint8_t* stage, const GemmLayo
                                             uint32_t* v) {
   constexpr uint32_t MAGIC = BF16 ? 0x43004300u : 0x64006400u;
   const uint8_t* row = stage + r * (64 * BITS / 8);
-  constexpr int NW = BITS == 4 ? 8 : (BITS == 3 ? 6 : 4);
+  constexpr int NW = BITS == 8 ? 16 : (BITS == 4 ? 8 : (BITS == 3 ? 6 : 4));
   uint32_t w[NW];
-  if constexpr (BITS == 4) {
+  if constexpr (BITS == 8) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint4 q = reinterpret_cast<const uint4*>(row)[i];
+      w[4 * i] = q.x; w[4 * i + 1] = q.y; w[4 * i + 2] = q.z; w[4 * i + 3] = q.w;
+    }
+  } else if constexpr (BITS == 4) {
     const uint4 q0 = reinterpret_cast<const uint4*>(row)[0];
     const uint4 q1 = reinterpret_cast<const uint4*>(row)[1];
     w[0] = q0.x; w[1] = q0.y; w[2] = q0.z; w[3] = q0.w;
@@ -471,12 +484,29 @@ __device__ __forceinline__ void dequant_row(const uint8_t* stage, const GemmLayo
   const uint32_t ss0 = (uint32_t)sc[0] * 0x00010001u;
   const uint32_t ss1 = (uint32_t)sc[b1] * 0x00010001u;
   uint32_t zz0 = MAGIC | ((1u << (BITS - 1)) * 0x00010001u), zz1 = zz0;
+  if constexpr (BITS == 8) zz0 = zz1 = code8_zq<BF16>(128u);
   if constexpr (ZPM == QMOE_ZP_UINT8) {
-    zz0 = MAGIC | ((uint32_t)zp[0] * 0x00010001u);
-    zz1 = MAGIC | ((uint32_t)zp[b1] * 0x00010001u);
+    if constexpr (BITS == 8) {
+      zz0 = code8_zq<BF16>(zp[0]);
+      zz1 = code8_zq<BF16>(zp[b1]);
+    } else {
+      zz0 = MAGIC | ((uint32_t)zp[0] * 0x00010001u);
+      zz1 = MAGIC | ((uint32_t)zp[b1] * 0x00010001u);
+    }
   }
 #pragma unroll
   for (int j = 0; j < 32; ++j) {
+    if constexpr (BITS == 8) {
+      // word j/2 holds the pairs 2(j/2) and 2(j/2)+1: bytes (0, 2) and (1, 3)
+      const uint32_t b = w[j >> 1] >> (8 * (j & 1));
+      uint32_t x;
+      if constexpr (ZPM == QMOE_ZP_OFFSET && !BF16)
+        x = sub2<false>(((b & 0x00FF00FFu) << 1) | Magic<false>::half, zoff2);
+      else
+        x = code8_minus_zp<BF16>(b, ZPM == QMOE_ZP_OFFSET ? zoff2 : (j < 16 ? zz0 : zz1));
+      v[j] = mul2<BF16>(x, j < 16 ? ss0 : ss1);
+      continue;
+    }
     uint32_t p;
     if constexpr (BITS == 4) p = (w[j >> 2] >> (4 * (j & 3))) & 0x000F000Fu;
     else if constexpr (BITS == 2) p = (w[j >> 3] >> (2 * (j & 7))) & 0x00030003u;
@@ -510,8 +540,8 @@ __device__ __forceinline__ float glu_fast(const ActParams& p, float g, float u) 
 // The weight tiles of one token tile run on neighbouring CTAs at the same
 // time; starting each at a different k-step (rotation by nt) spreads their
 // reads of the shared token tile over the L2 instead of hitting the same lines
-// together.  The MMA sums the k-steps in any order.  With two k-steps per
-// stage the pairs stay aligned (no rotation): a stage's k-steps are then one
+// together.  The MMA sums the k-steps in any order.  With several k-steps per
+// stage they stay aligned (no rotation): a stage's k-steps are then one
 // contiguous weight copy.
 struct TileSrc {
   const uint8_t* w;     // k-step kr at w + kr * stage_bytes
@@ -530,7 +560,7 @@ __device__ __forceinline__ TileSrc tile_src(const GemmArgs& a, int tile) {
   // only the 8-row groups that hold the item's rows (the MMA reads stale
   // rows past them into columns that are never stored)
   r.b_bytes = (uint32_t)min(Ring<DEC>::bsub, ((it.rows + 7) / 8) * 1024);
-  r.rot = DEC ? 0 : (int)(((long long)nt * L.ksteps) / L.ntiles);
+  r.rot = Ring<DEC>::ksub > 1 ? 0 : (int)(((long long)nt * L.ksteps) / L.ntiles);
   return r;
 }
 
@@ -730,7 +760,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const int q = warp & 3;
     const int grp = (warp - 4) >> 2;      // dequant group
     const int r = q * 32 + lane;          // TMEM lane = weight row of the tile
-    const uint32_t zoff2 = ZPM == QMOE_ZP_OFFSET ? half_magic_offset<BF16>(a.zp_offset) : 0u;
+    // offset zero point: the half-unit magic pair, or for bf16 8-bit codes
+    // (whose accepted offsets are integers) the pair (z, z)
+    uint32_t zoff2 = 0u;
+    if constexpr (ZPM == QMOE_ZP_OFFSET)
+      zoff2 = (BITS == 8 && BF16) ? (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(a.zp_offset)) * 0x00010001u
+                                  : half_magic_offset<BF16>(a.zp_offset);
     // stage steps are numbered across tiles (kc); this group takes kc = grp,
     // grp + kDeqGroups, ...
     const int n_steps = ((total_tiles - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x) * nss;
@@ -912,6 +947,7 @@ cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t s) {
     case 2: return launch_g_zp<2>(a, s);
     case 3: return launch_g_zp<3>(a, s);
     case 4: return launch_g_zp<4>(a, s);
+    case 8: return launch_g_zp<8>(a, s);
     default: return cudaErrorInvalidValue;
   }
 }
