@@ -407,31 +407,36 @@ __device__ __forceinline__ bool spin_or_abort(uint64_t* bar, uint32_t parity, co
 // producer: empty -> copies -> full;  dequant: full -> A -> ready;
 // MMA: ready -> MMAs -> commit empty.
 constexpr int kTmemCols = 512;
-constexpr int kDeqGroups = 3;     // dequant warp groups (4 warps each), stage step kc -> group kc % 3
-constexpr int kEpiWarp0 = 4 + 4 * kDeqGroups;
-constexpr int kGemmThreads = (kEpiWarp0 + 4) * 32;  // see the role map in the kernel
 constexpr int kEpiPitch = 36;     // fp32 words per row of an epilogue transpose tile (pad: banks)
 constexpr int kEpiBytes = 4 * 32 * kEpiPitch * 4;   // one 32x32 tile per epilogue warp
 
-// The two ring shapes.  Prefill items carry up to 128 token rows: two
-// 128-column accumulators and one k-step per stage.  Decode items (T <= 64)
-// carry at most 64 rows: two 64-column accumulators, and the TMEM this frees
-// holds 128-deep stages, so each barrier round, copy and commit covers twice
-// the MMA work (the hand-offs, not the MMAs, pace the ring at these shapes).
-template <bool DEC>
+// The two ring shapes; both hold two 64-deep k-steps per stage, so each
+// barrier round, copy and commit covers two k-steps of MMAs (the hand-offs,
+// not the MMAs, pace the ring at these shapes).  Prefill items carry up to
+// 128 token rows: two 128-column accumulators leave TMEM for 4 stages.
+// Decode items (T <= 64) carry at most 64 rows: two 64-column accumulators
+// leave room for 6 stages.
+// Dequant warp groups (4 warps each; stage step kc -> group kc % groups):
+// two, except three for the decode shape's 3-bit codes, whose two-plane
+// unpack is the longest dequant (measured: two groups 147 vs three 135 µs on
+// the mixed-width fc1; the other widths ran 2-4 % faster with two).
+template <bool DEC, int BITS = 4>
 struct Ring {
-  static constexpr int stages = 6;
-  static constexpr int ksub = DEC ? 2 : 1;          // 64-deep k-steps per stage
+  static constexpr int stages = DEC ? 6 : 4;
+  static constexpr int ksub = 2;                    // 64-deep k-steps per stage
+  static constexpr int groups = (DEC && BITS == 3) ? 3 : 2;
+  static constexpr int epi_warp0 = 4 + 4 * groups;  // first epilogue warp
+  static constexpr int threads = (epi_warp0 + 4) * 32;
   static constexpr int tile_n = DEC ? 64 : 128;     // token rows per item (MMA N <= tile_n)
   static constexpr int bsub = tile_n * 128;         // shared bytes of one k-step's token tile
   static constexpr int acc_cols = tile_n;           // accumulators: [0, acc) and [acc, 2 acc)
   static constexpr int acol0 = 2 * acc_cols;        // first TMEM column of the A ring
   static constexpr int a_cols = 32 * ksub;          // A columns per stage
   // Each stage is always dequantised by the same group (stage s -> group
-  // s % 3), so a group consumes its stages' phases in order and never runs a
-  // ring ahead of a fill that has not landed (a parity test could not tell
-  // those apart).
-  static_assert(stages % kDeqGroups == 0, "a stage belongs to one dequant group");
+  // s % groups), so a group consumes its stages' phases in order and
+  // never runs a ring ahead of a fill that has not landed (a parity test
+  // could not tell those apart).
+  static_assert(stages % groups == 0, "a stage belongs to one dequant group");
   static_assert(acol0 + stages * a_cols <= kTmemCols, "TMEM columns");
   // shared memory: B ring, W ring (128-byte aligned slots), epilogue tiles, barriers
   __host__ __device__ static int wslot(int stage_bytes) { return (ksub * stage_bytes + 127) / 128 * 128; }
@@ -579,19 +584,21 @@ __device__ __forceinline__ void bulk_g2s_elect(void* dst, const void* src, uint3
       : "memory");
 }
 
-// Warp roles (8 + 4 * kDeqGroups warps):
+// Warp roles (8 + 4 * groups warps):
 //   0      bulk-copy producer (whole warp, elect.sync): W + B of a stage into slot s
 //   1      MMA issuer (whole warp, elect.sync) and TMEM owner
 //   2..3   idle
-//   4 ..   dequant groups of 4 warps; group g takes stage steps kc % kDeqGroups == g,
+//   4 ..   dequant groups of 4 warps; group g takes stage steps kc % groups == g,
 //          warp w owns TMEM lanes 32*(w%4)
 //   last 4 epilogue (TMEM lanes 32*(w%4))
 // The MMA issuer polls without suspending (it paces the ring); the producer,
 // dequant and epilogue warps park on their barriers.
 template <int BITS, int ZPM, bool BF16, bool GLU, bool DEC>
-__global__ void __launch_bounds__(kGemmThreads, 1)
+__global__ void __launch_bounds__((Ring<DEC, BITS>::threads), 1)
     gemm_kernel(const GemmArgs a) {
-  using RG = Ring<DEC>;
+  using RG = Ring<DEC, BITS>;
+  constexpr int kDeqGroups = RG::groups;
+  constexpr int kEpiWarp0 = RG::epi_warp0;
   constexpr int kStages = RG::stages;
   constexpr int KSUB = RG::ksub;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -905,7 +912,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 // ----------------------------------------------------------------------------
 template <int BITS, int ZPM, bool BF16, bool GLU, bool DEC>
 static cudaError_t launch_g(const GemmArgs& a, cudaStream_t s) {
-  const int smem = Ring<DEC>::total(a.L.stage_bytes) + 1024;  // + alignment slack
+  const int smem = Ring<DEC, BITS>::total(a.L.stage_bytes) + 1024;  // + alignment slack
   auto kern = gemm_kernel<BITS, ZPM, BF16, GLU, DEC>;
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (err != cudaSuccess) return err;
@@ -914,7 +921,7 @@ static cudaError_t launch_g(const GemmArgs& a, cudaStream_t s) {
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.gridDim = dim3(a.grid);
-  cfg.blockDim = dim3(kGemmThreads);
+  cfg.blockDim = dim3(Ring<DEC, BITS>::threads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
   cfg.attrs = attr;
