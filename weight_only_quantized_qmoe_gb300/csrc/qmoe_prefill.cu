@@ -396,7 +396,7 @@ __device__ __forceinline__ bool spin_or_abort(uint64_t* bar, uint32_t parity, co
 // ----------------------------------------------------------------------------
 // The grouped GEMM kernel
 // ----------------------------------------------------------------------------
-// One ring of Ring<DEC>::stages stages: stage s holds KSUB consecutive 64-deep
+// One ring of Ring<>::stages stages: stage s holds KSUB consecutive 64-deep
 // k-steps -- their token tiles (B, shared memory), their packed weights (W,
 // shared memory, one contiguous copy) and their dequantised weights (A, 32
 // TMEM columns per k-step).  Three barriers per stage, one wait per role and
@@ -410,20 +410,21 @@ constexpr int kTmemCols = 512;
 constexpr int kEpiPitch = 36;     // fp32 words per row of an epilogue transpose tile (pad: banks)
 constexpr int kEpiBytes = 4 * 32 * kEpiPitch * 4;   // one 32x32 tile per epilogue warp
 
-// The two ring shapes; both hold two 64-deep k-steps per stage, so each
-// barrier round, copy and commit covers two k-steps of MMAs (the hand-offs,
-// not the MMAs, pace the ring at these shapes).  Prefill items carry up to
-// 128 token rows: two 128-column accumulators leave TMEM for 4 stages.
-// Decode items (T <= 64) carry at most 64 rows: two 64-column accumulators
-// leave room for 6 stages.
+// The two ring shapes.  A stage holds several 64-deep k-steps, so each
+// barrier round, copy and commit covers several k-steps of MMAs (the
+// hand-offs, not the MMAs, pace the ring at these shapes).  Prefill items
+// carry up to 128 token rows: two 128-column accumulators leave TMEM for 4
+// stages of 2 k-steps.  Decode items (T <= 64) carry at most 64 rows: two
+// 64-column accumulators leave TMEM for 4 stages of 3 k-steps (6 of 2 for
+// 3-bit codes, whose three dequant groups need a ring depth divisible by 3).
 // Dequant warp groups (4 warps each; stage step kc -> group kc % groups):
 // two, except three for the decode shape's 3-bit codes, whose two-plane
 // unpack is the longest dequant (measured: two groups 147 vs three 135 µs on
 // the mixed-width fc1; the other widths ran 2-4 % faster with two).
 template <bool DEC, int BITS = 4>
 struct Ring {
-  static constexpr int stages = DEC ? 6 : 4;
-  static constexpr int ksub = 2;                    // 64-deep k-steps per stage
+  static constexpr int stages = DEC ? (BITS == 3 ? 6 : 4) : 4;
+  static constexpr int ksub = DEC ? (BITS == 3 ? 2 : 3) : 2;   // 64-deep k-steps per stage
   static constexpr int groups = (DEC && BITS == 3) ? 3 : 2;
   static constexpr int epi_warp0 = 4 + 4 * groups;  // first epilogue warp
   static constexpr int threads = (epi_warp0 + 4) * 32;
@@ -554,7 +555,7 @@ struct TileSrc {
   uint32_t b_bytes;     // token bytes copied per k-step
   int rot;              // first k-step
 };
-template <bool DEC>
+template <bool DEC, int BITS>
 __device__ __forceinline__ TileSrc tile_src(const GemmArgs& a, int tile) {
   const GemmLayout& L = a.L;
   const int item = tile / L.ntiles, nt = tile - item * L.ntiles;
@@ -564,8 +565,8 @@ __device__ __forceinline__ TileSrc tile_src(const GemmArgs& a, int tile) {
   r.b = a.btiles + tok_tile_offset(item, L.ksteps, 0);
   // only the 8-row groups that hold the item's rows (the MMA reads stale
   // rows past them into columns that are never stored)
-  r.b_bytes = (uint32_t)min(Ring<DEC>::bsub, ((it.rows + 7) / 8) * 1024);
-  r.rot = Ring<DEC>::ksub > 1 ? 0 : (int)(((long long)nt * L.ksteps) / L.ntiles);
+  r.b_bytes = (uint32_t)min(Ring<DEC, BITS>::bsub, ((it.rows + 7) / 8) * 1024);
+  r.rot = Ring<DEC, BITS>::ksub > 1 ? 0 : (int)(((long long)nt * L.ksteps) / L.ntiles);
   return r;
 }
 
@@ -658,7 +659,7 @@ __global__ void __launch_bounds__((Ring<DEC, BITS>::threads), 1)
     for (int tile = blockIdx.x; tile < total_tiles && ok; tile += gridDim.x) {
       // (An L2 bulk prefetch a ring's depth ahead of each copy made the
       // kernel twice as slow: the copies queue behind the prefetches.)
-      const TileSrc src = tile_src<DEC>(a, tile);
+      const TileSrc src = tile_src<DEC, BITS>(a, tile);
       int kr = src.rot;
       for (int j = 0; j < nss; ++j, ++kc) {
         const int s = kc % kStages;
