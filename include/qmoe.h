@@ -130,18 +130,25 @@ qmoe_status qmoe_set_zero_point_offset(qmoe_layer* layer, float offset);
 qmoe_status qmoe_set_swiglu_params(qmoe_layer* layer, float alpha, float beta, float limit);
 
 /* Row order of fc1's canonical codes / scales / zero points / bias
- * [qmoe.rs qmoe_activate, swiglu_fusion]: 0 = concatenated [gate (I rows) |
- * up (I rows)] (default, swiglu_fusion 2), 1 = interleaved (row 2f = gate f,
- * row 2f+1 = up f; swiglu_fusion 1).  Must precede qmoe_prepack(fc = 1) and
- * qmoe_set_bias(fc = 1); STATE otherwise. */
-qmoe_status qmoe_set_fc1_layout(qmoe_layer* layer, int interleaved);
+ * [qmoe.rs qmoe_activate, swiglu_fusion]: QMOE_FC1_CONCAT = concatenated
+ * [gate (I rows) | up (I rows)] (default, swiglu_fusion 2),
+ * QMOE_FC1_INTERLEAVED = interleaved (row 2f = gate f, row 2f+1 = up f;
+ * swiglu_fusion 1), QMOE_FC1_SEPARATE_FC3 = fc1 holds the I gate rows and a
+ * third projection fc3 the I up rows (qmoe_activate with fc3: gate = fc1,
+ * linear = fc3), each [E, I, ...] and prepacked / biased with fc = 1 and
+ * fc = 3.  Other values: INVALID_ARG.  Must precede qmoe_prepack(fc = 1 or 3)
+ * and qmoe_set_bias(fc = 1 or 3); STATE otherwise. */
+enum { QMOE_FC1_CONCAT = 0, QMOE_FC1_INTERLEAVED = 1, QMOE_FC1_SEPARATE_FC3 = 2 };
+qmoe_status qmoe_set_fc1_layout(qmoe_layer* layer, int layout);
 
 /* Projection biases [qmoe.rs qmoe_linear_impl: output = sum + bias[e*N + n]]:
  * bias_dev is a float32 device array [E, N] (fc1: N = 2*inter in the fc1 row
- * order; fc2: N = hidden), added to the projection output (fc1 before the
- * gated activation, fc2 before the weighted combine).  The layer keeps its own
- * copy (the caller may free bias_dev once `stream` has been synchronised).
- * NULL removes the bias (synchronises `stream` first). */
+ * order, or inter with QMOE_FC1_SEPARATE_FC3; fc2: N = hidden; fc3: N = inter,
+ * only with QMOE_FC1_SEPARATE_FC3), added to the projection output (fc1 and
+ * fc3 before the gated activation, fc2 before the weighted combine).  The
+ * layer keeps its own copy (the caller may free bias_dev once `stream` has
+ * been synchronised).  NULL removes the bias (synchronises `stream` first;
+ * for fc1 / fc3 with separate projections it zeroes that half). */
 qmoe_status qmoe_set_bias(qmoe_layer* layer, int fc, const float* bias_dev, void* stream);
 
 /* Experts with more than `min_rows` routed rows take the tensor-core grouped
@@ -157,13 +164,16 @@ qmoe_status qmoe_set_gemm_min_rows(qmoe_layer* layer, int min_rows);
 qmoe_status qmoe_reserve(qmoe_layer* layer, int64_t max_tokens);
 
 /*
- * Copy one projection's weights (fc = 1 or 2) from the canonical layout into
- * the layer's own GB300 layouts, on `stream`.
+ * Copy one projection's weights (fc = 1, 2, or 3 with QMOE_FC1_SEPARATE_FC3)
+ * from the canonical layout into the layer's own GB300 layouts, on `stream`.
  *   codes_dev        uint8 [E, N, K*bits/8]
  *   scales_dev       D     [E, N, K/B]
  *   zero_points_dev  uint8 [E, N, ceil((K/B)*bits/8)], non-NULL iff
  *                    zp_mode == QMOE_ZP_UINT8 (else must be NULL)
- * May be called again to replace the weights.  Allocates device memory.
+ * with N = 2*inter (fc1), hidden (fc2), or inter (fc1 and fc3 with separate
+ * projections; fc3 uses fc1's code width).  With separate projections the
+ * fc1 layouts are built once both fc = 1 and fc = 3 have been given.  May be
+ * called again to replace the weights.  Allocates device memory.
  */
 qmoe_status qmoe_prepack(qmoe_layer* layer, int fc, const uint8_t* codes_dev,
                          const void* scales_dev, const uint8_t* zero_points_dev,

@@ -260,10 +260,12 @@ def to_f64(t) -> np.ndarray:
 
 
 def expert_weights(inputs: dict, fc: int, e: int) -> np.ndarray:
-    """Dense dequantised weights of expert e for fc1 ([2I, H]) or fc2 ([H, I])."""
+    """Dense dequantised weights of expert e for fc1 ([2I, H], or [I, H] of
+    gate rows beside a separate fc3), fc2 ([H, I]) or fc3 ([I, H] up rows;
+    fc1's code width, zero points and block size)."""
     cfg = inputs["cfg"]
-    bits, K = (cfg.bits1, cfg.H) if fc == 1 else (cfg.bits2, cfg.I)
-    pre = "fc1_" if fc == 1 else "fc2_"
+    bits, K = (cfg.bits2, cfg.I) if fc == 2 else (cfg.bits1, cfg.H)
+    pre = f"fc{fc}_"
     zp = inputs[pre + "zp"]
     return dequantize(
         np.asarray(inputs[pre + "codes"][e]), to_f64(inputs[pre + "scales"][e]), bits,
@@ -275,7 +277,7 @@ def projection_bias(inputs: dict, fc: int, e: int):
     """fp32 bias row of expert e added to the projection output (qmoe.rs
     ``qmoe_linear_impl``: ``output = value + bias[expert * out + feature]``),
     or 0 without biases."""
-    b = inputs.get("fc1_bias" if fc == 1 else "fc2_bias")
+    b = inputs.get(f"fc{fc}_bias")
     return 0.0 if b is None else to_f64(b[e])
 
 
@@ -313,7 +315,12 @@ def forward(inputs: dict, tokens=None, round_h: bool = False, return_parts: bool
         rows = need[e]
         xe = x[[t for t, _ in rows]]                       # [M_e, H]
         a = xe @ expert_weights(inputs, 1, e).T + projection_bias(inputs, 1, e)   # [M_e, 2I]
-        h = glu(a, cfg.I, cfg.act, cfg.fc1_layout, cfg.swiglu_alpha, cfg.swiglu_beta, cfg.swiglu_limit)
+        layout = cfg.fc1_layout
+        if layout == "separate":
+            # qmoe.rs qmoe_activate with fc3: gate = fc1's output, linear = fc3's
+            a3 = xe @ expert_weights(inputs, 3, e).T + projection_bias(inputs, 3, e)   # [M_e, I]
+            a, layout = np.concatenate([a, a3], axis=1), "concat"
+        h = glu(a, cfg.I, cfg.act, layout, cfg.swiglu_alpha, cfg.swiglu_beta, cfg.swiglu_limit)
         if round_h:
             h = round_to_dtype(h, cfg.dtype)
         ye = h @ expert_weights(inputs, 2, e).T + projection_bias(inputs, 2, e)  # [M_e, H]

@@ -26,7 +26,9 @@ and ``decode_affine_weight``):
   K/B per-block zero points, at the weight bit width (only in ``uint8`` mode).
 
 fc1 rows are ``[gate (I rows) | up (I rows)]`` (concatenated gate/up), or
-interleaved (row 2f = gate f, row 2f+1 = up f) when ``fc1_layout`` says so.
+interleaved (row 2f = gate f, row 2f+1 = up f) when ``fc1_layout`` says so,
+or, with ``fc1_layout == "separate"``, fc1 holds the I gate rows and a third
+projection fc3 (keys ``fc3_*``, drawn after every other tensor) the I up rows.
 Optional projection biases are float32 ``[E, N]`` in the same row order.
 """
 from __future__ import annotations
@@ -65,8 +67,9 @@ class QMoEConfig:
     zp_hi: int = 0
     logit_sigma: float = 1.0
     zipf_bias: float = 0.0  # logits[t, e] += zipf_bias * log(1 / (e + 1))
-    # fc1 row order: "concat" ([gate (I rows) | up (I rows)]) or "interleaved"
-    # (row 2f = gate f, row 2f+1 = up f)
+    # fc1 row order: "concat" ([gate (I rows) | up (I rows)]), "interleaved"
+    # (row 2f = gate f, row 2f+1 = up f) or "separate" (fc1 = gate rows, a
+    # third projection fc3 = up rows)
     fc1_layout: str = "concat"
     # SwiGLU attributes: h = min(g, L) * sigmoid(alpha * min(g, L)) * (clamp(u, -L, L) + beta)
     swiglu_alpha: float = 1.0
@@ -164,19 +167,28 @@ def make_inputs(cfg: QMoEConfig, T: Optional[int] = None) -> dict:
         bias = (cfg.zipf_bias * np.log(1.0 / (np.arange(cfg.E) + 1.0))).astype(np.float32)
         logits = (logits + bias[None, :]).astype(np.float32)
     x = _cast(rng.standard_normal((T, cfg.H), dtype=np.float32), cfg.dtype)
-    fc1 = _projection(rng, cfg, 2 * cfg.I, cfg.H, cfg.bits1)
+    # a separate fc3 holds the up rows: fc1 then has only the I gate rows
+    sep = cfg.fc1_layout == "separate"
+    n1 = cfg.I if sep else 2 * cfg.I
+    fc1 = _projection(rng, cfg, n1, cfg.H, cfg.bits1)
     fc2 = _projection(rng, cfg, cfg.H, cfg.I, cfg.bits2)
-    b1 = b2 = None
+    b1 = b2 = b3 = None
     if cfg.bias:   # drawn after everything else: the other streams do not move
-        b1 = torch.from_numpy((rng.standard_normal((cfg.E, 2 * cfg.I)) * cfg.bias_sigma).astype(np.float32))
+        b1 = torch.from_numpy((rng.standard_normal((cfg.E, n1)) * cfg.bias_sigma).astype(np.float32))
         b2 = torch.from_numpy((rng.standard_normal((cfg.E, cfg.H)) * cfg.bias_sigma).astype(np.float32))
+    fc3 = (None, None, None)
+    if sep:        # after that, fc3 (codes, scales, zero points, bias)
+        fc3 = _projection(rng, cfg, cfg.I, cfg.H, cfg.bits1)
+        if cfg.bias:
+            b3 = torch.from_numpy((rng.standard_normal((cfg.E, cfg.I)) * cfg.bias_sigma).astype(np.float32))
     return {
         "cfg": cfg.with_(T=T),
         "logits": torch.from_numpy(np.ascontiguousarray(logits)),
         "x": x,
         "fc1_codes": fc1[0], "fc1_scales": fc1[1], "fc1_zp": fc1[2],
         "fc2_codes": fc2[0], "fc2_scales": fc2[1], "fc2_zp": fc2[2],
-        "fc1_bias": b1, "fc2_bias": b2,
+        "fc3_codes": fc3[0], "fc3_scales": fc3[1], "fc3_zp": fc3[2],
+        "fc1_bias": b1, "fc2_bias": b2, "fc3_bias": b3,
     }
 
 

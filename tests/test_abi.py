@@ -74,7 +74,8 @@ def test_prepack_and_forward_state_checks(lib):
     st, h = _create(zp_mode=b.QMOE_ZP_UINT8)
     # zero points required in uint8 mode; checked before any device call
     assert b.qmoe_prepack(h, 1, 16, 16, 0, 0) == b.QMOE_ERR_INVALID_ARG
-    assert b.qmoe_prepack(h, 3, 16, 16, 16, 0) == b.QMOE_ERR_INVALID_ARG
+    assert b.qmoe_prepack(h, 4, 16, 16, 16, 0) == b.QMOE_ERR_INVALID_ARG
+    assert b.qmoe_prepack(h, 3, 16, 16, 16, 0) == b.QMOE_ERR_STATE       # fc3 needs separate projections
     assert b.qmoe_prepack(h, 1, 0, 16, 16, 0) == b.QMOE_ERR_INVALID_ARG
     # T == 0: no work, OK; T > 0 before prepack: STATE
     assert b.qmoe_forward(h, 16, 16, 16, 0, 0) == b.QMOE_OK
@@ -102,9 +103,15 @@ def test_activation_layout_and_bias_argument_checks(lib):
     assert b.qmoe_set_swiglu_params(h, 1.0, 0.0, -1.0) == b.QMOE_ERR_INVALID_ARG
     assert b.qmoe_set_fc1_layout(h, 1) == b.QMOE_OK
     assert b.qmoe_set_fc1_layout(h, 0) == b.QMOE_OK
-    assert b.qmoe_set_fc1_layout(h, 2) == b.QMOE_ERR_INVALID_ARG
-    assert b.qmoe_set_bias(h, 3, 16, 0) == b.QMOE_ERR_INVALID_ARG
+    assert b.qmoe_set_fc1_layout(h, 3) == b.QMOE_ERR_INVALID_ARG
+    assert b.qmoe_set_fc1_layout(h, -1) == b.QMOE_ERR_INVALID_ARG
+    assert b.qmoe_set_bias(h, 4, 16, 0) == b.QMOE_ERR_INVALID_ARG
+    # fc3 exists only beside a separate-gate fc1 (checked before any device call)
+    assert b.qmoe_set_bias(h, 3, 16, 0) == b.QMOE_ERR_STATE
+    assert b.qmoe_prepack(h, 3, 16, 16, None, None) == b.QMOE_ERR_STATE
     assert b.qmoe_set_bias(h, 1, 0, 0) == b.QMOE_OK                       # removing none is fine
+    assert b.qmoe_set_fc1_layout(h, b.QMOE_FC1_SEPARATE_FC3) == b.QMOE_OK
+    assert b.qmoe_set_bias(h, 3, 0, 0) == b.QMOE_OK                       # removing none is fine
     b.qmoe_destroy(h)
 
 

@@ -121,9 +121,10 @@ VARIANTS = {
 }
 
 
-# qmoe.rs swiglu_fusion 1 (interleaved gate/up), SwiGLU alpha / beta / limit
-# (the limit clamps many gates and up values at these sizes) and fp32 biases,
-# on both projection paths and the fp32 SIMT path.
+# qmoe.rs swiglu_fusion 1 (interleaved gate/up), the separate fc3 up
+# projection, SwiGLU alpha / beta / limit (the limit clamps many gates and up
+# values at these sizes) and fp32 biases, on both projection paths and the
+# fp32 SIMT path.
 FEATURE_VARIANTS = {
     "interleaved_bias_swiglu_params": dict(fc1_layout="interleaved", bias=True, swiglu_alpha=1.702,
                                            swiglu_beta=1.0, swiglu_limit=0.3, T=13),
@@ -135,6 +136,14 @@ FEATURE_VARIANTS = {
                                         swiglu_alpha=1.702, swiglu_beta=1.0, swiglu_limit=0.3, T=7),
     # a long fc2 reduction (K = 1024) with biases
     "bias_long_fc2_k": dict(bias=True, I=1024, E=4, T=6),
+    # qmoe.rs unfused SwiGLU: gate rows in fc1, up rows in a separate fc3
+    "separate_fc3_bias_swiglu_params": dict(fc1_layout="separate", bias=True, swiglu_alpha=1.702,
+                                            swiglu_beta=1.0, swiglu_limit=0.3, T=13),
+    "separate_fc3_geglu_int2_offset_f16": dict(fc1_layout="separate", act="geglu", bias=True, bits1=2,
+                                               bits2=2, zp_mode="offset", zp_offset=1.5, dtype="f16",
+                                               B=128, T=9),
+    "separate_fc3_uint8_T150": dict(fc1_layout="separate", zp_mode="uint8", zp_lo=5, zp_hi=11, E=4, T=150),
+    "f32_separate_fc3_bias": dict(dtype="f32", fc1_layout="separate", bias=True, T=7),
 }
 
 

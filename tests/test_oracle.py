@@ -262,8 +262,10 @@ def _brute_layer(inp):
     logits = inp["logits"].tolist()
 
     def weight(fc, e, n, d):
-        bits, K = (cfg.bits1, cfg.H) if fc == 1 else (cfg.bits2, cfg.I)
-        pre = "fc1_" if fc == 1 else "fc2_"
+        bits, K = (cfg.bits2, cfg.I) if fc == 2 else (cfg.bits1, cfg.H)
+        pre = f"fc{fc}_"
+        if fc == 1 and cfg.fc1_layout == "separate" and n >= cfg.I:
+            pre, n = "fc3_", n - cfg.I     # the up rows live in fc3
         row = bytes(inp[pre + "codes"][e, n].numpy())
         q = (int.from_bytes(row, "little") >> (d * bits)) & ((1 << bits) - 1)
         blk = d // cfg.B
@@ -291,6 +293,9 @@ def _brute_layer(inp):
                 W1[e] = [[weight(1, e, n, d) for d in range(cfg.H)] for n in range(2 * cfg.I)]
                 W2[e] = [[weight(2, e, n, d) for d in range(cfg.I)] for n in range(cfg.H)]
             b1 = inp["fc1_bias"][e].tolist() if inp.get("fc1_bias") is not None else [0.0] * (2 * cfg.I)
+            if cfg.fc1_layout == "separate":
+                b3 = inp["fc3_bias"][e].tolist() if inp.get("fc3_bias") is not None else [0.0] * cfg.I
+                b1 = (b1 if inp.get("fc1_bias") is not None else [0.0] * cfg.I) + b3
             b2 = inp["fc2_bias"][e].tolist() if inp.get("fc2_bias") is not None else [0.0] * cfg.H
             a = [sum(W1[e][n][d] * x[t][d] for d in range(cfg.H)) + b1[n] for n in range(2 * cfg.I)]
             h = []
@@ -330,6 +335,9 @@ SMALL_VARIANTS = {
     # 8-bit codes with byte zero points away from the centre
     "int8_uint8_f16": dict(bits1=8, bits2=8, zp_mode="uint8", zp_lo=100, zp_hi=150, dtype="f16",
                            H=64, I=64, scale_lo=0.0005, scale_hi=0.002),
+    # qmoe.rs unfused SwiGLU: gate rows in fc1, up rows in a separate fc3
+    "separate_fc3_bias_uint8": dict(fc1_layout="separate", bias=True, zp_mode="uint8", zp_lo=6, zp_hi=9,
+                                    dtype="bf16", H=64, I=64, E=4, k=2),
 }
 
 
@@ -422,6 +430,17 @@ def _variant_pin_fails(monkeypatch, variant, name, fake):
     inp = make_inputs(cfg)
     ulp = {"f32": 2.0 ** -23, "f16": 2.0 ** -10, "bf16": 2.0 ** -7}[cfg.dtype]
     return not np.allclose(O.forward(inp), _brute_layer(inp), rtol=ulp, atol=1e-30)
+
+
+def test_planted_swapped_fc1_fc3_is_caught(monkeypatch):
+    # gate from fc3 and up from fc1 instead of the other way round
+    cfg = CONFIGS["tiny"].with_(fc1_layout="separate", H=64, I=64)
+    inp = make_inputs(cfg)
+    ref = _brute_layer(inp)
+    swapped = dict(inp)
+    for part in ("codes", "scales", "zp", "bias"):
+        swapped["fc1_" + part], swapped["fc3_" + part] = inp["fc3_" + part], inp["fc1_" + part]
+    assert np.abs(O.forward(swapped) - ref).max() > 1e-3
 
 
 def test_planted_dropped_bias_is_caught(monkeypatch):

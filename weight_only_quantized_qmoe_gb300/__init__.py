@@ -62,8 +62,8 @@ class QMoELayer:
         layer = cls(cfg.H, cfg.I, cfg.E, cfg.k, cfg.bits1, cfg.bits2, cfg.B, cfg.zp_mode,
                     cfg.act, cfg.dtype, cfg.normalize,
                     cfg.zp_offset if cfg.zp_mode == "offset" else None)
-        if getattr(cfg, "fc1_layout", "concat") == "interleaved":
-            layer.set_fc1_layout(True)
+        if getattr(cfg, "fc1_layout", "concat") != "concat":
+            layer.set_fc1_layout(cfg.fc1_layout)
         if (getattr(cfg, "swiglu_alpha", 1.0), getattr(cfg, "swiglu_beta", 0.0),
                 getattr(cfg, "swiglu_limit", float("inf"))) != (1.0, 0.0, float("inf")):
             layer.set_swiglu_params(cfg.swiglu_alpha, cfg.swiglu_beta, cfg.swiglu_limit)
@@ -72,11 +72,17 @@ class QMoELayer:
     def set_swiglu_params(self, alpha, beta, limit):
         self._check(binding.qmoe_set_swiglu_params(self.handle, alpha, beta, limit))
 
-    def set_fc1_layout(self, interleaved):
-        self._check(binding.qmoe_set_fc1_layout(self.handle, 1 if interleaved else 0))
+    def set_fc1_layout(self, layout):
+        """"concat" | "interleaved" | "separate" (fc1 = gate rows, fc3 = up
+        rows), or True / False for interleaved / concatenated."""
+        codes = {"concat": binding.QMOE_FC1_CONCAT, "interleaved": binding.QMOE_FC1_INTERLEAVED,
+                 "separate": binding.QMOE_FC1_SEPARATE_FC3, True: binding.QMOE_FC1_INTERLEAVED,
+                 False: binding.QMOE_FC1_CONCAT}
+        self._check(binding.qmoe_set_fc1_layout(self.handle, codes.get(layout, layout)))
 
     def set_bias(self, fc, bias, stream=None):
-        """fp32 [E, N] device tensor, or None to remove."""
+        """fp32 [E, N] device tensor (fc 1, 2, or 3 beside a separate fc1), or
+        None to remove."""
         self._check(binding.qmoe_set_bias(self.handle, fc, _ptr(bias), _stream(stream)))
 
     def _check(self, st):
@@ -161,8 +167,10 @@ class QMoELayer:
 def load_inputs(layer: QMoELayer, inp: dict, device="cuda"):
     """Move one workload (qmoe_inputs.make_inputs) to the device and prepack
     it.  Returns (x, logits) device tensors."""
-    for fc in (1, 2):
+    for fc in (1, 2, 3):
         pre = f"fc{fc}_"
+        if inp.get(pre + "codes") is None:
+            continue      # fc3 only beside a separate-gate fc1
         codes = inp[pre + "codes"].to(device)
         scales = inp[pre + "scales"].to(device)
         zp = inp[pre + "zp"]

@@ -21,6 +21,7 @@ QMOE_OK, QMOE_ERR_INVALID_ARG, QMOE_ERR_UNSUPPORTED, QMOE_ERR_CUDA = 0, 1, 2, 3
 QMOE_ERR_OOM, QMOE_ERR_STATE, QMOE_ERR_TIMEOUT = 4, 5, 6
 QMOE_ZP_SYMMETRIC, QMOE_ZP_UINT8, QMOE_ZP_OFFSET = 0, 1, 2
 QMOE_ACT_SWIGLU, QMOE_ACT_GEGLU_TANH = 0, 1
+QMOE_FC1_CONCAT, QMOE_FC1_INTERLEAVED, QMOE_FC1_SEPARATE_FC3 = 0, 1, 2
 QMOE_F32, QMOE_F16, QMOE_BF16 = 0, 1, 2
 QMOE_TRACE_NUM_EVENTS = 5
 
@@ -105,8 +106,8 @@ def qmoe_set_swiglu_params(layer, alpha, beta, limit):
     return load().qmoe_set_swiglu_params(layer, float(alpha), float(beta), float(limit))
 
 
-def qmoe_set_fc1_layout(layer, interleaved):
-    return load().qmoe_set_fc1_layout(layer, int(interleaved))
+def qmoe_set_fc1_layout(layer, layout):
+    return load().qmoe_set_fc1_layout(layer, int(layout))
 
 
 def qmoe_set_bias(layer, fc, bias_dev, stream=None):

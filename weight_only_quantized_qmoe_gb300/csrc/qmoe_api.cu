@@ -51,6 +51,8 @@ struct qmoe_layer {
   // SwiGLU attributes (qmoe.rs swiglu_value defaults: alpha 1, beta 0, no limit)
   float sw_alpha = 1.f, sw_beta = 0.f, sw_limit = INFINITY;
   int fc1_interleaved = 0;                 // fc1 canonical rows: [gate | up] or (gate, up) pairs
+  int fc1_separate = 0;                    // gate rows from fc1, up rows from a separate fc3
+  bool fc1_half[2] = {false, false};       // separate: gate / up halves copied in
   float* bias[2] = {nullptr, nullptr};     // fc1: [E, I, 2] (gate, up) pairs ; fc2: [E, H]
   int normalize = 1;
   float zp_offset = NAN;
@@ -156,6 +158,19 @@ cudaError_t launch_pair_bias(const float* src, float* dst, int E, int I, int int
   const size_t n = (size_t)E * I;
   const int grid = (int)std::min<size_t>((n + 255) / 256, 4096);
   pair_bias_kernel<<<grid, 256, 0, s>>>(src, dst, E, I, interleaved);
+  return cudaGetLastError();
+}
+
+// Separate fc1 / fc3 bias [E, I] -> one half of the (gate, up) pairs; NULL
+// source zeroes the half.
+__global__ void half_bias_kernel(const float* __restrict__ src, float* __restrict__ dst, size_t n, int half) {
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x)
+    dst[2 * i + half] = src ? src[i] : 0.f;
+}
+
+cudaError_t launch_half_bias(const float* src, float* dst, size_t n, int half, cudaStream_t s) {
+  const int grid = (int)std::min<size_t>((n + 255) / 256, 4096);
+  half_bias_kernel<<<grid, 256, 0, s>>>(src, dst, n, half);
   return cudaGetLastError();
 }
 
@@ -337,17 +352,35 @@ qmoe_status qmoe_set_swiglu_params(qmoe_layer* l, float alpha, float beta, float
   return QMOE_OK;
 }
 
-qmoe_status qmoe_set_fc1_layout(qmoe_layer* l, int interleaved) {
-  if (!l || (interleaved != 0 && interleaved != 1)) return QMOE_ERR_INVALID_ARG;
-  if (l->proj[0].ready || l->bias[0])
-    return fail(l, QMOE_ERR_STATE, "set the fc1 layout before qmoe_prepack(fc=1) and qmoe_set_bias(fc=1)");
-  l->fc1_interleaved = interleaved;
+qmoe_status qmoe_set_fc1_layout(qmoe_layer* l, int layout) {
+  if (!l || layout < QMOE_FC1_CONCAT || layout > QMOE_FC1_SEPARATE_FC3) return QMOE_ERR_INVALID_ARG;
+  if (l->proj[0].ready || l->bias[0] || l->fc1_half[0] || l->fc1_half[1])
+    return fail(l, QMOE_ERR_STATE,
+                "set the fc1 layout before qmoe_prepack(fc=1/3) and qmoe_set_bias(fc=1/3)");
+  // Separate projections are assembled into the concatenated order.
+  l->fc1_interleaved = layout == QMOE_FC1_INTERLEAVED ? 1 : 0;
+  l->fc1_separate = layout == QMOE_FC1_SEPARATE_FC3 ? 1 : 0;
   return QMOE_OK;
 }
 
 qmoe_status qmoe_set_bias(qmoe_layer* l, int fc, const float* bias, void* stream) {
   if (!l) return QMOE_ERR_INVALID_ARG;
-  if (fc != 1 && fc != 2) return fail(l, QMOE_ERR_INVALID_ARG, "fc must be 1 or 2");
+  if (fc != 1 && fc != 2 && fc != 3) return fail(l, QMOE_ERR_INVALID_ARG, "fc must be 1, 2 or 3");
+  if (fc == 3 && !l->fc1_separate)
+    return fail(l, QMOE_ERR_STATE, "fc=3 needs qmoe_set_fc1_layout(QMOE_FC1_SEPARATE_FC3)");
+  if (l->fc1_separate && fc != 2) {
+    // one half of the (gate, up) pairs: fc1 = gate, fc3 = up
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    float*& dst = l->bias[0];
+    const size_t n = (size_t)l->E * l->I;
+    if (!dst) {
+      if (!bias) return QMOE_OK;
+      QMOE_CUDA(l, dalloc(&dst, 2 * n * sizeof(float)), "allocate bias");
+      QMOE_CUDA(l, cudaMemsetAsync(dst, 0, 2 * n * sizeof(float), s), "clear bias");
+    }
+    QMOE_CUDA(l, launch_half_bias(bias, dst, n, fc == 1 ? 0 : 1, s), "re-lay fc1/fc3 bias");
+    return QMOE_OK;
+  }
   float*& dst = l->bias[fc - 1];
   if (!bias) {
     if (dst) {
@@ -395,7 +428,13 @@ qmoe_status qmoe_reserve(qmoe_layer* l, int64_t max_tokens) {
 qmoe_status qmoe_prepack(qmoe_layer* l, int fc, const uint8_t* codes, const void* scales,
                          const uint8_t* zero_points, void* stream) {
   if (!l) return QMOE_ERR_INVALID_ARG;
-  if (fc != 1 && fc != 2) return fail(l, QMOE_ERR_INVALID_ARG, "fc must be 1 or 2");
+  if (fc != 1 && fc != 2 && fc != 3) return fail(l, QMOE_ERR_INVALID_ARG, "fc must be 1, 2 or 3");
+  if (fc == 3 && !l->fc1_separate)
+    return fail(l, QMOE_ERR_STATE, "fc=3 needs qmoe_set_fc1_layout(QMOE_FC1_SEPARATE_FC3)");
+  // With separate projections, fc1 (gate) and fc3 (up) each fill half of
+  // fc1's rows, assembled here in the concatenated order.
+  const int half = l->fc1_separate && fc != 2 ? (fc == 1 ? 0 : 1) : -1;
+  if (fc == 3) fc = 1;
   if (!codes || !scales) return fail(l, QMOE_ERR_INVALID_ARG, "codes and scales are required");
   if ((zero_points != nullptr) != (l->zp_mode == QMOE_ZP_UINT8))
     return fail(l, QMOE_ERR_INVALID_ARG, "zero_points must be given iff zp_mode == QMOE_ZP_UINT8");
@@ -432,10 +471,27 @@ qmoe_status qmoe_prepack(qmoe_layer* l, int fc, const uint8_t* codes, const void
     if (zp_bytes) QMOE_CUDA(l, dalloc(&p.zp, zp_bytes), "allocate zero points");
     p.zp_bytes = zp_bytes;
   }
-  QMOE_CUDA(l, cudaMemcpyAsync(p.codes, codes, codes_bytes, cudaMemcpyDeviceToDevice, s), "copy codes");
-  QMOE_CUDA(l, cudaMemcpyAsync(p.scales, scales, scales_bytes, cudaMemcpyDeviceToDevice, s), "copy scales");
-  if (zp_bytes)
-    QMOE_CUDA(l, cudaMemcpyAsync(p.zp, zero_points, zp_bytes, cudaMemcpyDeviceToDevice, s), "copy zp");
+  if (half < 0) {
+    QMOE_CUDA(l, cudaMemcpyAsync(p.codes, codes, codes_bytes, cudaMemcpyDeviceToDevice, s), "copy codes");
+    QMOE_CUDA(l, cudaMemcpyAsync(p.scales, scales, scales_bytes, cudaMemcpyDeviceToDevice, s), "copy scales");
+    if (zp_bytes)
+      QMOE_CUDA(l, cudaMemcpyAsync(p.zp, zero_points, zp_bytes, cudaMemcpyDeviceToDevice, s), "copy zp");
+  } else {
+    // per expert: the caller's I rows -> rows [half*I, half*I + I) of the 2I
+    auto copy_half = [&](void* dst, const void* src, size_t total_bytes) {
+      const size_t blk = total_bytes / (2 * E);   // bytes of I rows
+      return cudaMemcpy2DAsync(static_cast<uint8_t*>(dst) + half * blk, 2 * blk, src, blk, blk, E,
+                               cudaMemcpyDeviceToDevice, s);
+    };
+    QMOE_CUDA(l, copy_half(p.codes, codes, codes_bytes), "copy codes");
+    QMOE_CUDA(l, copy_half(p.scales, scales, scales_bytes), "copy scales");
+    if (zp_bytes) QMOE_CUDA(l, copy_half(p.zp, zero_points, zp_bytes), "copy zp");
+    l->fc1_half[half] = true;
+    if (!(l->fc1_half[0] && l->fc1_half[1])) {
+      p.ready = false;   // the layouts are built once both halves are in
+      return QMOE_OK;
+    }
+  }
   if (l->dtype != QMOE_F32) {
     p.L = make_decode_layout(p.bits, l->B, fc == 1 ? l->I : l->H, p.K, fc == 1 ? 2 : 1, l->zp_mode,
                              l->dsize);
