@@ -76,7 +76,18 @@ typedef enum {
 } qmoe_status;
 
 enum { QMOE_ZP_SYMMETRIC = 0, QMOE_ZP_UINT8 = 1, QMOE_ZP_OFFSET = 2 };
-enum { QMOE_ACT_SWIGLU = 0, QMOE_ACT_GEGLU_TANH = 1 };
+/* Gated activations (fc1 has 2*inter rows: gate and up) and the non-gated
+ * ones of [qmoe.rs qmoe_activate] (fc1 has inter rows, h = act(fc1 output)):
+ * relu max(v, 0); gelu the tanh form 0.5 v (1 + tanh(0.79788456 (v + 0.044715 v^3)));
+ * silu v * sigmoid(v); identity v. */
+enum {
+  QMOE_ACT_SWIGLU = 0,
+  QMOE_ACT_GEGLU_TANH = 1,
+  QMOE_ACT_RELU = 2,
+  QMOE_ACT_GELU_TANH = 3,
+  QMOE_ACT_SILU = 4,
+  QMOE_ACT_IDENTITY = 5
+};
 enum { QMOE_F32 = 0, QMOE_F16 = 1, QMOE_BF16 = 2 };
 
 /* Stage boundaries recorded by qmoe_set_trace_events (see there). */
@@ -100,7 +111,9 @@ enum {
  *   zp_mode         QMOE_ZP_SYMMETRIC (zp = 2^(bits-1)), QMOE_ZP_UINT8
  *                   (packed zero-point tensors), QMOE_ZP_OFFSET (one
  *                   fractional centre, set by qmoe_set_zero_point_offset)
- *   activation      QMOE_ACT_SWIGLU or QMOE_ACT_GEGLU_TANH
+ *   activation      QMOE_ACT_SWIGLU or QMOE_ACT_GEGLU_TANH (gated: fc1 has
+ *                   2*inter rows), or QMOE_ACT_RELU / _GELU_TANH / _SILU /
+ *                   _IDENTITY (non-gated: fc1 has inter rows)
  *   dtype           activation / scale / output type
  * Routing renormalisation defaults to on (qmoe_set_routing).
  * Returns INVALID_ARG for out-of-range values, UNSUPPORTED (with a
@@ -137,13 +150,15 @@ qmoe_status qmoe_set_swiglu_params(qmoe_layer* layer, float alpha, float beta, f
  * third projection fc3 the I up rows (qmoe_activate with fc3: gate = fc1,
  * linear = fc3), each [E, I, ...] and prepacked / biased with fc = 1 and
  * fc = 3.  Other values: INVALID_ARG.  Must precede qmoe_prepack(fc = 1 or 3)
- * and qmoe_set_bias(fc = 1 or 3); STATE otherwise. */
+ * and qmoe_set_bias(fc = 1 or 3); STATE otherwise.  With a non-gated
+ * activation only QMOE_FC1_CONCAT applies (INVALID_ARG otherwise). */
 enum { QMOE_FC1_CONCAT = 0, QMOE_FC1_INTERLEAVED = 1, QMOE_FC1_SEPARATE_FC3 = 2 };
 qmoe_status qmoe_set_fc1_layout(qmoe_layer* layer, int layout);
 
 /* Projection biases [qmoe.rs qmoe_linear_impl: output = sum + bias[e*N + n]]:
  * bias_dev is a float32 device array [E, N] (fc1: N = 2*inter in the fc1 row
- * order, or inter with QMOE_FC1_SEPARATE_FC3; fc2: N = hidden; fc3: N = inter,
+ * order, or inter with QMOE_FC1_SEPARATE_FC3 or a non-gated activation;
+ * fc2: N = hidden; fc3: N = inter,
  * only with QMOE_FC1_SEPARATE_FC3), added to the projection output (fc1 and
  * fc3 before the gated activation, fc2 before the weighted combine).  The
  * layer keeps its own copy (the caller may free bias_dev once `stream` has
@@ -170,8 +185,8 @@ qmoe_status qmoe_reserve(qmoe_layer* layer, int64_t max_tokens);
  *   scales_dev       D     [E, N, K/B]
  *   zero_points_dev  uint8 [E, N, ceil((K/B)*bits/8)], non-NULL iff
  *                    zp_mode == QMOE_ZP_UINT8 (else must be NULL)
- * with N = 2*inter (fc1), hidden (fc2), or inter (fc1 and fc3 with separate
- * projections; fc3 uses fc1's code width).  With separate projections the
+ * with N = 2*inter (fc1, gated activation), inter (fc1, non-gated; fc1 and
+ * fc3 with separate projections; fc3 uses fc1's code width) or hidden (fc2).  With separate projections the
  * fc1 layouts are built once both fc = 1 and fc = 3 have been given.  May be
  * called again to replace the weights.  Allocates device memory.
  */

@@ -229,6 +229,25 @@ def swiglu(g, u, alpha: float = 1.0, beta: float = 0.0, limit: float = float("in
     return g / (1.0 + np.exp(-alpha * g)) * (u + beta)
 
 
+GATED = ("swiglu", "geglu")
+
+
+def act_single(a, act: str):
+    """Non-gated activation of fc1's output (qmoe.rs ``qmoe_activate``,
+    activation 0 / 1 / 2 without fc3 / 4): relu, tanh-GELU (evaluated in
+    double there too), silu v * sigmoid(v), identity."""
+    a = np.asarray(a, dtype=np.float64)
+    if act == "relu":
+        return np.maximum(a, 0.0)
+    if act == "gelu":
+        return gelu_tanh(a)
+    if act == "silu":
+        return silu(a)
+    if act == "identity":
+        return a
+    raise ValueError(act)
+
+
 def split_gate_up(a, inter: int, layout: str = "concat"):
     """Gate and up halves of fc1's output (qmoe.rs ``qmoe_activate``):
     swiglu_fusion == 2 concatenates them (gate = a[:, :I], up = a[:, I:]),
@@ -260,9 +279,9 @@ def to_f64(t) -> np.ndarray:
 
 
 def expert_weights(inputs: dict, fc: int, e: int) -> np.ndarray:
-    """Dense dequantised weights of expert e for fc1 ([2I, H], or [I, H] of
-    gate rows beside a separate fc3), fc2 ([H, I]) or fc3 ([I, H] up rows;
-    fc1's code width, zero points and block size)."""
+    """Dense dequantised weights of expert e for fc1 ([2I, H]; [I, H] for a
+    non-gated activation or of gate rows beside a separate fc3), fc2 ([H, I])
+    or fc3 ([I, H] up rows; fc1's code width, zero points and block size)."""
     cfg = inputs["cfg"]
     bits, K = (cfg.bits2, cfg.I) if fc == 2 else (cfg.bits1, cfg.H)
     pre = f"fc{fc}_"
@@ -314,13 +333,16 @@ def forward(inputs: dict, tokens=None, round_h: bool = False, return_parts: bool
     for e in sorted(need):
         rows = need[e]
         xe = x[[t for t, _ in rows]]                       # [M_e, H]
-        a = xe @ expert_weights(inputs, 1, e).T + projection_bias(inputs, 1, e)   # [M_e, 2I]
+        a = xe @ expert_weights(inputs, 1, e).T + projection_bias(inputs, 1, e)   # [M_e, 2I] (I non-gated)
         layout = cfg.fc1_layout
         if layout == "separate":
             # qmoe.rs qmoe_activate with fc3: gate = fc1's output, linear = fc3's
             a3 = xe @ expert_weights(inputs, 3, e).T + projection_bias(inputs, 3, e)   # [M_e, I]
             a, layout = np.concatenate([a, a3], axis=1), "concat"
-        h = glu(a, cfg.I, cfg.act, layout, cfg.swiglu_alpha, cfg.swiglu_beta, cfg.swiglu_limit)
+        if cfg.act in GATED:
+            h = glu(a, cfg.I, cfg.act, layout, cfg.swiglu_alpha, cfg.swiglu_beta, cfg.swiglu_limit)
+        else:
+            h = act_single(a, cfg.act)
         if round_h:
             h = round_to_dtype(h, cfg.dtype)
         ye = h @ expert_weights(inputs, 2, e).T + projection_bias(inputs, 2, e)  # [M_e, H]

@@ -58,7 +58,7 @@ class QMoEConfig:
     B: int                 # quantisation block size along K
     zp_mode: str           # "sym" | "uint8" | "offset"
     dtype: str             # "f32" | "f16" | "bf16" (activations, scales, output)
-    act: str               # "swiglu" | "geglu"
+    act: str               # gated "swiglu" | "geglu", or non-gated "relu" | "gelu" | "silu" | "identity"
     scale_lo: float
     scale_hi: float
     seed: int
@@ -169,7 +169,8 @@ def make_inputs(cfg: QMoEConfig, T: Optional[int] = None) -> dict:
     x = _cast(rng.standard_normal((T, cfg.H), dtype=np.float32), cfg.dtype)
     # a separate fc3 holds the up rows: fc1 then has only the I gate rows
     sep = cfg.fc1_layout == "separate"
-    n1 = cfg.I if sep else 2 * cfg.I
+    gated = cfg.act in ("swiglu", "geglu")
+    n1 = cfg.I if (sep or not gated) else 2 * cfg.I
     fc1 = _projection(rng, cfg, n1, cfg.H, cfg.bits1)
     fc2 = _projection(rng, cfg, cfg.H, cfg.I, cfg.bits2)
     b1 = b2 = b3 = None
@@ -196,7 +197,8 @@ def weight_bytes_per_expert(cfg: QMoEConfig) -> int:
     """Bytes of one expert's packed codes + scales + zero points (both fcs)."""
     esz = torch.tensor([], dtype=DTYPES[cfg.dtype]).element_size()
     total = 0
-    for N, K, bits in ((2 * cfg.I, cfg.H, cfg.bits1), (cfg.H, cfg.I, cfg.bits2)):
+    n1 = 2 * cfg.I if cfg.act in ("swiglu", "geglu") else cfg.I
+    for N, K, bits in ((n1, cfg.H, cfg.bits1), (cfg.H, cfg.I, cfg.bits2)):
         total += N * K * bits // 8 + N * (K // cfg.B) * esz
         if cfg.zp_mode == "uint8":
             total += N * zp_row_bytes(K, cfg.B, bits)
@@ -206,7 +208,8 @@ def weight_bytes_per_expert(cfg: QMoEConfig) -> int:
 def expert_fc_bytes(cfg: QMoEConfig, fc: int) -> int:
     """Bytes of one expert's fc1 (fc=1) or fc2 (fc=2) codes + scales + zp."""
     esz = torch.tensor([], dtype=DTYPES[cfg.dtype]).element_size()
-    N, K, bits = ((2 * cfg.I, cfg.H, cfg.bits1) if fc == 1 else (cfg.H, cfg.I, cfg.bits2))
+    n1 = 2 * cfg.I if cfg.act in ("swiglu", "geglu") else cfg.I
+    N, K, bits = ((n1, cfg.H, cfg.bits1) if fc == 1 else (cfg.H, cfg.I, cfg.bits2))
     total = N * K * bits // 8 + N * (K // cfg.B) * esz
     if cfg.zp_mode == "uint8":
         total += N * zp_row_bytes(K, cfg.B, bits)

@@ -34,6 +34,14 @@ def test_create_validates(lib):
     st, h = _create()
     assert st == b.QMOE_OK and h
     b.qmoe_destroy(h)
+    for act in (b.QMOE_ACT_RELU, b.QMOE_ACT_GELU_TANH, b.QMOE_ACT_SILU, b.QMOE_ACT_IDENTITY):
+        st, h = _create(activation=act)
+        assert st == b.QMOE_OK and h, act
+        # the fc1 row layouts are for gated activations only
+        assert b.qmoe_set_fc1_layout(h, b.QMOE_FC1_INTERLEAVED) == b.QMOE_ERR_INVALID_ARG
+        assert b.qmoe_set_fc1_layout(h, b.QMOE_FC1_SEPARATE_FC3) == b.QMOE_ERR_INVALID_ARG
+        assert b.qmoe_set_fc1_layout(h, b.QMOE_FC1_CONCAT) == b.QMOE_OK
+        b.qmoe_destroy(h)
     for widths in ((8, 8), (8, 2), (3, 8)):
         st, h = _create(bits_fc1=widths[0], bits_fc2=widths[1])
         assert st == b.QMOE_OK and h, widths
@@ -49,7 +57,8 @@ def test_create_validates(lib):
         (dict(inter=96, block_size=64), b.QMOE_ERR_INVALID_ARG),
         (dict(experts=2000, top_k=2), b.QMOE_ERR_UNSUPPORTED),
         (dict(zp_mode=7), b.QMOE_ERR_INVALID_ARG),
-        (dict(activation=3), b.QMOE_ERR_INVALID_ARG),
+        (dict(activation=6), b.QMOE_ERR_INVALID_ARG),
+        (dict(activation=-1), b.QMOE_ERR_INVALID_ARG),
         (dict(dtype=9), b.QMOE_ERR_INVALID_ARG),
     ]:
         st, h = _create(**kw)

@@ -144,6 +144,15 @@ FEATURE_VARIANTS = {
                                                B=128, T=9),
     "separate_fc3_uint8_T150": dict(fc1_layout="separate", zp_mode="uint8", zp_lo=5, zp_hi=11, E=4, T=150),
     "f32_separate_fc3_bias": dict(dtype="f32", fc1_layout="separate", bias=True, T=7),
+    # non-gated activations (qmoe.rs qmoe_activate): fc1 has I rows, h = act(fc1 output)
+    "relu_bias": dict(act="relu", bias=True, T=13),
+    "gelu_uint8_f16_B64": dict(act="gelu", zp_mode="uint8", zp_lo=5, zp_hi=11, dtype="f16", B=64, T=9),
+    "silu_int2_offset_B128": dict(act="silu", bits1=2, bits2=2, zp_mode="offset", zp_offset=1.5, B=128,
+                                  T=20),
+    "identity_int8_f16": dict(act="identity", bits1=8, bits2=8, dtype="f16", T=12, scale_lo=0.0005,
+                              scale_hi=0.002),
+    "relu_T150_prefill_ring": dict(act="relu", bias=True, E=4, T=150),
+    "f32_silu_bias": dict(dtype="f32", act="silu", bias=True, T=7),
 }
 
 

@@ -235,6 +235,18 @@ def test_interleaved_layout_is_a_row_permutation_of_concat():
     np.testing.assert_array_equal(O.forward(inp), O.forward(cat))
 
 
+def test_non_gated_activations_match_torch():
+    # qmoe.rs qmoe_activate: relu, tanh-GELU, silu, identity
+    v = np.linspace(-8, 8, 161)
+    tv = torch.from_numpy(v)
+    np.testing.assert_allclose(O.act_single(v, "relu"), torch.relu(tv).numpy(), rtol=0, atol=0)
+    np.testing.assert_allclose(O.act_single(v, "gelu"),
+                               torch.nn.functional.gelu(tv, approximate="tanh").numpy(), rtol=1e-13, atol=1e-15)
+    np.testing.assert_allclose(O.act_single(v, "silu"), torch.nn.functional.silu(tv).numpy(), rtol=1e-13,
+                               atol=1e-15)
+    np.testing.assert_array_equal(O.act_single(v, "identity"), v)
+
+
 def test_activations_match_torch():
     g = torch.linspace(-12, 12, 2001, dtype=torch.float64)
     np.testing.assert_allclose(O.silu(g.numpy()), torch.nn.functional.silu(g).numpy(), rtol=1e-15, atol=1e-300)
@@ -290,16 +302,25 @@ def _brute_layer(inp):
         acc = [0.0] * cfg.H
         for e in sel:
             if e not in W1:
-                W1[e] = [[weight(1, e, n, d) for d in range(cfg.H)] for n in range(2 * cfg.I)]
+                n1 = 2 * cfg.I if cfg.act in ("swiglu", "geglu") else cfg.I
+                W1[e] = [[weight(1, e, n, d) for d in range(cfg.H)] for n in range(n1)]
                 W2[e] = [[weight(2, e, n, d) for d in range(cfg.I)] for n in range(cfg.H)]
             b1 = inp["fc1_bias"][e].tolist() if inp.get("fc1_bias") is not None else [0.0] * (2 * cfg.I)
             if cfg.fc1_layout == "separate":
                 b3 = inp["fc3_bias"][e].tolist() if inp.get("fc3_bias") is not None else [0.0] * cfg.I
                 b1 = (b1 if inp.get("fc1_bias") is not None else [0.0] * cfg.I) + b3
             b2 = inp["fc2_bias"][e].tolist() if inp.get("fc2_bias") is not None else [0.0] * cfg.H
-            a = [sum(W1[e][n][d] * x[t][d] for d in range(cfg.H)) + b1[n] for n in range(2 * cfg.I)]
+            gated = cfg.act in ("swiglu", "geglu")
+            n1 = 2 * cfg.I if gated else cfg.I
+            a = [sum(W1[e][n][d] * x[t][d] for d in range(cfg.H)) + b1[n] for n in range(n1)]
             h = []
             for n in range(cfg.I):
+                if not gated:
+                    v = a[n]
+                    h.append({"relu": max(v, 0.0), "identity": v, "silu": v / (1 + math.exp(-v)),
+                              "gelu": 0.5 * v * (1 + math.tanh(math.sqrt(2 / math.pi) * (v + 0.044715 * v ** 3)))
+                              }[cfg.act])
+                    continue
                 if cfg.fc1_layout == "interleaved":
                     g, u = a[2 * n], a[2 * n + 1]
                 else:
@@ -335,6 +356,12 @@ SMALL_VARIANTS = {
     # 8-bit codes with byte zero points away from the centre
     "int8_uint8_f16": dict(bits1=8, bits2=8, zp_mode="uint8", zp_lo=100, zp_hi=150, dtype="f16",
                            H=64, I=64, scale_lo=0.0005, scale_hi=0.002),
+    # non-gated activations: fc1 has I rows, h = act(fc1 output)
+    "relu_bias_f16": dict(act="relu", bias=True, dtype="f16", H=64, I=64),
+    "gelu_int3": dict(act="gelu", bits1=3, bits2=4, dtype="bf16", H=64, I=64, E=3, k=2),
+    "silu_uint8": dict(act="silu", zp_mode="uint8", zp_lo=6, zp_hi=9, dtype="f32", H=64, I=64),
+    "identity_offset_int2": dict(act="identity", bits1=2, bits2=2, zp_mode="offset", zp_offset=1.5,
+                                 dtype="f16", H=64, I=64, B=64),
     # qmoe.rs unfused SwiGLU: gate rows in fc1, up rows in a separate fc3
     "separate_fc3_bias_uint8": dict(fc1_layout="separate", bias=True, zp_mode="uint8", zp_lo=6, zp_hi=9,
                                     dtype="bf16", H=64, I=64, E=4, k=2),

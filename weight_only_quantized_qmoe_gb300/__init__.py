@@ -13,7 +13,9 @@ from .binding import *  # noqa: F401,F403  (the C-ABI names)
 _DT = {"f32": binding.QMOE_F32, "f16": binding.QMOE_F16, "bf16": binding.QMOE_BF16}
 _ZP = {"sym": binding.QMOE_ZP_SYMMETRIC, "uint8": binding.QMOE_ZP_UINT8,
        "offset": binding.QMOE_ZP_OFFSET}
-_ACT = {"swiglu": binding.QMOE_ACT_SWIGLU, "geglu": binding.QMOE_ACT_GEGLU_TANH}
+_ACT = {"swiglu": binding.QMOE_ACT_SWIGLU, "geglu": binding.QMOE_ACT_GEGLU_TANH,
+        "relu": binding.QMOE_ACT_RELU, "gelu": binding.QMOE_ACT_GELU_TANH, "silu": binding.QMOE_ACT_SILU,
+        "identity": binding.QMOE_ACT_IDENTITY}
 
 
 class QMoEError(RuntimeError):
@@ -38,7 +40,8 @@ class QMoELayer:
 
     Parameters mirror ``qmoe_create``; string forms are accepted for
     ``zp_mode`` ("sym" | "uint8" | "offset"), ``activation`` ("swiglu" |
-    "geglu") and ``dtype`` ("f32" | "f16" | "bf16").
+    "geglu" gated; "relu" | "gelu" | "silu" | "identity" non-gated) and
+    ``dtype`` ("f32" | "f16" | "bf16").
     """
 
     def __init__(self, hidden, inter, experts, top_k, bits_fc1, bits_fc2, block_size,

@@ -21,6 +21,7 @@ QMOE_OK, QMOE_ERR_INVALID_ARG, QMOE_ERR_UNSUPPORTED, QMOE_ERR_CUDA = 0, 1, 2, 3
 QMOE_ERR_OOM, QMOE_ERR_STATE, QMOE_ERR_TIMEOUT = 4, 5, 6
 QMOE_ZP_SYMMETRIC, QMOE_ZP_UINT8, QMOE_ZP_OFFSET = 0, 1, 2
 QMOE_ACT_SWIGLU, QMOE_ACT_GEGLU_TANH = 0, 1
+QMOE_ACT_RELU, QMOE_ACT_GELU_TANH, QMOE_ACT_SILU, QMOE_ACT_IDENTITY = 2, 3, 4, 5
 QMOE_FC1_CONCAT, QMOE_FC1_INTERLEAVED, QMOE_FC1_SEPARATE_FC3 = 0, 1, 2
 QMOE_F32, QMOE_F16, QMOE_BF16 = 0, 1, 2
 QMOE_TRACE_NUM_EVENTS = 5

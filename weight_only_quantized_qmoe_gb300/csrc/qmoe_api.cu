@@ -293,7 +293,7 @@ qmoe_status qmoe_create(int hidden, int inter, int experts, int top_k, int bits_
   if (block_size != 32 && block_size != 64 && block_size != 128) return QMOE_ERR_UNSUPPORTED;
   if (hidden % block_size || inter % block_size) return QMOE_ERR_INVALID_ARG;
   if (zp_mode < QMOE_ZP_SYMMETRIC || zp_mode > QMOE_ZP_OFFSET) return QMOE_ERR_INVALID_ARG;
-  if (activation != QMOE_ACT_SWIGLU && activation != QMOE_ACT_GEGLU_TANH) return QMOE_ERR_INVALID_ARG;
+  if (activation < QMOE_ACT_SWIGLU || activation > QMOE_ACT_IDENTITY) return QMOE_ERR_INVALID_ARG;
   if (dtype < QMOE_F32 || dtype > QMOE_BF16) return QMOE_ERR_INVALID_ARG;
   if ((long long)hidden * inter > (1LL << 31)) return QMOE_ERR_UNSUPPORTED;
   qmoe_layer* l = new qmoe_layer();
@@ -354,6 +354,8 @@ qmoe_status qmoe_set_swiglu_params(qmoe_layer* l, float alpha, float beta, float
 
 qmoe_status qmoe_set_fc1_layout(qmoe_layer* l, int layout) {
   if (!l || layout < QMOE_FC1_CONCAT || layout > QMOE_FC1_SEPARATE_FC3) return QMOE_ERR_INVALID_ARG;
+  if (layout != QMOE_FC1_CONCAT && !act_gated(l->act))
+    return fail(l, QMOE_ERR_INVALID_ARG, "fc1 row layouts apply to gated activations only");
   if (l->proj[0].ready || l->bias[0] || l->fc1_half[0] || l->fc1_half[1])
     return fail(l, QMOE_ERR_STATE,
                 "set the fc1 layout before qmoe_prepack(fc=1/3) and qmoe_set_bias(fc=1/3)");
@@ -390,10 +392,11 @@ qmoe_status qmoe_set_bias(qmoe_layer* l, int fc, const float* bias, void* stream
     dst = nullptr;
     return QMOE_OK;
   }
-  const size_t n = (size_t)l->E * (fc == 1 ? 2 * l->I : l->H);
+  const bool gated = act_gated(l->act);
+  const size_t n = (size_t)l->E * (fc == 1 ? (gated ? 2 * l->I : l->I) : l->H);
   if (!dst) QMOE_CUDA(l, dalloc(&dst, n * sizeof(float)), "allocate bias");
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (fc == 2)
+  if (fc == 2 || !gated)   // fc2, or a non-gated fc1: rows as given
     QMOE_CUDA(l, cudaMemcpyAsync(dst, bias, n * sizeof(float), cudaMemcpyDeviceToDevice, s), "copy bias");
   else
     QMOE_CUDA(l, launch_pair_bias(bias, dst, l->E, l->I, l->fc1_interleaved, s), "re-lay fc1 bias");
@@ -442,8 +445,12 @@ qmoe_status qmoe_prepack(qmoe_layer* l, int fc, const uint8_t* codes, const void
     return fail(l, QMOE_ERR_STATE, "call qmoe_set_zero_point_offset before qmoe_prepack");
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   Proj& p = l->proj[fc - 1];
+  const bool gated = act_gated(l->act);
+  // fc1 rows: gate and up (gated activations) or one row per feature; the
+  // GEMM and decode layouts treat a non-gated fc1 like fc2 (plain rows)
+  const bool pairs = fc == 1 && gated;
   p.bits = l->bits[fc - 1];
-  p.N = fc == 1 ? 2 * l->I : l->H;
+  p.N = fc == 1 ? (gated ? 2 * l->I : l->I) : l->H;
   p.K = fc == 1 ? l->H : l->I;
   const size_t E = (size_t)l->E;
   const size_t codes_bytes = E * p.N * ((size_t)p.K * p.bits / 8);
@@ -493,7 +500,7 @@ qmoe_status qmoe_prepack(qmoe_layer* l, int fc, const uint8_t* codes, const void
     }
   }
   if (l->dtype != QMOE_F32) {
-    p.L = make_decode_layout(p.bits, l->B, fc == 1 ? l->I : l->H, p.K, fc == 1 ? 2 : 1, l->zp_mode,
+    p.L = make_decode_layout(p.bits, l->B, fc == 1 ? l->I : l->H, p.K, pairs ? 2 : 1, l->zp_mode,
                              l->dsize);
     const size_t dec_bytes = p.L.expert_bytes * E;
     if (p.dec_bytes != dec_bytes) {
@@ -509,12 +516,12 @@ qmoe_status qmoe_prepack(qmoe_layer* l, int fc, const uint8_t* codes, const void
     ra.E = l->E;
     ra.N = p.N;
     ra.K = p.K;
-    ra.I_or_0 = fc == 1 ? l->I : 0;
+    ra.I_or_0 = pairs ? l->I : 0;
     ra.interleaved = l->fc1_interleaved;
     ra.dsize = l->dsize;
     ra.L = p.L;
     QMOE_CUDA(l, launch_repack_decode(ra, s), "repack weights");
-    p.GL = make_gemm_layout(p.bits, l->B, fc, p.N, p.K, l->I, l->zp_mode);
+    p.GL = make_gemm_layout(p.bits, l->B, pairs ? 1 : 2, p.N, p.K, l->I, l->zp_mode);
     const size_t gq_bytes = p.GL.expert_bytes * E;
     if (p.gq_bytes != gq_bytes) {
       if (p.gq) cudaFree(p.gq);
@@ -530,7 +537,7 @@ qmoe_status qmoe_prepack(qmoe_layer* l, int fc, const uint8_t* codes, const void
     ga.N = p.N;
     ga.K = p.K;
     ga.I = l->I;
-    ga.fc = fc;
+    ga.fc = pairs ? 1 : 2;
     ga.interleaved = l->fc1_interleaved;
     ga.L = p.GL;
     QMOE_CUDA(l, launch_repack_gemm(ga, s), "repack weights (GEMM layout)");

@@ -227,7 +227,8 @@ constexpr int kSimtRows = 4;
 
 template <int DT>
 __device__ __forceinline__ float simt_weight(const SimtArgs& a, int e, int row, int d) {
-  const int N = a.fc == 1 ? 2 * a.I_or_0 : a.N_out;
+  // canonical rows per expert: 2I for a gated fc1, else the output rows
+  const int N = a.fc == 1 && act_gated(a.act.act) ? 2 * a.I_or_0 : a.N_out;
   const int row_bytes = a.K * a.bits / 8;
   const int nblk = a.K / a.B;
   const size_t er = (size_t)e * N + row;
@@ -264,7 +265,8 @@ __global__ void __launch_bounds__(256) simt_kernel(const SimtArgs a) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n = blockIdx.x * 8 + warp;
   if (n >= a.N_out) return;
-  const bool glu_fc = a.fc == 1;
+  const bool glu_fc = a.fc == 1 && act_gated(a.act.act);
+  const bool act_fc = a.fc == 1 && !glu_fc;   // non-gated fc1
   float ag[kSimtRows] = {0.f, 0.f, 0.f, 0.f}, au[kSimtRows] = {0.f, 0.f, 0.f, 0.f};
   // fc1 rows of feature n: concatenated [gate | up] or interleaved pairs
   const int grow = glu_fc && a.interleaved ? 2 * n : n;
@@ -300,6 +302,7 @@ __global__ void __launch_bounds__(256) simt_kernel(const SimtArgs a) {
     for (int r = 0; r < it.rows && r < kSimtRows; ++r) {
       const size_t o = (size_t)(it.start + r) * a.N_out + n;
       if (glu_fc) store_d<DT>(a.dst, o, glu(a.act, ag[r] + bg, au[r] + bu));
+      else if (act_fc) store_d<DT>(a.dst, o, act_single(a.act, ag[r] + bg));
       else static_cast<float*>(a.dst)[o] = ag[r] + bg;
     }
   }

@@ -49,10 +49,12 @@ __device__ __forceinline__ uint32_t code_pair(const uint32_t* cw, const uint32_t
   }
 }
 
-template <int BITS, int ZPM, bool BF16, bool GLU, int BLK>
+// EPI: 0 = fc2, 1 = gated fc1 (gate and up sub-tiles), 2 = non-gated fc1.
+template <int BITS, int ZPM, bool BF16, int EPI, int BLK>
 __global__ void __launch_bounds__(kWarps * 32, 1)
     decode_mma_kernel(const DecodeArgs a, int tpc, int ksplit, int stages, int g_chunks) {
   extern __shared__ __align__(128) uint8_t smem[];
+  constexpr bool GLU = EPI == 1;
   constexpr int NSUB = GLU ? 2 : 1;
   constexpr int SC = BLK > 64 ? BLK : 64;  // super-chunk length along K
   constexpr int KT = SC / 16;              // k-tiles per super-chunk
@@ -351,8 +353,8 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
       if (GLU) acc[NSUB - 1][n][q] += bias_u[q >> 1];
       if (tok < it.rows) {
         const size_t o = (size_t)(it.start + tok) * a.N_out + row;
-        if (GLU) {
-          const float h = glu(a.act, acc[0][n][q], acc[1][n][q]);
+        if (EPI != 0) {
+          const float h = GLU ? glu(a.act, acc[0][n][q], acc[1][n][q]) : act_single(a.act, acc[0][n][q]);
           if (BF16) static_cast<__nv_bfloat16*>(a.dst)[o] = __float2bfloat16_rn(h);
           else static_cast<__half*>(a.dst)[o] = __float2half_rn(h);
         } else if (a.atomic) {
@@ -366,7 +368,7 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
   }
 }
 
-template <int BITS, int ZPM, bool BF16, bool GLU, int BLK>
+template <int BITS, int ZPM, bool BF16, int EPI, int BLK>
 static cudaError_t launch_dm(const DecodeArgs& a, cudaStream_t s) {
   const DecodeLayout& L = a.L;
   // Split-K when the tiles alone would not fill the GPU.
@@ -390,7 +392,7 @@ static cudaError_t launch_dm(const DecodeArgs& a, cudaStream_t s) {
     sm = decode_smem(L, a.ng, stages, g_chunks, ksplit);
   }
   if (sm.total > 227 * 1024) return cudaErrorInvalidConfiguration;
-  auto kern = decode_mma_kernel<BITS, ZPM, BF16, GLU, BLK>;
+  auto kern = decode_mma_kernel<BITS, ZPM, BF16, EPI, BLK>;
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, sm.total);
   if (err != cudaSuccess) return err;
   cudaLaunchConfig_t cfg = {};
@@ -406,16 +408,19 @@ static cudaError_t launch_dm(const DecodeArgs& a, cudaStream_t s) {
   return cudaLaunchKernelEx(&cfg, kern, a, tpc, ksplit, stages, g_chunks);
 }
 
-template <int BITS, int ZPM, bool BF16, bool GLU>
+template <int BITS, int ZPM, bool BF16, int EPI>
 static cudaError_t dispatch_blk(const DecodeArgs& a, cudaStream_t s) {
-  if (a.L.B == 32) return launch_dm<BITS, ZPM, BF16, GLU, 32>(a, s);
-  if (a.L.B == 64) return launch_dm<BITS, ZPM, BF16, GLU, 64>(a, s);
-  return launch_dm<BITS, ZPM, BF16, GLU, 128>(a, s);
+  if (a.L.B == 32) return launch_dm<BITS, ZPM, BF16, EPI, 32>(a, s);
+  if (a.L.B == 64) return launch_dm<BITS, ZPM, BF16, EPI, 64>(a, s);
+  return launch_dm<BITS, ZPM, BF16, EPI, 128>(a, s);
 }
 template <int BITS, int ZPM, bool BF16>
 static cudaError_t dispatch_glu(const DecodeArgs& a, cudaStream_t s) {
-  if (a.fc == 1) return dispatch_blk<BITS, ZPM, BF16, true>(a, s);
-  return dispatch_blk<BITS, ZPM, BF16, false>(a, s);
+  if (a.fc == 1) {
+    if (act_gated(a.act.act)) return dispatch_blk<BITS, ZPM, BF16, 1>(a, s);
+    return dispatch_blk<BITS, ZPM, BF16, 2>(a, s);
+  }
+  return dispatch_blk<BITS, ZPM, BF16, 0>(a, s);
 }
 template <int BITS, int ZPM>
 static cudaError_t dispatch_dt(const DecodeArgs& a, cudaStream_t s) {

@@ -82,7 +82,7 @@ cudaError_t launch_route_group(const RouteArgs& a, bool fused, cudaStream_t s);
 
 // Gated activation of fc1's output: SwiGLU (with its attributes) or GeGLU.
 struct ActParams {
-  int act;                  // QMOE_ACT_SWIGLU | QMOE_ACT_GEGLU_TANH
+  int act;                  // QMOE_ACT_* (gated: SWIGLU, GEGLU_TANH)
   float alpha, beta, limit; // SwiGLU only
 };
 
@@ -469,6 +469,19 @@ __device__ __forceinline__ float act_swiglu(float g, float u, float alpha, float
 }
 __device__ __forceinline__ float glu(const ActParams& p, float g, float u) {
   return p.act == QMOE_ACT_SWIGLU ? act_swiglu(g, u, p.alpha, p.beta, p.limit) : act_gelu_tanh(g) * u;
+}
+// Non-gated activation of one fc1 output [qmoe.rs qmoe_activate]: relu,
+// tanh-GELU, silu (v * stable sigmoid(v)) or identity.
+__device__ __forceinline__ float act_single(const ActParams& p, float v) {
+  switch (p.act) {
+    case QMOE_ACT_RELU: return fmaxf(v, 0.f);
+    case QMOE_ACT_GELU_TANH: return act_gelu_tanh(v);
+    case QMOE_ACT_SILU: return v * (v >= 0.f ? 1.f / (1.f + expf(-v)) : expf(v) / (1.f + expf(v)));
+    default: return v;
+  }
+}
+__host__ __device__ __forceinline__ bool act_gated(int act) {
+  return act == QMOE_ACT_SWIGLU || act == QMOE_ACT_GEGLU_TANH;
 }
 
 }  // namespace qmoe

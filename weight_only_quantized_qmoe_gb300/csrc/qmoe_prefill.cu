@@ -594,9 +594,11 @@ __device__ __forceinline__ void bulk_g2s_elect(void* dst, const void* src, uint3
 //   last 4 epilogue (TMEM lanes 32*(w%4))
 // The MMA issuer polls without suspending (it paces the ring); the producer,
 // dequant and epilogue warps park on their barriers.
-template <int BITS, int ZPM, bool BF16, bool GLU, bool DEC>
+// EPI: 0 = fc2 (weighted combine), 1 = gated fc1 (GLU), 2 = non-gated fc1.
+template <int BITS, int ZPM, bool BF16, int EPI, bool DEC>
 __global__ void __launch_bounds__((Ring<DEC, BITS>::threads), 1)
     gemm_kernel(const GemmArgs a) {
+  constexpr bool GLU = EPI == 1;
   using RG = Ring<DEC, BITS>;
   constexpr int kDeqGroups = RG::groups;
   constexpr int kEpiWarp0 = RG::epi_warp0;
@@ -803,7 +805,7 @@ __global__ void __launch_bounds__((Ring<DEC, BITS>::threads), 1)
       if (lane == 0) mbar_arrive(&ready[s]);
     }
   } else if (warp >= kEpiWarp0) {
-    // ---------------- epilogue: TMEM -> GLU -> h (fc1) | weighted scatter (fc2) ----------------
+    // ---------------- epilogue: TMEM -> GLU / act -> h (fc1) | weighted scatter (fc2) ----------------
     // Each warp owns TMEM lanes 32q..32q+31 (its 32 weight rows) and a 32x32
     // shared tile in which it turns its (row, token) values around, so that
     // global memory sees 16-byte stores (fc1) / 16-byte reductions (fc2)
@@ -827,7 +829,7 @@ __global__ void __launch_bounds__((Ring<DEC, BITS>::threads), 1)
         int my_tok = 0;
         float my_w = 0.f;
         const bool col_ok = c0 + lane < it.rows;
-        if (!GLU && col_ok) {
+        if (EPI == 0 && col_ok) {
           const int route = a.perm[it.start + c0 + lane];
           my_tok = route / a.k;
           my_w = a.w[route];
@@ -884,13 +886,44 @@ __global__ void __launch_bounds__((Ring<DEC, BITS>::threads), 1)
           for (int j = 0; j < 32; ++j) tile32[j * kEpiPitch + lane] = __uint_as_float(v[j]) + b;
           __syncwarp();
           const int mbase = nt * 128 + q * 32;
-          if (col_ok && mbase < a.N_out) {
-            float* dst = a.out_acc + (size_t)my_tok * a.N_out + mbase;
-            const float* src = tile32 + lane * kEpiPitch;
+          const float* src = tile32 + lane * kEpiPitch;
+          if (EPI == 0) {
+            if (col_ok && mbase < a.N_out) {
+              float* dst = a.out_acc + (size_t)my_tok * a.N_out + mbase;
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-              const float4 y = *reinterpret_cast<const float4*>(src + 4 * i);
-              red_add_v4_f32(dst + 4 * i, my_w * y.x, my_w * y.y, my_w * y.z, my_w * y.w);
+              for (int i = 0; i < 8; ++i) {
+                const float4 y = *reinterpret_cast<const float4*>(src + 4 * i);
+                red_add_v4_f32(dst + 4 * i, my_w * y.x, my_w * y.y, my_w * y.z, my_w * y.w);
+              }
+            }
+          } else {
+            // non-gated fc1: h = act(fc1 output) of token c0 + lane, features
+            // mbase .. mbase + 31 -> the tiled token layout of fc2's B operand
+            // (rows up to the next multiple of 8 and features past I as zeros)
+            const int c = c0 + lane, item = tile / L.ntiles;
+            if (c < ((it.rows + 7) & ~7)) {
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                const int n = mbase + 8 * i;
+                if (n < a.h_ksteps * 64) {
+                  uint32_t w4[4] = {0u, 0u, 0u, 0u};
+                  if (c < it.rows && n < a.N_out) {
+#pragma unroll
+                    for (int m = 0; m < 4; ++m) {
+                      const float h0 = act_single(a.act, src[8 * i + 2 * m]);
+                      const float h1 = act_single(a.act, src[8 * i + 2 * m + 1]);
+                      const uint32_t lo = BF16 ? __bfloat16_as_ushort(__float2bfloat16_rn(h0))
+                                               : __half_as_ushort(__float2half_rn(h0));
+                      const uint32_t hi = BF16 ? __bfloat16_as_ushort(__float2bfloat16_rn(h1))
+                                               : __half_as_ushort(__float2half_rn(h1));
+                      w4[m] = lo | (hi << 16);
+                    }
+                  }
+                  uint8_t* dst = a.htiles + tok_tile_offset(item, a.h_ksteps, n >> 6) + c * 128 +
+                                 ((((n & 63) >> 3) ^ (c & 7)) << 4);
+                  *reinterpret_cast<uint4*>(dst) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+                }
+              }
             }
           }
           __syncwarp();
@@ -911,10 +944,10 @@ __global__ void __launch_bounds__((Ring<DEC, BITS>::threads), 1)
 // ----------------------------------------------------------------------------
 // Host side
 // ----------------------------------------------------------------------------
-template <int BITS, int ZPM, bool BF16, bool GLU, bool DEC>
+template <int BITS, int ZPM, bool BF16, int EPI, bool DEC>
 static cudaError_t launch_g(const GemmArgs& a, cudaStream_t s) {
   const int smem = Ring<DEC, BITS>::total(a.L.stage_bytes) + 1024;  // + alignment slack
-  auto kern = gemm_kernel<BITS, ZPM, BF16, GLU, DEC>;
+  auto kern = gemm_kernel<BITS, ZPM, BF16, EPI, DEC>;
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (err != cudaSuccess) return err;
   cudaLaunchConfig_t cfg = {};
@@ -930,13 +963,14 @@ static cudaError_t launch_g(const GemmArgs& a, cudaStream_t s) {
   return cudaLaunchKernelEx(&cfg, kern, a);
 }
 
-template <int BITS, int ZPM, bool BF16, bool GLU>
+template <int BITS, int ZPM, bool BF16, int EPI>
 static cudaError_t launch_g_ring(const GemmArgs& a, cudaStream_t s) {
-  return a.dec ? launch_g<BITS, ZPM, BF16, GLU, true>(a, s) : launch_g<BITS, ZPM, BF16, GLU, false>(a, s);
+  return a.dec ? launch_g<BITS, ZPM, BF16, EPI, true>(a, s) : launch_g<BITS, ZPM, BF16, EPI, false>(a, s);
 }
 template <int BITS, int ZPM, bool BF16>
 static cudaError_t launch_g_glu(const GemmArgs& a, cudaStream_t s) {
-  return a.fc == 1 ? launch_g_ring<BITS, ZPM, BF16, true>(a, s) : launch_g_ring<BITS, ZPM, BF16, false>(a, s);
+  if (a.fc != 1) return launch_g_ring<BITS, ZPM, BF16, 0>(a, s);
+  return act_gated(a.act.act) ? launch_g_ring<BITS, ZPM, BF16, 1>(a, s) : launch_g_ring<BITS, ZPM, BF16, 2>(a, s);
 }
 template <int BITS, int ZPM>
 static cudaError_t launch_g_dt(const GemmArgs& a, cudaStream_t s) {
