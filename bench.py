@@ -35,7 +35,7 @@ METRIC = "QMoE layer µs & tokens/s; % HBM roofline (decode), % tensor peak (pre
 # gemm_kernel launch, from one ncu capture of the current kernel
 # (profiles/gemm_kernel_decode_int2_fc1.md, profiles/gemm_kernel_prefill_fc1.md);
 # None where no capture of the current kernel exists for the workload.
-FC1_TRAFFIC = {"decode_int2": 19_205_632, "prefill_int4": 803_082_752}
+FC1_TRAFFIC = {"decode_int2": 19_206_144, "prefill_int4": 802_950_656}
 L2_BYTES = 129 * 1024 * 1024
 
 
