@@ -105,7 +105,7 @@ enum {
  *   hidden, inter   H and I (fc1 has 2*inter rows, gate then up)
  *   experts, top_k  E (1..1024) and k (1 <= k <= E)  [qmoe.rs requires
  *                   0 < k <= num_experts]
- *   bits_fc1/fc2    code widths, each in {2, 3, 4, 8}
+ *   bits_fc1/fc2    code widths, each in {1, 2, 3, 4, 8}
  *   block_size      B in {32, 64, 128}; hidden and inter must be multiples
  *                   of B  [qmoe.rs: power of two >= 16 dividing K]
  *   zp_mode         QMOE_ZP_SYMMETRIC (zp = 2^(bits-1)), QMOE_ZP_UINT8

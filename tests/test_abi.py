@@ -42,14 +42,15 @@ def test_create_validates(lib):
         assert b.qmoe_set_fc1_layout(h, b.QMOE_FC1_SEPARATE_FC3) == b.QMOE_ERR_INVALID_ARG
         assert b.qmoe_set_fc1_layout(h, b.QMOE_FC1_CONCAT) == b.QMOE_OK
         b.qmoe_destroy(h)
-    for widths in ((8, 8), (8, 2), (3, 8)):
+    for widths in ((8, 8), (8, 2), (3, 8), (1, 1), (1, 4)):
         st, h = _create(bits_fc1=widths[0], bits_fc2=widths[1])
         assert st == b.QMOE_OK and h, widths
         b.qmoe_destroy(h)
     for kw, want in [
         (dict(bits_fc1=5), b.QMOE_ERR_UNSUPPORTED),
         (dict(bits_fc2=7), b.QMOE_ERR_UNSUPPORTED),
-        (dict(bits_fc1=1), b.QMOE_ERR_UNSUPPORTED),
+        (dict(bits_fc1=0), b.QMOE_ERR_UNSUPPORTED),
+        (dict(bits_fc2=6), b.QMOE_ERR_UNSUPPORTED),
         (dict(block_size=16), b.QMOE_ERR_UNSUPPORTED),
         (dict(top_k=9), b.QMOE_ERR_INVALID_ARG),
         (dict(top_k=0), b.QMOE_ERR_INVALID_ARG),

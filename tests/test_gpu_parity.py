@@ -190,6 +190,7 @@ WIDTH_CASES = dict(_width_cases())
 # 8-bit codes (fp16 magic path; bf16 nibble-split path) with every zero-point
 # mode, mixed with narrower widths, and on the fp32 SIMT path; scales sized so
 # that fp16 outputs stay in range with codes up to +-255 from the centre.
+# 1-bit codes likewise.
 WIDTH_CASES.update({
     "w88_B32_sym_f16": dict(bits1=8, bits2=8, B=32, dtype="f16", T=12, scale_lo=0.0005, scale_hi=0.002),
     "w88_B128_sym_bf16": dict(bits1=8, bits2=8, B=128, dtype="bf16", T=12, scale_lo=0.0005, scale_hi=0.002),
@@ -201,6 +202,14 @@ WIDTH_CASES.update({
                                     T=12, scale_lo=0.01, scale_hi=0.03),
     "w48_B32_offset_int_bf16": dict(bits1=4, bits2=8, B=32, zp_mode="offset", zp_offset=3.0,
                                     dtype="bf16", T=12, scale_lo=0.002, scale_hi=0.006),
+    # 1-bit codes (centre 1)
+    "w11_B32_sym_bf16": dict(bits1=1, bits2=1, B=32, dtype="bf16", T=12, scale_lo=0.05, scale_hi=0.2),
+    "w12_B64_offset_f16": dict(bits1=1, bits2=2, B=64, zp_mode="offset", zp_offset=0.5, dtype="f16", T=12,
+                               scale_lo=0.05, scale_hi=0.2),
+    "w41_B128_uint8_bf16": dict(bits1=4, bits2=1, B=128, zp_mode="uint8", zp_lo=0, zp_hi=1, dtype="bf16",
+                                T=12, scale_lo=0.005, scale_hi=0.02),
+    "w18_B32_sym_f16": dict(bits1=1, bits2=8, B=32, dtype="f16", T=12, scale_lo=0.05, scale_hi=0.1),
+    "w11_B64_sym_f32": dict(bits1=1, bits2=1, B=64, dtype="f32", T=9, scale_lo=0.05, scale_hi=0.2),
     "w88_B64_uint8_f32": dict(bits1=8, bits2=8, B=64, zp_mode="uint8", zp_lo=90, zp_hi=170, dtype="f32",
                               T=9, scale_lo=0.0005, scale_hi=0.002),
 })

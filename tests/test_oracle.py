@@ -153,7 +153,7 @@ def test_unpack_int3_straddles_bytes():
 
 def test_pack_unpack_roundtrip():
     rng = np.random.default_rng(7)
-    for bits in (2, 3, 4, 8):
+    for bits in (1, 2, 3, 4, 8):
         vals = rng.integers(0, 1 << bits, size=(5, 96))
         np.testing.assert_array_equal(O.unpack_fields(pack_fields(vals, bits), bits, 96), vals)
 
@@ -176,7 +176,7 @@ def test_dequant_symmetric_golden():
         np.testing.assert_array_equal(W, mult * s)
 
 
-@pytest.mark.parametrize("bits", [2, 3, 4, 8])
+@pytest.mark.parametrize("bits", [1, 2, 3, 4, 8])
 def test_zero_point_modes_agree_at_the_centre(bits):
     rng = np.random.default_rng(8 + bits)
     N, K, B = 6, 128, 32
@@ -356,6 +356,9 @@ SMALL_VARIANTS = {
     # 8-bit codes with byte zero points away from the centre
     "int8_uint8_f16": dict(bits1=8, bits2=8, zp_mode="uint8", zp_lo=100, zp_hi=150, dtype="f16",
                            H=64, I=64, scale_lo=0.0005, scale_hi=0.002),
+    # 1-bit codes (centre 1) with 1-bit zero points
+    "int1_uint8_bf16": dict(bits1=1, bits2=1, zp_mode="uint8", zp_lo=0, zp_hi=1, dtype="bf16",
+                            H=64, I=64, scale_lo=0.05, scale_hi=0.2),
     # non-gated activations: fc1 has I rows, h = act(fc1 output)
     "relu_bias_f16": dict(act="relu", bias=True, dtype="f16", H=64, I=64),
     "gelu_int3": dict(act="gelu", bits1=3, bits2=4, dtype="bf16", H=64, I=64, E=3, k=2),

@@ -16,7 +16,8 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIB_PATH = os.path.join(HERE, "libqmoe.so")
 SOURCES = ["qmoe_api.cu", "qmoe_route.cu", "qmoe_decode.cu", "qmoe_prefill.cu", "qmoe_decode_b2.cu",
-           "qmoe_decode_b3.cu", "qmoe_decode_b4.cu", "qmoe_decode_b8.cu"]
+           "qmoe_decode_b3.cu", "qmoe_decode_b4.cu", "qmoe_decode_b8.cu",
+           "qmoe_decode_b1.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
          "--expt-relaxed-constexpr", "-I", INCLUDE]

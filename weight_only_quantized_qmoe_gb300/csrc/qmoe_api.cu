@@ -289,7 +289,7 @@ qmoe_status qmoe_create(int hidden, int inter, int experts, int top_k, int bits_
   if (experts > 1024) return QMOE_ERR_UNSUPPORTED;
   if (top_k > experts) return QMOE_ERR_INVALID_ARG;
   for (int b : {bits_fc1, bits_fc2})
-    if (b != 2 && b != 3 && b != 4 && b != 8) return QMOE_ERR_UNSUPPORTED;
+    if (b != 1 && b != 2 && b != 3 && b != 4 && b != 8) return QMOE_ERR_UNSUPPORTED;
   if (block_size != 32 && block_size != 64 && block_size != 128) return QMOE_ERR_UNSUPPORTED;
   if (hidden % block_size || inter % block_size) return QMOE_ERR_INVALID_ARG;
   if (zp_mode < QMOE_ZP_SYMMETRIC || zp_mode > QMOE_ZP_OFFSET) return QMOE_ERR_INVALID_ARG;

@@ -94,7 +94,23 @@ __global__ void repack_decode_kernel(const RepackArgs a) {
       return kc * L.SC + j * 16 + 2 * t + ((r & 2) ? 8 : 0) + e2;
     };
     uint32_t* cw = reinterpret_cast<uint32_t*>(out + s * L.code_bytes);
-    if (bits == 8) {
+    if (bits == 1) {
+      // one word per lane and four k-tiles: bit 4 (j & 3) + r of the low half
+      // holds element 0 of pair r of k-tile j, the same bit of the high half
+      // element 1
+      const int W = ktiles / 4;
+      for (int i = threadIdx.x; i < 32 * W; i += blockDim.x) {
+        const int lane = i / W, wj = i % W, g = lane >> 2, t = lane & 3;
+        uint32_t w = 0;
+        for (int jj = 0; jj < 4; ++jj)
+          for (int r = 0; r < 4; ++r) {
+            const int j = 4 * wj + jj, row = crow(g + ((r & 1) ? 8 : 0));
+            w |= (uint32_t)code(row, kidx(j, t, r, 0)) << (4 * jj + r);
+            w |= (uint32_t)code(row, kidx(j, t, r, 1)) << (16 + 4 * jj + r);
+          }
+        cw[lane * W + wj] = w;
+      }
+    } else if (bits == 8) {
       // two words per lane and k-tile: word 2j + (r >> 1) holds pair r in
       // bytes (r & 1) and 2 + (r & 1)
       const int W = 2 * ktiles;
@@ -201,6 +217,7 @@ cudaError_t launch_repack_decode(const RepackArgs& a, cudaStream_t s) {
 
 template <int BITS>
 cudaError_t launch_decode_mma_bits(const DecodeArgs& a, cudaStream_t s);
+extern template cudaError_t launch_decode_mma_bits<1>(const DecodeArgs&, cudaStream_t);
 extern template cudaError_t launch_decode_mma_bits<2>(const DecodeArgs&, cudaStream_t);
 extern template cudaError_t launch_decode_mma_bits<3>(const DecodeArgs&, cudaStream_t);
 extern template cudaError_t launch_decode_mma_bits<4>(const DecodeArgs&, cudaStream_t);
@@ -210,6 +227,7 @@ cudaError_t launch_decode_mma(const DecodeArgs& a, cudaStream_t s) {
   if (a.max_items <= 0) return cudaSuccess;
   if (a.ng < 1 || a.ng > 4) return cudaErrorInvalidValue;
   switch (a.L.bits) {
+    case 1: return launch_decode_mma_bits<1>(a, s);
     case 2: return launch_decode_mma_bits<2>(a, s);
     case 3: return launch_decode_mma_bits<3>(a, s);
     case 4: return launch_decode_mma_bits<4>(a, s);

@@ -38,6 +38,8 @@ template <int BITS>
 __device__ __forceinline__ uint32_t code_pair(const uint32_t* cw, const uint32_t* hw, int j, int r) {
   if (BITS == 8) {
     return cw[2 * j + (r >> 1)] >> (8 * (r & 1));   // bytes 0 and 2 (bits above ignored)
+  } else if (BITS == 1) {
+    return (cw[j >> 2] >> (4 * (j & 3) + r)) & 0x00010001u;
   } else if (BITS == 4) {
     return (cw[j] >> (4 * r)) & 0x000F000Fu;
   } else if (BITS == 2) {
@@ -191,7 +193,7 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
       const uint8_t* ch = st + c * L.scb;
       const int kc = kc0 + i * g_chunks + c;
       // this lane's code words for each sub-tile
-      constexpr int WPL = BITS == 8 ? SC / 8 : (BITS == 4 ? SC / 16 : SC / 32);   // (low-plane) words per lane
+      constexpr int WPL = BITS == 8 ? SC / 8 : (BITS == 4 ? SC / 16 : (BITS == 1 ? SC / 64 : SC / 32));   // (low-plane) words per lane
       constexpr int WPH = BITS == 3 ? SC / 64 : 1;
       uint32_t cw[NSUB][WPL];
       uint32_t hw[NSUB][WPH];
@@ -204,13 +206,15 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
             const uint4 q4 = *reinterpret_cast<const uint4*>(base + lane * WPL + w);
             cw[s][w] = q4.x; cw[s][w + 1] = q4.y; cw[s][w + 2] = q4.z; cw[s][w + 3] = q4.w;
           }
-        } else {
-          static_assert(WPL % 2 == 0, "code words per lane");
+        } else if constexpr (WPL % 2 == 0) {
 #pragma unroll
           for (int w = 0; w < WPL; w += 2) {
             const uint2 q2 = *reinterpret_cast<const uint2*>(base + lane * WPL + w);
             cw[s][w] = q2.x; cw[s][w + 1] = q2.y;
           }
+        } else {
+          static_assert(WPL == 1, "code words per lane");
+          cw[s][0] = base[lane];
         }
         if constexpr (BITS == 3) {
 #pragma unroll

@@ -76,7 +76,17 @@ __global__ void repack_gemm_kernel(const GemmRepackArgs a) {
   uint8_t* stage = a.out + ((((size_t)e * L.ntiles + nt) * L.ksteps) + ks) * L.stage_bytes;
   uint32_t* cw = reinterpret_cast<uint32_t*>(stage + (size_t)r * L.code_row);
   const int k0 = ks * 64;
-  if (bits == 8) {
+  if (bits == 1) {
+    // word i: bit m of the low / high half = codes k0 + 32 i + 2 m / + 1
+    for (int i = 0; i < 2; ++i) {
+      uint32_t w = 0;
+      for (int m = 0; m < 16; ++m) {
+        w |= (uint32_t)code(k0 + 32 * i + 2 * m) << m;
+        w |= (uint32_t)code(k0 + 32 * i + 2 * m + 1) << (16 + m);
+      }
+      cw[i] = w;
+    }
+  } else if (bits == 8) {
     // word i: k pairs 2i (bytes 0 and 2) and 2i+1 (bytes 1 and 3)
     for (int i = 0; i < 16; ++i) {
       const int kk = k0 + 4 * i;
@@ -458,9 +468,12 @@ __device__ __forceinline__ void dequant_row(const uint8_t* stage, const GemmLayo
                                             uint32_t* v) {
   constexpr uint32_t MAGIC = BF16 ? 0x43004300u : 0x64006400u;
   const uint8_t* row = stage + r * (64 * BITS / 8);
-  constexpr int NW = BITS == 8 ? 16 : (BITS == 4 ? 8 : (BITS == 3 ? 6 : 4));
+  constexpr int NW = BITS == 8 ? 16 : (BITS == 4 ? 8 : (BITS == 3 ? 6 : (BITS == 1 ? 2 : 4)));
   uint32_t w[NW];
-  if constexpr (BITS == 8) {
+  if constexpr (BITS == 1) {
+    const uint2 q0 = reinterpret_cast<const uint2*>(row)[0];
+    w[0] = q0.x; w[1] = q0.y;
+  } else if constexpr (BITS == 8) {
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       const uint4 q = reinterpret_cast<const uint4*>(row)[i];
@@ -514,7 +527,8 @@ __device__ __forceinline__ void dequant_row(const uint8_t* stage, const GemmLayo
       continue;
     }
     uint32_t p;
-    if constexpr (BITS == 4) p = (w[j >> 2] >> (4 * (j & 3))) & 0x000F000Fu;
+    if constexpr (BITS == 1) p = (w[j >> 4] >> (j & 15)) & 0x00010001u;
+    else if constexpr (BITS == 4) p = (w[j >> 2] >> (4 * (j & 3))) & 0x000F000Fu;
     else if constexpr (BITS == 2) p = (w[j >> 3] >> (2 * (j & 7))) & 0x00030003u;
     else p = ((w[j >> 3] >> (2 * (j & 7))) & 0x00030003u) | (((w[4 + (j >> 4)] >> (j & 15)) & 0x00010001u) << 2);
     uint32_t x;
@@ -986,6 +1000,7 @@ static cudaError_t launch_g_zp(const GemmArgs& a, cudaStream_t s) {
 cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t s) {
   if (a.max_items <= 0 || a.grid <= 0) return cudaSuccess;
   switch (a.L.bits) {
+    case 1: return launch_g_zp<1>(a, s);
     case 2: return launch_g_zp<2>(a, s);
     case 3: return launch_g_zp<3>(a, s);
     case 4: return launch_g_zp<4>(a, s);

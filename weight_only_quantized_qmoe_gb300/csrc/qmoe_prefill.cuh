@@ -13,7 +13,8 @@ namespace qmoe {
 //   codes : 128 rows x (64*bits/8) bytes; per 32-bit word the two codes of a
 //           k pair sit in the low and high 16-bit halves (int3: 2-bit plane
 //           words, then 1-bit plane words; int8: word i holds the pairs 2i in
-//           bytes 0 and 2 and 2i+1 in bytes 1 and 3)
+//           bytes 0 and 2 and 2i+1 in bytes 1 and 3; 1-bit: bit m of word i's
+//           low / high half holds codes 32i + 2m / 32i + 2m + 1)
 //   scales: 128 rows x nbs values of D (nbs = quantisation blocks in the step)
 //   zp    : 128 rows x nbs bytes (uint8 zero points), padded to 16 bytes
 // so each step is one contiguous bulk copy.  Rows past N and k past K hold
