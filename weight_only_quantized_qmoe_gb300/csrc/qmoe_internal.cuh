@@ -236,28 +236,6 @@ __device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Non-blocking test of four mbarrier phases at once (one round trip to the
-// barrier unit instead of four).
-__device__ __forceinline__ bool mbar_test_wait4(uint64_t* b0, uint32_t p0, uint64_t* b1, uint32_t p1,
-                                                uint64_t* b2, uint32_t p2, uint64_t* b3, uint32_t p3) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred q0, q1, q2, q3;\n\t"
-      "mbarrier.test_wait.parity.shared::cta.b64 q0, [%1], %2;\n\t"
-      "mbarrier.test_wait.parity.shared::cta.b64 q1, [%3], %4;\n\t"
-      "mbarrier.test_wait.parity.shared::cta.b64 q2, [%5], %6;\n\t"
-      "mbarrier.test_wait.parity.shared::cta.b64 q3, [%7], %8;\n\t"
-      "and.pred q0, q0, q1;\n\t"
-      "and.pred q2, q2, q3;\n\t"
-      "and.pred q0, q0, q2;\n\t"
-      "selp.u32 %0, 1, 0, q0;\n\t}"
-      : "=r"(ok)
-      : "r"(smem_u32(b0)), "r"(p0), "r"(smem_u32(b1)), "r"(p1), "r"(smem_u32(b2)), "r"(p2),
-        "r"(smem_u32(b3)), "r"(p3)
-      : "memory");
-  return ok != 0;
-}
-
 // Bounded wait: returns false (and records DEV_TIMEOUT) if the phase did not
 // complete within `limit` polls.
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity,
