@@ -151,7 +151,10 @@ qmoe_status qmoe_set_swiglu_params(qmoe_layer* layer, float alpha, float beta, f
  * linear = fc3), each [E, I, ...] and prepacked / biased with fc = 1 and
  * fc = 3.  Other values: INVALID_ARG.  Must precede qmoe_prepack(fc = 1 or 3)
  * and qmoe_set_bias(fc = 1 or 3); STATE otherwise.  With a non-gated
- * activation only QMOE_FC1_CONCAT applies (INVALID_ARG otherwise). */
+ * activation only QMOE_FC1_CONCAT applies (INVALID_ARG otherwise), except
+ * QMOE_ACT_SILU with QMOE_FC1_SEPARATE_FC3, which is the gated form (gate =
+ * fc1, up = fc3 through the SwiGLU of qmoe_set_swiglu_params) [qmoe.rs
+ * uses_separate_gate]: the layer then behaves as QMOE_ACT_SWIGLU. */
 enum { QMOE_FC1_CONCAT = 0, QMOE_FC1_INTERLEAVED = 1, QMOE_FC1_SEPARATE_FC3 = 2 };
 qmoe_status qmoe_set_fc1_layout(qmoe_layer* layer, int layout);
 

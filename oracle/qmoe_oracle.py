@@ -341,6 +341,10 @@ def forward(inputs: dict, tokens=None, round_h: bool = False, return_parts: bool
             a, layout = np.concatenate([a, a3], axis=1), "concat"
         if cfg.act in GATED:
             h = glu(a, cfg.I, cfg.act, layout, cfg.swiglu_alpha, cfg.swiglu_beta, cfg.swiglu_limit)
+        elif cfg.act == "silu" and cfg.fc1_layout == "separate":
+            # qmoe.rs uses_separate_gate: silu beside fc3 takes the gated
+            # branch of qmoe_activate (swiglu_value of gate = fc1, linear = fc3)
+            h = glu(a, cfg.I, "swiglu", layout, cfg.swiglu_alpha, cfg.swiglu_beta, cfg.swiglu_limit)
         else:
             h = act_single(a, cfg.act)
         if round_h:

@@ -37,9 +37,11 @@ def test_create_validates(lib):
     for act in (b.QMOE_ACT_RELU, b.QMOE_ACT_GELU_TANH, b.QMOE_ACT_SILU, b.QMOE_ACT_IDENTITY):
         st, h = _create(activation=act)
         assert st == b.QMOE_OK and h, act
-        # the fc1 row layouts are for gated activations only
+        # the fc1 row layouts are for gated activations only (silu beside a
+        # separate fc3 is the gated form)
         assert b.qmoe_set_fc1_layout(h, b.QMOE_FC1_INTERLEAVED) == b.QMOE_ERR_INVALID_ARG
-        assert b.qmoe_set_fc1_layout(h, b.QMOE_FC1_SEPARATE_FC3) == b.QMOE_ERR_INVALID_ARG
+        want = b.QMOE_OK if act == b.QMOE_ACT_SILU else b.QMOE_ERR_INVALID_ARG
+        assert b.qmoe_set_fc1_layout(h, b.QMOE_FC1_SEPARATE_FC3) == want
         assert b.qmoe_set_fc1_layout(h, b.QMOE_FC1_CONCAT) == b.QMOE_OK
         b.qmoe_destroy(h)
     for widths in ((8, 8), (8, 2), (3, 8), (1, 1), (1, 4)):

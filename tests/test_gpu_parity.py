@@ -144,6 +144,8 @@ FEATURE_VARIANTS = {
                                                B=128, T=9),
     "separate_fc3_uint8_T150": dict(fc1_layout="separate", zp_mode="uint8", zp_lo=5, zp_hi=11, E=4, T=150),
     "f32_separate_fc3_bias": dict(dtype="f32", fc1_layout="separate", bias=True, T=7),
+    # qmoe.rs uses_separate_gate: silu beside fc3 is the gated form
+    "silu_fc3_params": dict(act="silu", fc1_layout="separate", swiglu_limit=0.5, bias=True, T=11),
     # non-gated activations (qmoe.rs qmoe_activate): fc1 has I rows, h = act(fc1 output)
     "relu_bias": dict(act="relu", bias=True, T=13),
     "gelu_uint8_f16_B64": dict(act="gelu", zp_mode="uint8", zp_lo=5, zp_hi=11, dtype="f16", B=64, T=9),

@@ -302,7 +302,7 @@ def _brute_layer(inp):
         acc = [0.0] * cfg.H
         for e in sel:
             if e not in W1:
-                n1 = 2 * cfg.I if cfg.act in ("swiglu", "geglu") else cfg.I
+                n1 = 2 * cfg.I if (cfg.act in ("swiglu", "geglu") or cfg.fc1_layout == "separate") else cfg.I
                 W1[e] = [[weight(1, e, n, d) for d in range(cfg.H)] for n in range(n1)]
                 W2[e] = [[weight(2, e, n, d) for d in range(cfg.I)] for n in range(cfg.H)]
             b1 = inp["fc1_bias"][e].tolist() if inp.get("fc1_bias") is not None else [0.0] * (2 * cfg.I)
@@ -311,11 +311,11 @@ def _brute_layer(inp):
                 b1 = (b1 if inp.get("fc1_bias") is not None else [0.0] * cfg.I) + b3
             b2 = inp["fc2_bias"][e].tolist() if inp.get("fc2_bias") is not None else [0.0] * cfg.H
             gated = cfg.act in ("swiglu", "geglu")
-            n1 = 2 * cfg.I if gated else cfg.I
+            n1 = 2 * cfg.I if (gated or cfg.fc1_layout == "separate") else cfg.I
             a = [sum(W1[e][n][d] * x[t][d] for d in range(cfg.H)) + b1[n] for n in range(n1)]
             h = []
             for n in range(cfg.I):
-                if not gated:
+                if not gated and cfg.fc1_layout != "separate":
                     v = a[n]
                     h.append({"relu": max(v, 0.0), "identity": v, "silu": v / (1 + math.exp(-v)),
                               "gelu": 0.5 * v * (1 + math.tanh(math.sqrt(2 / math.pi) * (v + 0.044715 * v ** 3)))
@@ -325,7 +325,7 @@ def _brute_layer(inp):
                     g, u = a[2 * n], a[2 * n + 1]
                 else:
                     g, u = a[n], a[cfg.I + n]
-                if cfg.act == "swiglu":
+                if cfg.act in ("swiglu", "silu"):   # silu here only beside fc3 (gated)
                     L = cfg.swiglu_limit
                     g = min(g, L)
                     u = max(-L, min(L, u))
@@ -365,6 +365,9 @@ SMALL_VARIANTS = {
     "silu_uint8": dict(act="silu", zp_mode="uint8", zp_lo=6, zp_hi=9, dtype="f32", H=64, I=64),
     "identity_offset_int2": dict(act="identity", bits1=2, bits2=2, zp_mode="offset", zp_offset=1.5,
                                  dtype="f16", H=64, I=64, B=64),
+    # qmoe.rs uses_separate_gate: silu beside fc3 is the gated form
+    "silu_fc3_params": dict(act="silu", fc1_layout="separate", swiglu_limit=0.5, bias=True, dtype="bf16",
+                            H=64, I=64, E=3, k=2),
     # qmoe.rs unfused SwiGLU: gate rows in fc1, up rows in a separate fc3
     "separate_fc3_bias_uint8": dict(fc1_layout="separate", bias=True, zp_mode="uint8", zp_lo=6, zp_hi=9,
                                     dtype="bf16", H=64, I=64, E=4, k=2),

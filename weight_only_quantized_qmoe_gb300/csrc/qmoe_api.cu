@@ -52,6 +52,7 @@ struct qmoe_layer {
   float sw_alpha = 1.f, sw_beta = 0.f, sw_limit = INFINITY;
   int fc1_interleaved = 0;                 // fc1 canonical rows: [gate | up] or (gate, up) pairs
   int fc1_separate = 0;                    // gate rows from fc1, up rows from a separate fc3
+  int act_created = 0;                     // the activation given to qmoe_create (act may differ: silu + fc3)
   bool fc1_half[2] = {false, false};       // separate: gate / up halves copied in
   float* bias[2] = {nullptr, nullptr};     // fc1: [E, I, 2] (gate, up) pairs ; fc2: [E, H]
   int normalize = 1;
@@ -306,6 +307,7 @@ qmoe_status qmoe_create(int hidden, int inter, int experts, int top_k, int bits_
   l->B = block_size;
   l->zp_mode = zp_mode;
   l->act = activation;
+  l->act_created = activation;
   l->dtype = dtype;
   l->dsize = dtype == QMOE_F32 ? 4 : 2;
   *out = l;
@@ -354,7 +356,10 @@ qmoe_status qmoe_set_swiglu_params(qmoe_layer* l, float alpha, float beta, float
 
 qmoe_status qmoe_set_fc1_layout(qmoe_layer* l, int layout) {
   if (!l || layout < QMOE_FC1_CONCAT || layout > QMOE_FC1_SEPARATE_FC3) return QMOE_ERR_INVALID_ARG;
-  if (layout != QMOE_FC1_CONCAT && !act_gated(l->act))
+  // silu beside a separate fc3 is the gated form [qmoe.rs uses_separate_gate,
+  // qmoe_activate: gate = fc1, linear = fc3, through swiglu_value]
+  const bool silu_fc3 = l->act_created == QMOE_ACT_SILU && layout == QMOE_FC1_SEPARATE_FC3;
+  if (layout != QMOE_FC1_CONCAT && !act_gated(l->act_created) && !silu_fc3)
     return fail(l, QMOE_ERR_INVALID_ARG, "fc1 row layouts apply to gated activations only");
   if (l->proj[0].ready || l->bias[0] || l->fc1_half[0] || l->fc1_half[1])
     return fail(l, QMOE_ERR_STATE,
@@ -362,6 +367,7 @@ qmoe_status qmoe_set_fc1_layout(qmoe_layer* l, int layout) {
   // Separate projections are assembled into the concatenated order.
   l->fc1_interleaved = layout == QMOE_FC1_INTERLEAVED ? 1 : 0;
   l->fc1_separate = layout == QMOE_FC1_SEPARATE_FC3 ? 1 : 0;
+  l->act = silu_fc3 ? QMOE_ACT_SWIGLU : l->act_created;
   return QMOE_OK;
 }
 
