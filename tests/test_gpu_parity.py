@@ -227,6 +227,21 @@ def test_width_matrix_parity(qm, name, path):
     check_out(out, O.forward(inp), cfg.dtype)
 
 
+# The block-size-32 ("two scales per 64-deep step") int2 and mixed int2/int4
+# decode of the "fast INT3" PR's tests: widths (2,2), (2,4), (4,2), 1, 4 and
+# 64 token rows, top-10 routing, on both projection paths.
+@pytest.mark.parametrize("path", sorted(PATHS))
+@pytest.mark.parametrize("T", [1, 4, 64])
+@pytest.mark.parametrize("widths", [(2, 2), (2, 4), (4, 2)])
+def test_block32_int2_decode_parity(qm, widths, T, path):
+    cfg = BASE.with_(bits1=widths[0], bits2=widths[1], B=32, E=64, k=10, T=T, H=256, I=256,
+                     scale_lo=0.02, scale_hi=0.08)
+    inp = make_inputs(cfg)
+    layer, out = run_layer(qm, inp, min_rows=PATHS[path])
+    check_routing(layer, inp, min_rows=PATHS[path])
+    check_out(out, O.forward(inp), cfg.dtype)
+
+
 @pytest.mark.parametrize("name", list(VARIANTS))
 def test_variant_parity(qm, name):
     cfg = BASE.with_(**VARIANTS[name])
