@@ -178,12 +178,19 @@ qmoe_status qmoe_set_bias(qmoe_layer* layer, int fc, const float* bias_dev, void
 qmoe_status qmoe_set_gemm_min_rows(qmoe_layer* layer, int min_rows);
 
 /* Size the device workspace for up to max_tokens tokens.  Required before
- * capturing qmoe_forward into a CUDA graph.  Allocates device memory. */
+ * capturing qmoe_forward into a CUDA graph.  Allocates device memory.
+ * [qmoe.rs QMoEKernel scratch pool (`slots`): a warmed eager pass sizes the
+ * pooled scratch, `capture_support` refuses capture until then, and a slot
+ * that would have to grow during capture is an error] */
 qmoe_status qmoe_reserve(qmoe_layer* layer, int64_t max_tokens);
 
 /*
  * Copy one projection's weights (fc = 1, 2, or 3 with QMOE_FC1_SEPARATE_FC3)
  * from the canonical layout into the layer's own GB300 layouts, on `stream`.
+ * [onnxruntime PR "fused int2 mixed-input GEMM + GeGLU + fractional
+ * zero-point": PrePack wiring for fc1/fc2 (weights re-laid once, at load);
+ * PR "fast INT3 QMoE kernels": PrePack releases the canonical scales once
+ * they are re-laid]
  *   codes_dev        uint8 [E, N, K*bits/8]
  *   scales_dev       D     [E, N, K/B]
  *   zero_points_dev  uint8 [E, N, ceil((K/B)*bits/8)], non-NULL iff
@@ -199,6 +206,9 @@ qmoe_status qmoe_prepack(qmoe_layer* layer, int fc, const uint8_t* codes_dev,
 
 /*
  * The layer forward on device buffers, asynchronous on `stream`.
+ * [qmoe.rs QMoEKernel::execute: validate the inputs, route, group by expert,
+ * run fc1 + activation, fc2 and the weighted combine on the stream; no host
+ * synchronisation while capturing]
  *   x_dev       D [num_tokens, H]
  *   logits_dev  float32 [num_tokens, E]
  *   out_dev     D [num_tokens, H] (written)
@@ -221,7 +231,8 @@ qmoe_status qmoe_forward_host(qmoe_layer* layer, const void* x_host, const float
 
 /*
  * Routing of the last forward (device pointers, any may be NULL), enqueued
- * on `stream`:
+ * on `stream`.  [qmoe.rs launch_route (route indices and weights) and
+ * launch_grouping (per-expert counts, offsets, grouped routes)]
  *   ids_dev     int32 [T*k]  selected experts, slot order (rank)
  *   weights_dev float32 [T*k]
  *   perm_dev    int32 [T*k]  routes grouped by expert, ascending r inside
@@ -256,8 +267,14 @@ int64_t qmoe_worklist_capacity(const qmoe_layer* layer, int which, int64_t num_t
  */
 qmoe_status qmoe_set_trace_events(qmoe_layer* layer, void* const* events, int n);
 
-/* Read (and clear) the device status word: QMOE_OK, or QMOE_ERR_TIMEOUT if
- * a bounded wait inside a kernel ran out.  Synchronises the device. */
+/* Read (and clear) the device status words: QMOE_OK, or QMOE_ERR_TIMEOUT if
+ * a bounded wait inside a kernel ran out -- in this layer's forwards, or in
+ * any qmoe_forward_noalloc call of this context since the last poll (that
+ * entry point's word is shared by all layers).  Synchronises the device.
+ * [qmoe.rs QMoEKernel::execute reports device-side failures when the eager
+ * pass synchronises its stream; the pages have no device status word, so
+ * this word, set by the bounded waits of these kernels, is the library's own
+ * counterpart of that report] */
 qmoe_status qmoe_poll_device_status(qmoe_layer* layer);
 
 /* The iteration limit of bounded device-side waits (0 = the default, about
@@ -274,31 +291,35 @@ qmoe_status qmoe_set_wait_limit(qmoe_layer* layer, int64_t iterations);
  * is a convenience of this library.)
  *
  * Who needs it: callers that may not call cudaMalloc at the moment they run
- * the layer -- e.g. code executing while a framework captures a CUDA graph in
- * a capture mode that forbids allocation, runtimes whose caching allocator
- * owns all device memory, or embedded deployments with a fixed memory plan.
- * qmoe_forward would allocate its workspace on first use (or when num_tokens
- * outgrows qmoe_reserve); this entry point instead uses one file-scope device
- * array of QMOE_NOALLOC_SCRATCH_BYTES that every GPU loading the library
- * holds until the process exits.  It never calls cudaMalloc, cudaFree or any
- * allocating library routine.
+ * the layer -- runtimes whose caching allocator owns all device memory (a
+ * cudaMalloc from a library beside it can fail or fragment that pool),
+ * embedded or safety-certified deployments with a fixed memory plan decided
+ * before start-up, and code that runs where an allocation would stall other
+ * work.  qmoe_forward would allocate its workspace on first use (or when
+ * num_tokens outgrows qmoe_reserve); this entry point instead uses one
+ * file-scope device array of QMOE_NOALLOC_SCRATCH_BYTES that every GPU
+ * loading the library holds until the process exits.  It never calls
+ * cudaMalloc, cudaFree or any allocating library routine.
  *
  * Arguments and layouts are those of qmoe_forward (x_dev, logits_dev,
  * out_dev are device pointers owned by the caller; x and out 16-byte
  * aligned).  The layer must already be prepacked.  Only the weight-streaming
- * decode kernels run (no grouped GEMM), so results equal qmoe_forward's
- * decode path.  Returns UNSUPPORTED (with the byte count in
- * qmoe_last_error) when num_tokens needs more scratch than the array holds;
- * use qmoe_forward for such sizes.
+ * decode kernels run (no grouped GEMM); the output matches qmoe_forward's
+ * within the output tolerance (not necessarily bit for bit).  Returns
+ * UNSUPPORTED (with the byte count in qmoe_last_error) when num_tokens needs
+ * more scratch than the array holds; use qmoe_forward for such sizes.
  *
- * Set-up: the first call on a device, with that device current, looks up the
- * array's device address (cudaGetSymbolAddress) and caches it; make that
- * first call before any stream capture.  All calls share the one array and it
- * keeps the last call's contents (each call clears its status word itself):
- * calls that overlap on the GPU (other streams, other layers) race and must
- * be serialised by the caller.  Bounded-wait timeouts of this entry point are
- * recorded in the scratch array, not in the layer (qmoe_poll_device_status
- * does not see them); routing of such a call is not kept for
+ * Set-up: the first call on a device (per CUDA context), with that device
+ * current, looks up the array's device address (cudaGetSymbolAddress) and
+ * caches it; a call in a new context (e.g. after cudaDeviceReset) looks it up
+ * again.  All calls share the one array and it keeps the last call's
+ * contents: calls that overlap on the GPU (other streams, other layers) race
+ * and must be serialised by the caller.
+ *
+ * Failures: a bounded device-side wait that runs out in this entry point sets
+ * a status word at the start of the array (shared by every layer); it stays
+ * set until qmoe_poll_device_status of any layer reads and clears it, which
+ * then returns QMOE_ERR_TIMEOUT.  Routing of such a call is not kept for
  * qmoe_get_routing.
  */
 qmoe_status qmoe_forward_noalloc(qmoe_layer* layer, const void* x_dev, const float* logits_dev,
@@ -320,7 +341,8 @@ const char* qmoe_last_error(const qmoe_layer* layer);
 /* Human-readable name of a status code. */
 const char* qmoe_status_string(qmoe_status status);
 
-/* Free every device buffer of the layer (synchronises the device). */
+/* Free every device buffer of the layer (synchronises the device).
+ * [qmoe.rs `impl Drop for QMoEKernel`: frees every scratch slot] */
 void qmoe_destroy(qmoe_layer* layer);
 
 #ifdef __cplusplus

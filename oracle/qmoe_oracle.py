@@ -23,7 +23,7 @@ in float64, written from these pages:
 * metrale ``gemm_quant_moe.rs``, ``moe_build_tile_worklist``: the tile
   work-list order (experts ascending, then m-tile, then n-tile).
 
-Readings where the pages leave a step open (also listed in the design notes):
+Readings where the pages leave a step open:
 selection is on the fp32 logits (equal to selection on the exact softmax,
 which is strictly increasing); fc1 rows are concatenated ``[gate | up]``;
 scales are stored in the activation type D; biases are fp32 (qmoe.rs);

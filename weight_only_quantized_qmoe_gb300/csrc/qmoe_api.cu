@@ -13,6 +13,8 @@
 #include <cstdio>
 #include <cstring>
 #include <mutex>
+
+#include <cuda.h>
 #include <string>
 
 #include "qmoe_internal.cuh"
@@ -95,6 +97,10 @@ struct qmoe_layer {
 };
 
 namespace {
+
+// Status word of qmoe_forward_noalloc's static array in the current context
+// (nullptr if that entry point has not run there); defined with the array.
+cudaError_t noalloc_status_word(void** out);
 
 qmoe_status fail(qmoe_layer* l, qmoe_status st, const std::string& msg) {
   if (l) l->err = msg;
@@ -799,11 +805,22 @@ qmoe_status qmoe_set_trace_events(qmoe_layer* l, void* const* events, int n) {
 
 qmoe_status qmoe_poll_device_status(qmoe_layer* l) {
   if (!l) return QMOE_ERR_INVALID_ARG;
-  if (!l->status) return QMOE_OK;
-  int h = 0;
+  // The layer's own status word and, once qmoe_forward_noalloc has run in
+  // this context, the one at the start of its static array.
+  int* words[2] = {l->status, nullptr};
+  void* na = nullptr;
+  QMOE_CUDA(l, noalloc_status_word(&na), "look up the static scratch array");
+  words[1] = static_cast<int*>(na);
+  if (!words[0] && !words[1]) return QMOE_OK;
   QMOE_CUDA(l, cudaDeviceSynchronize(), "synchronise");
-  QMOE_CUDA(l, cudaMemcpy(&h, l->status, sizeof(int), cudaMemcpyDeviceToHost), "read status");
-  QMOE_CUDA(l, cudaMemset(l->status, 0, sizeof(int)), "clear status");
+  int h = 0;
+  for (int* w : words) {
+    if (!w) continue;
+    int v = 0;
+    QMOE_CUDA(l, cudaMemcpy(&v, w, sizeof(int), cudaMemcpyDeviceToHost), "read status");
+    if (v != 0) QMOE_CUDA(l, cudaMemset(w, 0, sizeof(int)), "clear status");
+    if (v == DEV_TIMEOUT) h = DEV_TIMEOUT;
+  }
   if (h == DEV_TIMEOUT) return fail(l, QMOE_ERR_TIMEOUT, "a bounded device-side wait ran out");
   return QMOE_OK;
 }
@@ -851,21 +868,46 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[QMOE_NOALLOC_SC
 constexpr int kMaxDevices = 256;
 std::mutex g_noalloc_mu;
 void* g_noalloc_ptr[kMaxDevices] = {};
+CUcontext g_noalloc_ctx[kMaxDevices] = {};
+
+// The calling thread's current CUDA context, through the runtime's driver
+// entry-point lookup (the library does not link the driver library itself,
+// so it still loads on a machine without a GPU driver); nullptr if unknown.
+CUcontext current_context() {
+  using GetCurrent = CUresult (*)(CUcontext*);
+  static GetCurrent fn = [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 4000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      p = nullptr;
+    return reinterpret_cast<GetCurrent>(p);
+  }();
+  CUcontext ctx = nullptr;
+  if (!fn || fn(&ctx) != CUDA_SUCCESS) return nullptr;
+  return ctx;
+}
 
 // Device address of g_noalloc_scratch on the current device.  In host code
 // the array's name is only a host-side stand-in, so the address is looked up
-// once per device (with that device current) and cached.
-cudaError_t noalloc_scratch(void** out) {
+// (with that device current) once per device and CUDA context and cached; a
+// new context (after cudaDeviceReset, say) may place the array elsewhere.
+// `lookup` = false only reads the cache (nullptr if never looked up here).
+cudaError_t noalloc_scratch(void** out, bool lookup = true) {
+  *out = nullptr;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  CUcontext ctx = current_context();
   std::lock_guard<std::mutex> lock(g_noalloc_mu);
-  if (!g_noalloc_ptr[dev]) {
+  if (!g_noalloc_ptr[dev] || g_noalloc_ctx[dev] != ctx) {
+    if (!lookup) return cudaSuccess;
     void* p = nullptr;
     e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
     if (e != cudaSuccess) return e;
     g_noalloc_ptr[dev] = p;
+    g_noalloc_ctx[dev] = ctx;
   }
   *out = g_noalloc_ptr[dev];
   return cudaSuccess;
@@ -877,11 +919,23 @@ struct NoAllocPlan {
 
 size_t up256(size_t v) { return (v + 255) & ~size_t(255); }
 
+}  // namespace
+
+namespace {
+// The status word is the array's first int (offset 0 in every plan).
+cudaError_t noalloc_status_word(void** out) { return noalloc_scratch(out, false); }
+}  // namespace
+
+namespace {
+
 NoAllocPlan noalloc_plan(const qmoe_layer* l, int64_t T, int cap0) {
   const size_t R = (size_t)T * l->k;
   NoAllocPlan p;
   size_t o = 0;
   auto take = [&](size_t bytes) { const size_t at = o; o = up256(o + bytes); return at; };
+  // The status word sits at offset 0 whatever the token count, so a timeout
+  // stays readable (qmoe_poll_device_status) until it is polled.
+  p.status = take(sizeof(int));
   p.ids = take(R * sizeof(int));
   p.w = take(R * sizeof(float));
   p.counts = take((size_t)l->E * sizeof(int));
@@ -893,7 +947,6 @@ NoAllocPlan noalloc_plan(const qmoe_layer* l, int64_t T, int cap0) {
   p.items1 = take(sizeof(Item));
   p.hbuf = take(R * l->I * (size_t)l->dsize);
   p.ybuf = take(R * l->H * sizeof(float));
-  p.status = take(sizeof(int));
   p.total = o;
   return p;
 }
@@ -925,9 +978,9 @@ extern "C" qmoe_status qmoe_forward_noalloc(qmoe_layer* l, const void* x, const 
   QMOE_CUDA(l, noalloc_scratch(&base), "look up the static scratch array");
   unsigned char* sb = static_cast<unsigned char*>(base);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // The status word is zero when the library loads and is cleared only by
+  // qmoe_poll_device_status (a timeout stays visible until it is polled).
   int* status = reinterpret_cast<int*>(sb + plan.status);
-  // The array keeps the previous call's contents: the status word must start at zero.
-  QMOE_CUDA(l, cudaMemsetAsync(status, 0, sizeof(int), s), "clear status");
   int* ids = reinterpret_cast<int*>(sb + plan.ids);
   float* w = reinterpret_cast<float*>(sb + plan.w);
   int* perm = reinterpret_cast<int*>(sb + plan.perm);
@@ -1011,6 +1064,7 @@ extern "C" qmoe_status qmoe_forward_noalloc(qmoe_layer* l, const void* x, const 
       da.bf16 = l->dtype == QMOE_BF16;
       da.wait = wait;
       da.pdl = 1;
+      da.inject_stall = l->inject_stall;
       QMOE_CUDA(l, launch_decode_mma(da, s), "launch decode projection");
     }
   }
