@@ -84,13 +84,39 @@ def test_config_parity(qm, name, path):
     check_out(out, O.forward(inp), inp["cfg"].dtype)
 
 
-def test_prefill_config_sampled(qm):
+def stratified_tokens(rt, k, m_tile, seed=11):
+    """Tokens whose routes reach every (expert, m_tile-row tile) of the grouped
+    order: one random route per tile plus each expert's last (ragged) row.
+    Returns the sorted tokens and the set of all (expert, tile) pairs."""
+    rng = np.random.default_rng(seed)
+    offsets, perm = rt["offsets"], rt["perm"]
+    tokens, tiles = set(), set()
+    for e in range(len(offsets) - 1):
+        c = int(offsets[e + 1] - offsets[e])
+        for t0 in range(0, c, m_tile):
+            tiles.add((e, t0 // m_tile))
+            tokens.add(int(perm[offsets[e] + t0 + rng.integers(min(m_tile, c - t0))]) // k)
+        if c:
+            tokens.add(int(perm[offsets[e + 1] - 1]) // k)
+    return np.array(sorted(tokens)), tiles
+
+
+def test_prefill_config_every_tile(qm):
+    # Full-size prefill (T = 4096, 32768 routes, K = 4096): the oracle runs on
+    # a token set whose routes land in every (expert, 128-row m-tile) of the
+    # grouped GEMM, each expert's ragged last tile included.
     cfg = CONFIGS["prefill_int4"]
     inp = make_inputs(cfg)
     layer, out = run_layer(qm, inp)
-    check_routing(layer, inp)
-    rng = np.random.default_rng(11)
-    tokens = np.sort(rng.choice(cfg.T, size=12, replace=False))
+    rt = check_routing(layer, inp)
+    tokens, tiles = stratified_tokens(rt, cfg.k, 128)
+    covered = set()
+    for t in tokens:
+        for j in range(cfg.k):
+            r = t * cfg.k + j
+            e = int(rt["ids"][t, j])
+            covered.add((e, (int(rt["pos"][r]) - int(rt["offsets"][e])) // 128))
+    assert covered == tiles and len(tiles) == sum(-(-int(c) // 128) for c in rt["counts"])
     ref = O.forward(inp, tokens=tokens)
     check_out(out, ref, cfg.dtype, tokens)
 
