@@ -8,7 +8,9 @@ activation, fc2, weighted combine) over one batch of synthetic tokens.
 
 Default workload: the int2 GeGLU decode (T=8, hidden=inter=2048, E=8, top-2,
 block 128, fractional zero point 1.5, fp16), the shape of the pages' H100
-decode figure.  Each rank (torchrun, one GPU each) runs its own replica of
+decode figure.  The same line carries a `workloads` block with the
+many-expert int4 decode, the mixed int3/int4 decode and the int4 prefill,
+each with its µs per layer, tokens/s, roofline fraction and oracle baseline.  Each rank (torchrun, one GPU each) runs its own replica of
 the workload: the layer does not shard, so scaling is weak and no
 collective touches the data path.
 
@@ -31,12 +33,14 @@ sys.path.insert(0, ROOT)
 
 METRIC = "QMoE layer µs & tokens/s; % HBM roofline (decode), % tensor peak (prefill)"
 
-# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one fc1
-# gemm_kernel launch, from one ncu capture of the current kernel
-# (profiles/gemm_kernel_decode_int2_fc1.md, profiles/gemm_kernel_prefill_fc1.md);
-# None where no capture of the current kernel exists for the workload.
-FC1_TRAFFIC = {"decode_int2": 19_206_144, "prefill_int4": 802_950_656}
 L2_BYTES = 129 * 1024 * 1024
+# Every workload the line reports besides the headline one; the tiny case is
+# a parity case only.
+WORKLOADS = ["decode_int2", "decode_many_expert_int4", "mixed_int3_int4", "prefill_int4"]
+# DRAM traffic of a kernel is reported only from an ncu capture of the exact
+# sources being run: lines "<kernel> <workload> <sources sha256[:16]> <bytes
+# per launch>" in this file (written from the capture).
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.txt")
 
 
 def parse():
@@ -50,6 +54,10 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--gemm-min-rows", type=int, default=None,
                     help="experts with more rows take the tensor-core grouped GEMM")
+    ap.add_argument("--separate", action="store_true",
+                    help="run the separate kernels instead of the single-launch decode forward")
+    ap.add_argument("--only-headline", action="store_true",
+                    help="time only --workload (no `workloads` block)")
     return ap.parse_args()
 
 
@@ -152,97 +160,147 @@ def algorithmic_bytes(cfg, counts):
     active = int(sum(1 for c in counts if c > 0))
     R = cfg.T * cfg.k
     fc1 = active * expert_fc_bytes(cfg, 1) + cfg.T * cfg.H * ds + R * cfg.I * ds
+    fc2 = active * expert_fc_bytes(cfg, 2) + R * cfg.I * ds + cfg.T * cfg.H * ds
     layer = active * (expert_fc_bytes(cfg, 1) + expert_fc_bytes(cfg, 2)) + \
         cfg.T * cfg.H * ds * 2 + cfg.T * cfg.E * 4
-    return fc1, layer, active
+    return {"fc1": fc1, "fc2": fc2, "layer": layer, "active": active}
 
 
-def cpu_baseline(cfg_name, budget_s=20.0):
-    """Time the oracle (as it stands) on this host on a bounded sample."""
+def algorithmic_flops(cfg):
+    """Multiply-adds x 2 of the two projections over the T*k routed rows."""
+    R = cfg.T * cfg.k
+    n1 = 2 * cfg.I if cfg.act in ("swiglu", "geglu") else cfg.I
+    fc1 = 2.0 * R * cfg.H * n1
+    fc2 = 2.0 * R * cfg.I * cfg.H
+    return {"fc1": fc1, "fc2": fc2, "layer": fc1 + fc2}
+
+
+def sources_sha() -> str:
+    """sha256[:16] of the CUDA sources and the C header the library is built from."""
+    import hashlib
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "weight_only_quantized_qmoe_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)) + ["../../../include/qmoe.h"]:
+        path = os.path.normpath(os.path.join(csrc, f))
+        if os.path.isfile(path):
+            with open(path, "rb") as fh:
+                h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def measured_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch of `kernel` on `workload` from an ncu capture of
+    these exact sources, else None."""
+    if not os.path.exists(TRAFFIC_FILE):
+        return None
+    sha = sources_sha()
+    with open(TRAFFIC_FILE) as f:
+        for line in f:
+            parts = line.split()
+            if len(parts) == 4 and parts[0] == kernel and parts[1] == workload and parts[2] == sha:
+                return int(parts[3])
+    return None
+
+
+def oracle_sample_tokens(cfg, rt, max_experts=8):
+    """A bounded sample of tokens for the oracle: tokens in order until their
+    routes touch `max_experts` distinct experts (the oracle's cost is the
+    dequantisation of every expert it touches)."""
     import numpy as np
+    seen, tokens = set(), []
+    for t in range(cfg.T):
+        new = set(int(e) for e in rt["ids"][t])
+        if tokens and len(seen | new) > max_experts:
+            break
+        seen |= new
+        tokens.append(t)
+    return np.array(tokens)
+
+
+def time_oracle(cfg_name, runs=1):
+    """The oracle (as it stands) on this host on a bounded sample of the
+    workload: tokens/s, and the cores it actually kept busy (process CPU
+    time over wall time)."""
     from oracle import qmoe_oracle as O
     from qmoe_inputs import CONFIGS, make_inputs
     cfg = CONFIGS[cfg_name]
     inp = make_inputs(cfg)
-    T = cfg.T
-    tokens = np.arange(T) if T <= 64 else np.arange(0, T, max(1, T // 16))[:16]
-    t0 = time.perf_counter()
-    runs = 0
-    while True:
+    tokens = oracle_sample_tokens(cfg, O.routing(inp))
+    w0, c0 = time.perf_counter(), time.process_time()
+    for _ in range(runs):
         O.forward(inp, tokens=tokens)
-        runs += 1
-        if time.perf_counter() - t0 > budget_s / 4 or runs >= 3:
-            break
-    dt = (time.perf_counter() - t0) / runs
-    threads = os.environ.get("OMP_NUM_THREADS") or str(os.cpu_count())
-    return {"value": len(tokens) / dt, "unit": "tokens/s", "cores": int(threads),
-            "kind": "oracle",
-            "sample": f"{len(tokens)} of {T} tokens of {cfg_name}, mean of {runs} run(s), "
-                      f"{dt * 1e3:.0f} ms per run"}
+    wall, cpu = time.perf_counter() - w0, time.process_time() - c0
+    dt = wall / runs
+    return {"value": len(tokens) / dt, "unit": "tokens/s", "cores": max(1, round(cpu / wall)),
+            "cores_busy": round(cpu / wall, 2), "kind": "oracle",
+            "sample": f"{len(tokens)} of {cfg.T} tokens of {cfg_name} (routes touching <= 8 experts), "
+                      f"{runs} run(s), {dt * 1e3:.0f} ms per run"}
 
 
 def run_reference(args):
     rank, world, _ = dist_env()
     if rank != 0:
         return
-    import numpy as np
     from oracle import qmoe_oracle as O
     from qmoe_inputs import CONFIGS, make_inputs
     cfg = CONFIGS[args.workload]
     inp = make_inputs(cfg)
-    T = cfg.T
-    tokens = np.arange(T) if T <= 64 else np.arange(0, T, max(1, T // 16))[:16]
+    tokens = oracle_sample_tokens(cfg, O.routing(inp))
     for _ in range(args.warmup):
         O.forward(inp, tokens=tokens)
-    t0 = time.perf_counter()
+    w0, c0 = time.perf_counter(), time.process_time()
     for _ in range(args.steps):
         O.forward(inp, tokens=tokens)
-    dt = (time.perf_counter() - t0) / max(1, args.steps)
+    wall, cpu = time.perf_counter() - w0, time.process_time() - c0
+    dt = wall / max(1, args.steps)
     value = len(tokens) / dt
-    threads = int(os.environ.get("OMP_NUM_THREADS") or os.cpu_count())
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic", "impl": "reference",
         "config": {"workload": cfg.name, "tokens_per_step": len(tokens)},
-        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads, "kind": "oracle",
-                         "sample": f"{len(tokens)} of {T} tokens per step"},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": max(1, round(cpu / wall)),
+                         "kind": "oracle",
+                         "sample": f"{len(tokens)} of {cfg.T} tokens per step (routes touching <= 8 experts)"},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
 
 
-def run_ours(args):
+PATH_NAMES = {1: "separate kernels", 2: "single launch"}
+
+
+def launches_per_step(cfg, path, min_rows):
+    """Kernels one forward launches: the single launch, or the separate
+    sequence -- routing (fused with grouping for T <= 64, else route +
+    group), the x gather and one GEMM per projection when the grouped GEMM
+    runs, one decode-class kernel per projection when any expert can take
+    that class, and the combine."""
+    if path == 2:
+        return 1
+    gemm_on = cfg.dtype != "f32" and cfg.T > min_rows
+    decode_on = not gemm_on or min_rows > 0
+    return (1 if cfg.T <= 64 else 2) + (3 if gemm_on else 0) + (2 if decode_on else 0) + 1
+
+
+def measure(q, cfg, args, dev, stream, flush, steps, warmup, fused=1, min_rows=0):
+    """Time one workload: graph-replayed (or eager) forwards with the L2
+    flushed before each, CUDA events on the launching stream around each
+    step; a separate traced pass for the per-stage times of the separate
+    kernels; the host-buffer entry point end to end."""
     import torch
-    import torch.distributed as dist
-
-    rank, world, local = dist_env()
-    if world > 1:
-        dist.init_process_group("nccl")
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
-
-    import weight_only_quantized_qmoe_gb300 as q
-    from weight_only_quantized_qmoe_gb300 import build as qb
-    from qmoe_inputs import CONFIGS, DTYPES, make_inputs
-    qb.build()
-
-    cfg = CONFIGS[args.workload]
+    from qmoe_inputs import DTYPES, make_inputs
     inp = make_inputs(cfg)
     layer = q.QMoELayer.from_config(cfg)
-    if args.gemm_min_rows is not None:
-        layer.set_gemm_min_rows(args.gemm_min_rows)
+    layer.set_fused_decode(fused)
+    layer.set_gemm_min_rows(min_rows)
     layer.reserve(cfg.T)
     x, logits = q.load_inputs(layer, inp, device=dev)
     out = torch.empty_like(x)
-    stream = torch.cuda.Stream(device=dev)
-    flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
 
     def make_step(traced):
-        """A step callable: the forward replayed from a CUDA graph (or eager),
-        with the library's stage events recorded inside it when `traced`."""
         ev = [torch.cuda.Event(enable_timing=True) for _ in range(q.QMOE_TRACE_NUM_EVENTS)]
         layer.set_trace_events(ev if traced else None)
         with torch.cuda.stream(stream):
@@ -262,27 +320,20 @@ def run_ours(args):
                 layer.forward(x, logits, out, stream=stream)
         return step, ev
 
-    # Timed steps: no events inside the forward (recording them between the
-    # kernels would break their programmatic launch overlap); one pair of
-    # events on the launching stream brackets each step.
+    # Timed steps: no events inside the forward (between the separate kernels
+    # they would break the programmatic launch overlap).
     step, _ = make_step(False)
+    path = layer.last_path()
     with torch.cuda.stream(stream):
-        for _ in range(max(3, args.warmup)):
+        for _ in range(max(3, warmup)):
             flush.zero_()
             step()
-    torch.cuda.synchronize()
-
-    clocks = ClockSampler(local)
-    clocks.start()
-    time.sleep(0.3)
-    if world > 1:
-        dist.barrier()
     torch.cuda.synchronize()
     per_step = []
     t_beg = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
     with torch.cuda.stream(stream):
-        for _ in range(args.steps):
+        for _ in range(steps):
             flush.zero_()                      # L2 flush between timed iterations
             t_beg.record(stream)
             step()
@@ -290,86 +341,147 @@ def run_ours(args):
             stream.synchronize()
             per_step.append(t_beg.elapsed_time(t_end))
     torch.cuda.synchronize()
-    if world > 1:
-        dist.barrier()
-    clk = clocks.stop()
 
-    # Stage breakdown (and fc1's time for the roofline) from a separate pass
-    # with the library's stage events inside the forward.
-    tstep, ev = make_step(True)
-    stage_ms = [[] for _ in range(q.QMOE_TRACE_NUM_EVENTS - 1)]
-    with torch.cuda.stream(stream):
-        for i in range(max(3, args.warmup) + max(5, args.steps // 2)):
-            flush.zero_()
-            tstep()
-            stream.synchronize()
-            if i >= max(3, args.warmup):
-                for j in range(len(stage_ms)):
-                    stage_ms[j].append(ev[j].elapsed_time(ev[j + 1]))
-    torch.cuda.synchronize()
+    stages = None
+    if path == 1:
+        tstep, ev = make_step(True)
+        stage_ms = [[] for _ in range(q.QMOE_TRACE_NUM_EVENTS - 1)]
+        with torch.cuda.stream(stream):
+            for i in range(3 + max(5, steps // 2)):
+                flush.zero_()
+                tstep()
+                stream.synchronize()
+                if i >= 3:
+                    for j in range(len(stage_ms)):
+                        stage_ms[j].append(ev[j].elapsed_time(ev[j + 1]))
+        torch.cuda.synchronize()
+        stages = {n: statistics.mean(v) * 1e3 for n, v in
+                  zip(["route_group", "fc1", "fc2", "combine"], stage_ms)}
+    layer.set_trace_events(None)
     status = layer.poll()
     if status != 0:
-        # a bounded device-side wait ran out: the timings are not valid
-        print(json.dumps({"error": f"device status {status} after the timed steps"}), file=sys.stderr)
+        print(json.dumps({"error": f"{cfg.name}: device status {status} after the timed steps"}), file=sys.stderr)
         sys.exit(1)
 
-    ms = max_over_ranks(sum(per_step) / len(per_step), dev)
-    value = job_throughput(cfg.T, world, ms)
-
-    # Routing of the run: distinct experts -> algorithmic bytes.
     _, _, _, offs = layer.routing(cfg.T, stream=None)
     torch.cuda.synchronize()
     o = offs.cpu().tolist()
     counts = [o[i + 1] - o[i] for i in range(cfg.E)]
-    fc1_bytes, layer_bytes, active = algorithmic_bytes(cfg, counts)
-    fc1_stage = statistics.mean(stage_ms[1])
-    hbm_peak, bf16_peak, peak_kind = measured_peaks()
-    min_rows = args.gemm_min_rows if args.gemm_min_rows is not None else 0
-    # fc1's roofline: the larger of its HBM time (algorithmic bytes at the
-    # measured copy bandwidth) and its tensor time (2 * R * H * 2I FLOPs at
-    # the measured bf16 peak) decides what bounds it.
-    fc1_flops = 2.0 * cfg.T * cfg.k * cfg.H * 2 * cfg.I
-    # counters taken on the default path only (every expert on the GEMM)
-    traffic = FC1_TRAFFIC.get(cfg.name) if (min_rows == 0 and cfg.dtype != "f32") else None
-    if fc1_flops / (bf16_peak * 1e12) > fc1_bytes / (hbm_peak * 1e9):
-        achieved_t = fc1_flops / (fc1_stage * 1e-3) / 1e12
-        roofline = {"bound": "tensor", "achieved": achieved_t, "peak": bf16_peak, "unit": "TFLOP/s",
-                    "frac": achieved_t / bf16_peak, "traffic": traffic,
-                    "kernel": "fc1 (gemm_kernel, tcgen05 grouped GEMM)", "flops_per_launch": fc1_flops,
-                    "peak_kind": peak_kind + " bf16 burst"}
-    else:
-        achieved = fc1_bytes / (fc1_stage * 1e-3) / 1e9
-        roofline = {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
-                    "frac": achieved / hbm_peak, "traffic": traffic,
-                    "kernel": "fc1 (gemm_kernel)" if cfg.T > min_rows and cfg.dtype != "f32"
-                    else "fc1 (decode_mma_kernel)", "bytes_per_launch": fc1_bytes,
-                    "peak_kind": peak_kind}
 
-    # End-to-end through the public host-buffer entry point (pinned memory).
+    # end to end through the host-buffer entry point (pinned memory)
     ds = torch.tensor([], dtype=DTYPES[cfg.dtype]).element_size()
     xh = inp["x"].pin_memory()
     lh = inp["logits"].pin_memory()
     oh = torch.empty_like(xh).pin_memory()
-    layer.set_trace_events(None)
     for _ in range(3):
         layer.forward_host(xh, lh, oh, stream=stream)
     e2e_ms = []
-    for _ in range(args.steps):
+    for _ in range(steps):
         flush.zero_()
         torch.cuda.synchronize()
         t0 = time.perf_counter()
         layer.forward_host(xh, lh, oh, stream=stream)
         e2e_ms.append((time.perf_counter() - t0) * 1e3)
-    e2e = max_over_ranks(statistics.mean(e2e_ms), dev)
+    layer.close()
+    return {"ms": statistics.mean(per_step), "ms_median": statistics.median(per_step), "path": path,
+            "stages_us": stages, "counts": counts, "e2e_ms": statistics.mean(e2e_ms),
+            "h2d": cfg.T * cfg.H * ds + cfg.T * cfg.E * 4, "d2h": cfg.T * cfg.H * ds}
 
-    # Kernels one forward launches (the library's launch sequence): routing
-    # (fused with grouping for T <= 64, else route + group), the x gather and
-    # one GEMM per projection when the grouped GEMM runs, one decode-class
-    # kernel per projection when any expert can take that class (a positive
-    # threshold, or fp32 / T below it), and the combine.
-    gemm_on = cfg.dtype != "f32" and cfg.T > min_rows
-    decode_on = not gemm_on or min_rows > 0
-    launches_per_step = ((1 if cfg.T <= 64 else 2) + (3 if gemm_on else 0) + (2 if decode_on else 0) + 1)
+
+def roofline_of(cfg, m, hbm_peak, bf16_peak, peak_kind):
+    """Roofline of the dominant kernel of a measured workload.
+
+    Single launch: the one kernel is the whole layer (time = the timed step).
+    Separate kernels: fc1's grouped GEMM (or decode kernel), timed by the
+    traced pass.  Each takes the bound whose floor is larger: HBM (algorithmic
+    bytes at the measured copy bandwidth) or tensor (FLOPs at the measured
+    bf16 peak)."""
+    by = algorithmic_bytes(cfg, m["counts"])
+    fl = algorithmic_flops(cfg)
+    if m["path"] == 2:
+        kernel, bytes_, flops_, ms, tkey = "fused_decode_kernel (single launch)", by["layer"], fl["layer"], m["ms"], \
+            "fused_decode_kernel"
+    else:
+        kernel, bytes_, flops_ = "fc1 gemm_kernel (tcgen05 grouped GEMM)", by["fc1"], fl["fc1"]
+        ms, tkey = m["stages_us"]["fc1"] * 1e-3, "gemm_kernel_fc1"
+    if flops_ / (bf16_peak * 1e12) > bytes_ / (hbm_peak * 1e9):
+        ach = flops_ / (ms * 1e-3) / 1e12
+        r = {"bound": "tensor", "achieved": ach, "peak": bf16_peak, "unit": "TFLOP/s", "frac": ach / bf16_peak,
+             "flops_per_launch": flops_, "peak_kind": peak_kind + " bf16 burst"}
+    else:
+        ach = bytes_ / (ms * 1e-3) / 1e9
+        r = {"bound": "hbm", "achieved": ach, "peak": hbm_peak, "unit": "GB/s", "frac": ach / hbm_peak,
+             "bytes_per_launch": bytes_, "peak_kind": peak_kind}
+    r["traffic"] = measured_traffic(tkey, cfg.name)
+    r["kernel"] = kernel
+    r["launch_us"] = ms * 1e3
+    return r, by, fl
+
+
+def workload_summary(cfg, m, hbm_peak, bf16_peak, peak_kind, world):
+    roof, by, fl = roofline_of(cfg, m, hbm_peak, bf16_peak, peak_kind)
+    d = {"us_per_layer": m["ms"] * 1e3, "tokens_per_s": job_throughput(cfg.T, world, m["ms"]),
+         "path": PATH_NAMES.get(m["path"], "?"), "active_experts": by["active"],
+         "layer_bytes": by["layer"], "layer_flops": fl["layer"],
+         "layer_hbm_frac": by["layer"] / (m["ms"] * 1e-3) / 1e9 / hbm_peak,
+         "layer_tensor_frac": fl["layer"] / (m["ms"] * 1e-3) / 1e12 / bf16_peak,
+         "roofline": roof,
+         "e2e_tokens_per_s": job_throughput(cfg.T, world, m["e2e_ms"])}
+    if m["stages_us"]:
+        st = m["stages_us"]
+        d["stage_us_traced"] = st
+        d["fc1_frac"] = (fl["fc1"] / (st["fc1"] * 1e-6) / 1e12 / bf16_peak if cfg.T > 64 else
+                         by["fc1"] / (st["fc1"] * 1e-6) / 1e9 / hbm_peak)
+        d["fc2_frac"] = (fl["fc2"] / (st["fc2"] * 1e-6) / 1e12 / bf16_peak if cfg.T > 64 else
+                         by["fc2"] / (st["fc2"] * 1e-6) / 1e9 / hbm_peak)
+    return d
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    rank, world, local = dist_env()
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    import weight_only_quantized_qmoe_gb300 as q
+    from weight_only_quantized_qmoe_gb300 import build as qb
+    from qmoe_inputs import CONFIGS
+    qb.build()
+
+    cfg = CONFIGS[args.workload]
+    stream = torch.cuda.Stream(device=dev)
+    flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
+    hbm_peak, bf16_peak, peak_kind = measured_peaks()
+    fused = 0 if args.separate else 1
+    min_rows = args.gemm_min_rows if args.gemm_min_rows is not None else 0
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    head = measure(q, cfg, args, dev, stream, flush, args.steps, args.warmup, fused, min_rows)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    others = {}
+    if not args.only_headline:
+        for name in WORKLOADS:
+            if name == cfg.name:
+                continue
+            others[name] = measure(q, CONFIGS[name], args, dev, stream, flush, max(10, args.steps // 2),
+                                   args.warmup, fused, min_rows)
+    clk = clocks.stop()
+
+    ms = max_over_ranks(head["ms"], dev)
+    value = job_throughput(cfg.T, world, ms)
+    roof, by, fl = roofline_of(cfg, head, hbm_peak, bf16_peak, peak_kind)
+    e2e = max_over_ranks(head["e2e_ms"], dev)
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
@@ -379,23 +491,31 @@ def run_ours(args):
                    "experts": cfg.E, "top_k": cfg.k, "bits": [cfg.bits1, cfg.bits2],
                    "block_size": cfg.B, "zp": cfg.zp_mode, "act": cfg.act,
                    "mode": args.mode, "l2": "flushed between timed steps (258 MB write)",
-                   "us_per_layer": ms * 1e3, "active_experts": active,
-                   "stage_us_traced": {n: statistics.mean(v) * 1e3 for n, v in
-                                       zip(["route_group", "fc1", "fc2", "combine"], stage_ms)},
-                   "layer_bytes": layer_bytes,
-                   "layer_hbm_frac": layer_bytes / (ms * 1e-3) / 1e9 / hbm_peak},
-        "roofline": roofline,
+                   "path": PATH_NAMES.get(head["path"], "?"),
+                   "us_per_layer": ms * 1e3, "active_experts": by["active"],
+                   "layer_bytes": by["layer"],
+                   "layer_hbm_frac": by["layer"] / (ms * 1e-3) / 1e9 / hbm_peak},
+        "roofline": roof,
         "clocks": clk,
         "e2e": {"value": job_throughput(cfg.T, world, e2e), "unit": "tokens/s",
-                "h2d_bytes_per_step": cfg.T * cfg.H * ds + cfg.T * cfg.E * 4,
-                "d2h_bytes_per_step": cfg.T * cfg.H * ds},
-        "gpu_launches": launches_per_step * args.steps,
+                "h2d_bytes_per_step": head["h2d"], "d2h_bytes_per_step": head["d2h"]},
+        "gpu_launches": launches_per_step(cfg, head["path"], min_rows) * args.steps,
     }
+    if head["stages_us"]:
+        line["config"]["stage_us_traced"] = head["stages_us"]
+    if others or not args.only_headline:
+        wl = {cfg.name: workload_summary(cfg, head, hbm_peak, bf16_peak, peak_kind, world)}
+        for name, m in others.items():
+            wl[name] = workload_summary(CONFIGS[name], m, hbm_peak, bf16_peak, peak_kind, world)
+        line["workloads"] = wl
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(args.workload)
+        line["cpu_baseline"] = time_oracle(cfg.name)
+        if "workloads" in line:
+            for name in line["workloads"]:
+                line["workloads"][name]["cpu_baseline"] = (line["cpu_baseline"] if name == cfg.name
+                                                           else time_oracle(name))
     if rank == 0:
         print(json.dumps(line), flush=True)
-    layer.close()
     if world > 1:
         dist.destroy_process_group()
 

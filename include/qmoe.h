@@ -177,6 +177,26 @@ qmoe_status qmoe_set_bias(qmoe_layer* layer, int fc, const float* bias_dev, void
  * PR "fast INT3" kMaxProfiledExpandedRows] */
 qmoe_status qmoe_set_gemm_min_rows(qmoe_layer* layer, int min_rows);
 
+/* The single-launch decode forward (1) or the separate kernels (0,
+ * default).  When it applies -- 16-bit activations, at most 64 tokens, E <= 256,
+ * k <= 32, T*k <= 512, fc1 and fc2 code widths in {2, 3, 4} -- qmoe_forward
+ * runs routing, grouping, fc1 with its activation, fc2 and the slot-ordered
+ * combine in one persistent kernel launch; otherwise, or when disabled, the
+ * separate kernels run (qmoe_set_gemm_min_rows picks between their
+ * projection paths).  Either gives the same result within tolerance; the
+ * single launch is bitwise deterministic.  [The pages motivate the fusion:
+ * PR "fast INT3 QMoE kernels", single-CTA FusedSoftmaxTopKMapsKernel for up
+ * to 8 rows and the fused finalize of moe_gemv; ferrum moe.rs
+ * SingleTokenDirectMarlin.] */
+qmoe_status qmoe_set_fused_decode(qmoe_layer* layer, int enable);
+
+/* Which launch sequence the last qmoe_forward / qmoe_forward_host used:
+ * QMOE_PATH_NONE (no forward with tokens yet), QMOE_PATH_SEPARATE (routing,
+ * projection and combine kernels) or QMOE_PATH_FUSED (the single launch).
+ * For tests and benchmarks that must know what they measured. */
+enum { QMOE_PATH_NONE = 0, QMOE_PATH_SEPARATE = 1, QMOE_PATH_FUSED = 2 };
+int qmoe_last_forward_path(const qmoe_layer* layer);
+
 /* Size the device workspace for up to max_tokens tokens.  Required before
  * capturing qmoe_forward into a CUDA graph.  Allocates device memory.
  * [qmoe.rs QMoEKernel scratch pool (`slots`): a warmed eager pass sizes the

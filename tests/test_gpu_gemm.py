@@ -1,15 +1,15 @@
 """Parity of the tensor-core grouped GEMM path (tcgen05, A = dequantised
 weights in TMEM, B = routed token rows) with the CPU oracle.  Setting the
 GEMM threshold to 0 sends every expert with rows to it, so small shapes cover
-the variant matrix; the prefill workload runs at full size in
-test_gpu_parity.py."""
+the variant matrix (with the single-launch decode forward switched off); the
+prefill workload runs at full size in test_gpu_parity.py."""
 import numpy as np
 import pytest
 import torch
 
 from oracle import qmoe_oracle as O
 from qmoe_inputs import CONFIGS, make_inputs
-from test_gpu_parity import check_out, check_routing, run_layer
+from test_gpu_parity import check_out, check_routing, run_layer, separate_path
 
 pytestmark = pytest.mark.gpu
 
@@ -43,8 +43,8 @@ GEMM_VARIANTS = {
 def test_gemm_variant_parity(qm, name):
     cfg = BASE.with_(**GEMM_VARIANTS[name])
     inp = make_inputs(cfg)
-    layer, out = run_layer(qm, inp, min_rows=0)
-    check_routing(layer, inp, min_rows=0)
+    layer, out = run_layer(qm, inp, path="gemm")
+    check_routing(layer, inp, path="gemm")
     items, m_tile = layer.worklist(1, cfg.T)
     assert m_tile == 128 and len(items) > 0
     check_out(out, O.forward(inp), cfg.dtype)
@@ -54,8 +54,8 @@ def test_gemm_and_decode_classes_agree(qm):
     # The same forward through the decode kernel only and the GEMM only.
     cfg = BASE.with_(T=48, E=4, k=2)
     inp = make_inputs(cfg)
-    _, out_dec = run_layer(qm, inp, min_rows=10 ** 6)
-    _, out_gemm = run_layer(qm, inp, min_rows=0)
+    _, out_dec = run_layer(qm, inp, path="decode")
+    _, out_gemm = run_layer(qm, inp, path="gemm")
     ref = O.forward(inp)
     check_out(out_dec, ref, cfg.dtype)
     check_out(out_gemm, ref, cfg.dtype)
@@ -65,7 +65,7 @@ def test_mixed_classes_in_one_forward(qm):
     # Skewed routing: some experts above, some below the threshold.
     cfg = BASE.with_(T=200, E=16, k=2, zipf_bias=1.5)
     inp = make_inputs(cfg)
-    layer, out = run_layer(qm, inp, min_rows=24)
-    rt = check_routing(layer, inp, min_rows=24)
+    layer, out = run_layer(qm, inp, path=separate_path(24))
+    rt = check_routing(layer, inp, path=separate_path(24))
     assert (rt["counts"] > 24).any() and ((rt["counts"] > 0) & (rt["counts"] <= 24)).any()
     check_out(out, O.forward(inp), cfg.dtype)

@@ -21,11 +21,24 @@ def qm():
     return q
 
 
-def run_layer(qm, inp, reserve=None, min_rows=None):
+# The projection paths: the single launch (default; it serves 16-bit
+# activations, <= 64 tokens and code widths {2, 3, 4}, the separate kernels
+# otherwise), and with it switched off the tensor-core grouped GEMM for every
+# expert or the mma.sync decode kernel (threshold above any expert's rows).
+PATHS = {"fused": (1, 0), "gemm": (0, 0), "decode": (0, 10 ** 6)}
+
+
+def separate_path(min_rows):
+    """The separate kernels with experts above `min_rows` rows on the GEMM."""
+    return (0, min_rows)
+
+
+def run_layer(qm, inp, reserve=None, path="fused"):
     cfg = inp["cfg"]
     layer = qm.QMoELayer.from_config(cfg)
-    if min_rows is not None:
-        layer.set_gemm_min_rows(min_rows)
+    fused, min_rows = PATHS.get(path, path)
+    layer.set_fused_decode(fused)
+    layer.set_gemm_min_rows(min_rows)
     if reserve:
         layer.reserve(reserve)
     x, logits = qm.load_inputs(layer, inp)
@@ -35,7 +48,8 @@ def run_layer(qm, inp, reserve=None, min_rows=None):
     return layer, out
 
 
-def check_routing(layer, inp, min_rows=0):
+def check_routing(layer, inp, path="fused"):
+    from weight_only_quantized_qmoe_gb300 import binding
     cfg = inp["cfg"]
     ids, w, perm, offs = layer.routing(cfg.T)
     torch.cuda.synchronize()
@@ -45,9 +59,14 @@ def check_routing(layer, inp, min_rows=0):
     np.testing.assert_array_equal(offs.cpu().numpy(), rt["offsets"])
     np.testing.assert_allclose(w.cpu().numpy().reshape(cfg.T, cfg.k), rt["weights"],
                                rtol=2e-6, atol=1e-7)
-    # Work-lists: experts with more than `min_rows` rows go to the grouped GEMM
-    # (class 1) once T can exceed it; the rest to the decode kernel (class 0).
-    thr = min_rows if (cfg.dtype != "f32" and cfg.T > min_rows) else None
+    min_rows = PATHS.get(path, path)[1]
+    if layer.last_path() == binding.QMOE_PATH_FUSED:
+        # the single launch: every expert's rows in groups of m_tile, no GEMM class
+        thr = 10 ** 9
+    else:
+        # experts with more than `min_rows` rows go to the grouped GEMM
+        # (class 1) once T can exceed it; the rest to the decode kernel (class 0)
+        thr = min_rows if (cfg.dtype != "f32" and cfg.T > min_rows) else None
     for which in (0, 1):
         items, m_tile = layer.worklist(which, cfg.T)
         if thr is None:
@@ -70,17 +89,12 @@ def check_out(out, ref, dtype, tokens=None):
     return err, tol
 
 
-# Both projection paths: the default (tensor-core grouped GEMM for every
-# expert) and the mma.sync decode kernel (threshold above any expert's rows).
-PATHS = {"gemm": 0, "decode": 10 ** 6}
-
-
 @pytest.mark.parametrize("path", sorted(PATHS))
 @pytest.mark.parametrize("name", ["tiny", "decode_int2", "decode_many_expert_int4", "mixed_int3_int4"])
 def test_config_parity(qm, name, path):
     inp = make_inputs(CONFIGS[name])
-    layer, out = run_layer(qm, inp, min_rows=PATHS[path])
-    check_routing(layer, inp, min_rows=PATHS[path])
+    layer, out = run_layer(qm, inp, path=path)
+    check_routing(layer, inp, path=path)
     check_out(out, O.forward(inp), inp["cfg"].dtype)
 
 
@@ -189,8 +203,8 @@ FEATURE_VARIANTS = {
 def test_feature_parity(qm, name, path):
     cfg = BASE.with_(**FEATURE_VARIANTS[name])
     inp = make_inputs(cfg)
-    layer, out = run_layer(qm, inp, min_rows=PATHS[path])
-    check_routing(layer, inp, min_rows=PATHS[path])
+    layer, out = run_layer(qm, inp, path=path)
+    check_routing(layer, inp, path=path)
     check_out(out, O.forward(inp), cfg.dtype)
 
 
@@ -248,8 +262,8 @@ WIDTH_CASES.update({
 def test_width_matrix_parity(qm, name, path):
     cfg = BASE.with_(**WIDTH_CASES[name])
     inp = make_inputs(cfg)
-    layer, out = run_layer(qm, inp, min_rows=PATHS[path])
-    check_routing(layer, inp, min_rows=PATHS[path])
+    layer, out = run_layer(qm, inp, path=path)
+    check_routing(layer, inp, path=path)
     check_out(out, O.forward(inp), cfg.dtype)
 
 
@@ -263,8 +277,8 @@ def test_block32_int2_decode_parity(qm, widths, T, path):
     cfg = BASE.with_(bits1=widths[0], bits2=widths[1], B=32, E=64, k=10, T=T, H=256, I=256,
                      scale_lo=0.02, scale_hi=0.08)
     inp = make_inputs(cfg)
-    layer, out = run_layer(qm, inp, min_rows=PATHS[path])
-    check_routing(layer, inp, min_rows=PATHS[path])
+    layer, out = run_layer(qm, inp, path=path)
+    check_routing(layer, inp, path=path)
     check_out(out, O.forward(inp), cfg.dtype)
 
 
@@ -321,7 +335,8 @@ def test_graph_capture_replay_matches_eager(qm, path):
     cfg = CONFIGS["decode_int2"]
     inp = make_inputs(cfg)
     layer = qm.QMoELayer.from_config(cfg)
-    layer.set_gemm_min_rows(PATHS[path])
+    layer.set_fused_decode(PATHS[path][0])
+    layer.set_gemm_min_rows(PATHS[path][1])
     layer.reserve(cfg.T)
     x, logits = qm.load_inputs(layer, inp)
     eager = layer.forward(x, logits).clone()
@@ -337,7 +352,7 @@ def test_graph_capture_replay_matches_eager(qm, path):
     out.zero_()
     g.replay()
     torch.cuda.synchronize()
-    if path == "decode":
+    if path != "gemm":
         assert torch.equal(out, eager)               # slot-ordered combine: bitwise deterministic
     else:
         # fp32 reductions into the combine accumulator: the order of the k
@@ -366,7 +381,8 @@ def test_forward_host_matches_device(qm, path):
     cfg = CONFIGS["decode_many_expert_int4"]
     inp = make_inputs(cfg)
     layer = qm.QMoELayer.from_config(cfg)
-    layer.set_gemm_min_rows(PATHS[path])
+    layer.set_fused_decode(PATHS[path][0])
+    layer.set_gemm_min_rows(PATHS[path][1])
     layer.reserve(cfg.T)
     x, logits = qm.load_inputs(layer, inp)
     dev = layer.forward(x, logits)
@@ -375,7 +391,7 @@ def test_forward_host_matches_device(qm, path):
     oh = torch.empty_like(xh).pin_memory()
     layer.forward_host(xh, lh, oh)
     torch.cuda.synchronize()
-    if path == "decode":
+    if path != "gemm":
         assert torch.equal(oh, dev.cpu())            # slot-ordered combine: bitwise deterministic
     else:
         # fp32 reductions into the combine accumulator: slot order may differ
@@ -387,13 +403,15 @@ def test_forward_host_matches_device(qm, path):
 def test_bounded_wait_reports_timeout_and_context_survives(qm, path):
     # Host-injected failure: the first copy stage of every decode warp (or of
     # every grouped-GEMM CTA) is armed but never issued, so the bounded waits
-    # on it run out.  The kernel records QMOE_ERR_TIMEOUT, drains its real
+    # on it run out; in the single launch every fc2 item waits on a flag that
+    # nothing sets.  The kernel records QMOE_ERR_TIMEOUT, drains its real
     # copies and returns; the context stays usable and the next forward is
     # correct.
     cfg = BASE.with_(T=4)
     inp = make_inputs(cfg)
     layer = qm.QMoELayer.from_config(cfg)
-    layer.set_gemm_min_rows(PATHS[path])
+    layer.set_fused_decode(PATHS[path][0])
+    layer.set_gemm_min_rows(PATHS[path][1])
     x, logits = qm.load_inputs(layer, inp)
     layer.set_wait_limit(2000)
     layer.inject_stall(True)

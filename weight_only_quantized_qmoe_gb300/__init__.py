@@ -98,6 +98,14 @@ class QMoELayer:
     def set_gemm_min_rows(self, n):
         self._check(binding.qmoe_set_gemm_min_rows(self.handle, n))
 
+    def set_fused_decode(self, enable):
+        self._check(binding.qmoe_set_fused_decode(self.handle, enable))
+
+    def last_path(self):
+        """QMOE_PATH_SEPARATE or QMOE_PATH_FUSED: the launch sequence of the
+        last forward (QMOE_PATH_NONE before any)."""
+        return binding.qmoe_last_forward_path(self.handle)
+
     def prepack(self, fc, codes, scales, zp=None, stream=None):
         self._check(binding.qmoe_prepack(self.handle, fc, _ptr(codes), _ptr(scales), _ptr(zp),
                                          _stream(stream)))

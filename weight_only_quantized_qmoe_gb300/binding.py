@@ -25,6 +25,7 @@ QMOE_ACT_RELU, QMOE_ACT_GELU_TANH, QMOE_ACT_SILU, QMOE_ACT_IDENTITY = 2, 3, 4, 5
 QMOE_FC1_CONCAT, QMOE_FC1_INTERLEAVED, QMOE_FC1_SEPARATE_FC3 = 0, 1, 2
 QMOE_F32, QMOE_F16, QMOE_BF16 = 0, 1, 2
 QMOE_TRACE_NUM_EVENTS = 5
+QMOE_PATH_NONE, QMOE_PATH_SEPARATE, QMOE_PATH_FUSED = 0, 1, 2
 
 _p = ctypes.c_void_p
 _i = ctypes.c_int
@@ -34,6 +35,8 @@ _SIGS = {
     "qmoe_set_routing": (_i, [_p, _i]),
     "qmoe_set_zero_point_offset": (_i, [_p, ctypes.c_float]),
     "qmoe_set_gemm_min_rows": (_i, [_p, _i]),
+    "qmoe_set_fused_decode": (_i, [_p, _i]),
+    "qmoe_last_forward_path": (_i, [_p]),
     "qmoe_set_swiglu_params": (_i, [_p, ctypes.c_float, ctypes.c_float, ctypes.c_float]),
     "qmoe_set_fc1_layout": (_i, [_p, _i]),
     "qmoe_set_bias": (_i, [_p, _i, _p, _p]),
@@ -101,6 +104,14 @@ def qmoe_set_zero_point_offset(layer, offset):
 
 def qmoe_set_gemm_min_rows(layer, min_rows):
     return load().qmoe_set_gemm_min_rows(layer, int(min_rows))
+
+
+def qmoe_set_fused_decode(layer, enable):
+    return load().qmoe_set_fused_decode(layer, int(enable))
+
+
+def qmoe_last_forward_path(layer):
+    return load().qmoe_last_forward_path(layer)
 
 
 def qmoe_set_swiglu_params(layer, alpha, beta, limit):

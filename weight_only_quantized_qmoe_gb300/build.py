@@ -17,7 +17,9 @@ INCLUDE = os.path.join(ROOT, "include")
 LIB_PATH = os.path.join(HERE, "libqmoe.so")
 SOURCES = ["qmoe_api.cu", "qmoe_route.cu", "qmoe_decode.cu", "qmoe_prefill.cu", "qmoe_decode_b2.cu",
            "qmoe_decode_b3.cu", "qmoe_decode_b4.cu", "qmoe_decode_b8.cu",
-           "qmoe_decode_b1.cu"]
+           "qmoe_decode_b1.cu", "qmoe_fused.cu", "qmoe_fused_w22.cu", "qmoe_fused_w23.cu",
+           "qmoe_fused_w24.cu", "qmoe_fused_w32.cu", "qmoe_fused_w33.cu", "qmoe_fused_w34.cu",
+           "qmoe_fused_w42.cu", "qmoe_fused_w43.cu", "qmoe_fused_w44.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
          "--expt-relaxed-constexpr", "-I", INCLUDE]

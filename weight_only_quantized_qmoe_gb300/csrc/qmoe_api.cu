@@ -19,6 +19,7 @@
 
 #include "qmoe_internal.cuh"
 #include "qmoe_prefill.cuh"
+#include "qmoe_fused.cuh"
 
 using namespace qmoe;
 
@@ -61,6 +62,8 @@ struct qmoe_layer {
   float zp_offset = NAN;
   bool offset_set = false;
   int gemm_min_rows = 0;
+  int fused = 0;                           // single-launch decode forward when it applies
+  int last_path = QMOE_PATH_NONE;
   int device = -1;
   long long wait_limit = kDefaultWaitLimit;
   int inject_stall = 0;
@@ -86,6 +89,7 @@ struct qmoe_layer {
   uint8_t* xt = nullptr;       // x of GEMM-class items, tiled token layout (fc1 B operand)
   uint8_t* ht = nullptr;       // h of GEMM-class items, tiled token layout (fc2 B operand)
   float* out_acc = nullptr;    // fp32 [T, H] combine accumulator (mixed forwards)
+  int* sync = nullptr;         // counters of the single-launch decode forward (zero between launches)
   bool tiles_ok = false;
   int num_sms = 0;
 
@@ -184,7 +188,7 @@ cudaError_t launch_half_bias(const float* src, float* dst, size_t n, int half, c
 void free_workspace(qmoe_layer* l) {
   void* bufs[] = {l->ids, l->w, l->counts, l->offsets, l->perm, l->pos, l->n_items, l->items[0],
                   l->items[1], l->hbuf, l->ybuf, l->status, l->x_stage, l->logits_stage,
-                  l->out_stage, l->xt, l->ht, l->out_acc};
+                  l->out_stage, l->xt, l->ht, l->out_acc, l->sync};
   for (void* b : bufs)
     if (b) cudaFree(b);
   l->ids = nullptr;
@@ -200,6 +204,7 @@ void free_workspace(qmoe_layer* l) {
   l->xt = nullptr;
   l->ht = nullptr;
   l->out_acc = nullptr;
+  l->sync = nullptr;
   l->tiles_ok = false;
   l->cap_T = 0;
 }
@@ -263,6 +268,11 @@ qmoe_status ensure_workspace(qmoe_layer* l, int64_t T) {
     QMOE_CUDA(l, cudaMemset(l->out_acc, 0, (size_t)T * l->H * sizeof(float)), "clear accumulator");
     l->tiles_ok = true;
   }
+  {
+    const size_t n = (size_t)kSyncHeader + l->E + (l->H + 15) / 16;
+    QMOE_CUDA(l, dalloc(&l->sync, n * sizeof(int)), "allocate workspace");
+    QMOE_CUDA(l, cudaMemset(l->sync, 0, n * sizeof(int)), "clear counters");
+  }
   if (l->num_sms == 0) {
     int dev = 0;
     QMOE_CUDA(l, cudaGetDevice(&dev), "cudaGetDevice");
@@ -282,6 +292,82 @@ void trace(qmoe_layer* l, int i, cudaStream_t s) {
   // Under stream capture the record becomes an event-record node of the graph.
   if (l->trace_on && l->trace[i])
     cudaEventRecordWithFlags(l->trace[i], s, capturing(s) ? cudaEventRecordExternal : cudaEventRecordDefault);
+}
+
+// ----------------------------------------------------------------------------
+// Single-launch decode forward (qmoe_fused.cu): small token counts, 16-bit
+// activations, code widths {2, 3, 4}.
+// ----------------------------------------------------------------------------
+// Shared memory of one CTA at most, so that two CTAs share an SM.
+constexpr int kFusedMaxSmem = 110 * 1024;
+
+bool fused_applies(const qmoe_layer* l, int64_t T, int* smem) {
+  if (!l->fused || l->dtype == QMOE_F32 || !l->sync) return false;
+  if (T > kFusedMaxTokens || l->E > kFusedMaxExperts || l->k > kFusedMaxK) return false;
+  if (T * l->k > kFusedMaxRoutes) return false;
+  if (!fused_widths_supported(l->bits[0], l->bits[1])) return false;
+  const int sc = l->proj[0].L.SC;
+  const int nkc = l->proj[0].L.nkc > l->proj[1].L.nkc ? l->proj[0].L.nkc : l->proj[1].L.nkc;
+  *smem = fused_smem_bytes((int)(T * l->k), l->E, nkc * sc);
+  return *smem <= kFusedMaxSmem;
+}
+
+qmoe_status forward_fused(qmoe_layer* l, const void* x, const float* logits, void* out, int64_t T, int smem,
+                          cudaStream_t s) {
+  const int R = (int)(T * l->k);
+  const int grid_max = 2 * l->num_sms;
+  FusedArgs a{};
+  a.logits = logits;
+  a.x = x;
+  a.out = out;
+  a.T = (int)T;
+  a.E = l->E;
+  a.k = l->k;
+  a.normalize = l->normalize;
+  a.H = l->H;
+  a.I = l->I;
+  a.gated = act_gated(l->act) ? 1 : 0;
+  // one group of routed rows per expert that receives any (more above 16 rows)
+  const long long nrg_est = R < l->E ? R : l->E;
+  for (int f = 0; f < 2; ++f) {
+    const Proj& p = l->proj[f];
+    FusedProj& q = a.p[f];
+    q.wpk = p.dec;
+    q.L = p.L;
+    q.K = p.K;
+    q.ntiles = p.L.ntiles;
+    q.bias = l->bias[f];
+    fused_item_shape(q.ntiles, p.L.nkc, nrg_est, grid_max, &q.tpi, &q.ks);
+  }
+  a.act = act_params(l);
+  a.zp_mode = l->zp_mode;
+  a.zp_offset = l->zp_offset;
+  a.ids = l->ids;
+  a.w = l->w;
+  a.counts = l->counts;
+  a.offsets = l->offsets;
+  a.perm = l->perm;
+  a.items0 = l->items[0];
+  a.n_items = l->n_items;
+  a.hbuf = l->hbuf;
+  a.ybuf = l->ybuf;
+  a.sync = l->sync;
+  a.n_mg = (a.p[1].ntiles + a.p[1].tpi - 1) / a.p[1].tpi;
+  a.wait = WaitCfg{l->status, l->wait_limit};
+  a.inject_stall = l->inject_stall;
+  // no more CTAs than the largest possible item count keeps busy
+  const long long nrg_max = nrg_est + R / kFusedRowsPerGroup;
+  const long long items_max = nrg_max * ((a.p[0].ntiles + a.p[0].tpi - 1) / a.p[0].tpi + a.n_mg);
+  const int grid = (int)(items_max < grid_max ? items_max : grid_max);
+  l->last_T = T;
+  l->last_path = QMOE_PATH_FUSED;
+  l->last_tb[0] = kFusedRowsPerGroup;
+  l->last_tb[1] = 128;
+  trace(l, QMOE_TRACE_BEGIN, s);
+  QMOE_CUDA(l, launch_fused(a, l->bits[0], l->bits[1], l->dtype == QMOE_BF16, l->proj[0].L.SC, grid, smem, s),
+            "launch the single-launch decode forward");
+  for (int i = QMOE_TRACE_ROUTED; i <= QMOE_TRACE_END; ++i) trace(l, i, s);
+  return QMOE_OK;
 }
 
 }  // namespace
@@ -420,6 +506,14 @@ qmoe_status qmoe_set_gemm_min_rows(qmoe_layer* l, int min_rows) {
   l->gemm_min_rows = min_rows;
   return QMOE_OK;
 }
+
+qmoe_status qmoe_set_fused_decode(qmoe_layer* l, int enable) {
+  if (!l) return QMOE_ERR_INVALID_ARG;
+  l->fused = enable ? 1 : 0;
+  return QMOE_OK;
+}
+
+int qmoe_last_forward_path(const qmoe_layer* l) { return l ? l->last_path : QMOE_PATH_NONE; }
 
 qmoe_status qmoe_set_wait_limit(qmoe_layer* l, int64_t iterations) {
   if (!l || iterations < 0) return QMOE_ERR_INVALID_ARG;
@@ -576,9 +670,12 @@ qmoe_status qmoe_forward(qmoe_layer* l, const void* x, const float* logits, void
     const qmoe_status st = ensure_workspace(l, T);
     if (st != QMOE_OK) return st;
   }
+  int fsmem = 0;
+  if (fused_applies(l, T, &fsmem)) return forward_fused(l, x, logits, out, T, fsmem, s);
   int tb0, tb1;
   item_heights(l, T, &tb0, &tb1);
   l->last_T = T;
+  l->last_path = QMOE_PATH_SEPARATE;
   l->last_tb[0] = tb0;
   l->last_tb[1] = tb1;
   const int R = (int)(T * l->k);
