@@ -54,8 +54,11 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--gemm-min-rows", type=int, default=None,
                     help="experts with more rows take the tensor-core grouped GEMM")
-    ap.add_argument("--separate", action="store_true",
-                    help="run the separate kernels instead of the single-launch decode forward")
+    ap.add_argument("--path", default="auto", choices=["auto", "fused", "separate"],
+                    help="launch sequence: the library's automatic choice (default), the single "
+                         "launch wherever it applies, or the separate kernels")
+    ap.add_argument("--deterministic", action="store_true",
+                    help="slot-ordered combine on the tensor-core path (qmoe_set_deterministic)")
     ap.add_argument("--only-headline", action="store_true",
                     help="time only --workload (no `workloads` block)")
     return ap.parse_args()
@@ -296,6 +299,7 @@ def measure(q, cfg, args, dev, stream, flush, steps, warmup, fused=1, min_rows=0
     layer = q.QMoELayer.from_config(cfg)
     layer.set_fused_decode(fused)
     layer.set_gemm_min_rows(min_rows)
+    layer.set_deterministic(1 if args.deterministic else 0)
     layer.reserve(cfg.T)
     x, logits = q.load_inputs(layer, inp, device=dev)
     out = torch.empty_like(x)
@@ -456,7 +460,7 @@ def run_ours(args):
     stream = torch.cuda.Stream(device=dev)
     flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
     hbm_peak, bf16_peak, peak_kind = measured_peaks()
-    fused = 0 if args.separate else 1
+    fused = {"auto": 2, "fused": 1, "separate": 0}[args.path]
     min_rows = args.gemm_min_rows if args.gemm_min_rows is not None else 0
 
     clocks = ClockSampler(local)

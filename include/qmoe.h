@@ -177,18 +177,32 @@ qmoe_status qmoe_set_bias(qmoe_layer* layer, int fc, const float* bias_dev, void
  * PR "fast INT3" kMaxProfiledExpandedRows] */
 qmoe_status qmoe_set_gemm_min_rows(qmoe_layer* layer, int min_rows);
 
-/* The single-launch decode forward (1) or the separate kernels (0,
- * default).  When it applies -- 16-bit activations, at most 64 tokens, E <= 256,
- * k <= 32, T*k <= 512, fc1 and fc2 code widths in {2, 3, 4} -- qmoe_forward
- * runs routing, grouping, fc1 with its activation, fc2 and the slot-ordered
- * combine in one persistent kernel launch; otherwise, or when disabled, the
- * separate kernels run (qmoe_set_gemm_min_rows picks between their
- * projection paths).  Either gives the same result within tolerance; the
- * single launch is bitwise deterministic.  [The pages motivate the fusion:
+/* Which launch sequence qmoe_forward uses for small token counts:
+ * QMOE_FUSED_OFF (0) the separate kernels; QMOE_FUSED_ON (1) the single
+ * launch whenever it applies; QMOE_FUSED_AUTO (2, default) the single launch
+ * when it applies and T * k <= 64 (where it measured faster).  It applies to
+ * 16-bit activations, at most 64 tokens, E <= 256 with E a multiple of 4,
+ * k <= 32, T * k <= 512 and fc1 / fc2 code widths in {2, 3, 4}: then routing,
+ * grouping, fc1 with its activation, fc2 and the slot-ordered combine run in
+ * one persistent (cooperative) kernel launch.  Otherwise the separate kernels
+ * run (qmoe_set_gemm_min_rows picks between their projection paths).  Either
+ * gives the same result within tolerance; the single launch is bitwise
+ * deterministic.  Other values: INVALID_ARG.  [The pages motivate the fusion:
  * PR "fast INT3 QMoE kernels", single-CTA FusedSoftmaxTopKMapsKernel for up
  * to 8 rows and the fused finalize of moe_gemv; ferrum moe.rs
  * SingleTokenDirectMarlin.] */
-qmoe_status qmoe_set_fused_decode(qmoe_layer* layer, int enable);
+enum { QMOE_FUSED_OFF = 0, QMOE_FUSED_ON = 1, QMOE_FUSED_AUTO = 2 };
+qmoe_status qmoe_set_fused_decode(qmoe_layer* layer, int mode);
+
+/* The combine of the tensor-core grouped GEMM path: 0 (default) adds each
+ * route's w * y into an fp32 [T, H] accumulator with fp32 reductions in the
+ * fc2 epilogue (the order of the k additions may vary run to run: a last-bit
+ * difference at most after rounding to D); 1 writes the y rows and adds the
+ * k slots in ascending order in a separate pass, bitwise deterministic at the
+ * cost of writing and reading T * k * H fp32 values.  The single launch and
+ * the decode kernels always add the slots in order.  [qmoe.rs
+ * qmoe_combine_impl: slots summed in order] */
+qmoe_status qmoe_set_deterministic(qmoe_layer* layer, int enable);
 
 /* Which launch sequence the last qmoe_forward / qmoe_forward_host used:
  * QMOE_PATH_NONE (no forward with tokens yet), QMOE_PATH_SEPARATE (routing,

@@ -438,3 +438,24 @@ def test_trace_events_bracket_stages(qm):
     times = [ev[i].elapsed_time(ev[i + 1]) for i in range(len(ev) - 1)]
     assert all(t >= 0 for t in times)
     layer.set_trace_events(None)
+
+
+@pytest.mark.parametrize("min_rows", [0, 24])
+def test_deterministic_gemm_combine(qm, min_rows):
+    # qmoe_set_deterministic: the fc2 GEMM writes y rows and the k slots are
+    # added in order [qmoe.rs qmoe_combine_impl] instead of fp32 reductions;
+    # with min_rows = 24 the forward mixes decode-class and GEMM-class experts.
+    cfg = BASE.with_(T=200, E=16, k=2, zipf_bias=1.5)
+    inp = make_inputs(cfg)
+    layer = qm.QMoELayer.from_config(cfg)
+    layer.set_fused_decode(0)
+    layer.set_gemm_min_rows(min_rows)
+    layer.set_deterministic(1)
+    x, logits = qm.load_inputs(layer, inp)
+    out1 = layer.forward(x, logits).clone()
+    out2 = layer.forward(x, logits)
+    torch.cuda.synchronize()
+    assert layer.poll() == 0
+    assert torch.equal(out1, out2)
+    check_routing(layer, inp, path=separate_path(min_rows))
+    check_out(out1, O.forward(inp), cfg.dtype)

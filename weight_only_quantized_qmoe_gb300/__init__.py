@@ -98,8 +98,13 @@ class QMoELayer:
     def set_gemm_min_rows(self, n):
         self._check(binding.qmoe_set_gemm_min_rows(self.handle, n))
 
-    def set_fused_decode(self, enable):
-        self._check(binding.qmoe_set_fused_decode(self.handle, enable))
+    def set_fused_decode(self, mode):
+        """QMOE_FUSED_OFF / QMOE_FUSED_ON / QMOE_FUSED_AUTO (default)."""
+        self._check(binding.qmoe_set_fused_decode(self.handle, mode))
+
+    def set_deterministic(self, enable):
+        """Slot-ordered (bitwise deterministic) combine on the tensor-core path."""
+        self._check(binding.qmoe_set_deterministic(self.handle, enable))
 
     def last_path(self):
         """QMOE_PATH_SEPARATE or QMOE_PATH_FUSED: the launch sequence of the

@@ -26,6 +26,7 @@ QMOE_FC1_CONCAT, QMOE_FC1_INTERLEAVED, QMOE_FC1_SEPARATE_FC3 = 0, 1, 2
 QMOE_F32, QMOE_F16, QMOE_BF16 = 0, 1, 2
 QMOE_TRACE_NUM_EVENTS = 5
 QMOE_PATH_NONE, QMOE_PATH_SEPARATE, QMOE_PATH_FUSED = 0, 1, 2
+QMOE_FUSED_OFF, QMOE_FUSED_ON, QMOE_FUSED_AUTO = 0, 1, 2
 
 _p = ctypes.c_void_p
 _i = ctypes.c_int
@@ -37,6 +38,7 @@ _SIGS = {
     "qmoe_set_gemm_min_rows": (_i, [_p, _i]),
     "qmoe_set_fused_decode": (_i, [_p, _i]),
     "qmoe_last_forward_path": (_i, [_p]),
+    "qmoe_set_deterministic": (_i, [_p, _i]),
     "qmoe_set_swiglu_params": (_i, [_p, ctypes.c_float, ctypes.c_float, ctypes.c_float]),
     "qmoe_set_fc1_layout": (_i, [_p, _i]),
     "qmoe_set_bias": (_i, [_p, _i, _p, _p]),
@@ -106,8 +108,12 @@ def qmoe_set_gemm_min_rows(layer, min_rows):
     return load().qmoe_set_gemm_min_rows(layer, int(min_rows))
 
 
-def qmoe_set_fused_decode(layer, enable):
-    return load().qmoe_set_fused_decode(layer, int(enable))
+def qmoe_set_fused_decode(layer, mode):
+    return load().qmoe_set_fused_decode(layer, int(mode))
+
+
+def qmoe_set_deterministic(layer, enable):
+    return load().qmoe_set_deterministic(layer, int(enable))
 
 
 def qmoe_last_forward_path(layer):

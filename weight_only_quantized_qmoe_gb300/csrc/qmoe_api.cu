@@ -62,7 +62,8 @@ struct qmoe_layer {
   float zp_offset = NAN;
   bool offset_set = false;
   int gemm_min_rows = 0;
-  int fused = 0;                           // single-launch decode forward when it applies
+  int fused = 2;                           // single launch: 0 off, 1 whenever it applies, 2 auto
+  int deterministic = 0;                   // tensor-core path: slot-ordered combine instead of fp32 reductions
   int last_path = QMOE_PATH_NONE;
   int device = -1;
   long long wait_limit = kDefaultWaitLimit;
@@ -269,7 +270,10 @@ qmoe_status ensure_workspace(qmoe_layer* l, int64_t T) {
     l->tiles_ok = true;
   }
   {
-    const size_t n = (size_t)kSyncHeader + l->E + (l->H + 15) / 16;
+    // counters of the single launch: header, one per segment (group of <= 16
+    // routed rows of an expert; at most min(R, E) + R / 16 + 1)
+    const size_t segs = (size_t)(R < l->E ? R : l->E) + R / kFusedRowsPerGroup + 1;
+    const size_t n = (size_t)kSyncHeader + segs;
     QMOE_CUDA(l, dalloc(&l->sync, n * sizeof(int)), "allocate workspace");
     QMOE_CUDA(l, cudaMemset(l->sync, 0, n * sizeof(int)), "clear counters");
   }
@@ -298,24 +302,61 @@ void trace(qmoe_layer* l, int i, cudaStream_t s) {
 // Single-launch decode forward (qmoe_fused.cu): small token counts, 16-bit
 // activations, code widths {2, 3, 4}.
 // ----------------------------------------------------------------------------
-// Shared memory of one CTA at most, so that two CTAs share an SM.
-constexpr int kFusedMaxSmem = 110 * 1024;
+// Shared memory of a CTA: two 8-warp CTAs per SM when the plan fits (each
+// CTA's barriers are then covered by the other's work), else one 16-warp CTA.
+constexpr int kFusedSmemTwoPerSm = 113 * 1024;
+constexpr int kFusedSmemOnePerSm = 227 * 1024;
+// Smallest ring stage worth two CTAs per SM (16 warps x 3 stages in flight).
+constexpr int kFusedMinStageTwoPerSm = 1024;
 
-bool fused_applies(const qmoe_layer* l, int64_t T, int* smem) {
+struct FusedShape {
+  int smem, sb, g1, g2, ng_max, warps, ctas_per_sm;
+};
+
+// Segments (groups of <= 16 routed rows of one expert) a forward of T tokens
+// can have at most.
+int fused_max_segments(const qmoe_layer* l, int64_t T) {
+  const int64_t R = T * l->k;
+  return (int)((R < l->E ? R : l->E) + R / kFusedRowsPerGroup + 1);
+}
+
+// Routes up to which the automatic choice takes the single launch (measured:
+// it wins at 8 tokens x top-2, the separate kernels at 256 routes).
+constexpr int64_t kFusedAutoMaxRoutes = 64;
+
+bool fused_applies(const qmoe_layer* l, int64_t T, FusedShape* fs) {
   if (!l->fused || l->dtype == QMOE_F32 || !l->sync) return false;
+  if (l->fused == 2 && T * l->k > kFusedAutoMaxRoutes) return false;
   if (T > kFusedMaxTokens || l->E > kFusedMaxExperts || l->k > kFusedMaxK) return false;
-  if (T * l->k > kFusedMaxRoutes) return false;
+  if (T * l->k > kFusedMaxRoutes || l->E % 4) return false;
   if (!fused_widths_supported(l->bits[0], l->bits[1])) return false;
   const int sc = l->proj[0].L.SC;
   const int nkc = l->proj[0].L.nkc > l->proj[1].L.nkc ? l->proj[0].L.nkc : l->proj[1].L.nkc;
-  *smem = fused_smem_bytes((int)(T * l->k), l->E, nkc * sc);
-  return *smem <= kFusedMaxSmem;
+  const int R = (int)(T * l->k);
+  // an expert's group of rows holds at most min(16, T) tokens
+  fs->ng_max = T > 8 ? 2 : 1;
+  const int scb1 = l->proj[0].L.scb, scb2 = l->proj[1].L.scb;
+  // one 16-warp CTA per SM (measured faster than two 8-warp CTAs: the B
+  // staging is not held twice, so the rings are deeper)
+  for (int warps : {16}) {
+    const int budget = warps == 8 ? kFusedSmemTwoPerSm : kFusedSmemOnePerSm;
+    const int fixed = fused_plan(R, l->E, nkc * sc, fs->ng_max, 0, warps).total;
+    if (fixed >= budget) continue;
+    if (!fused_ring_shape(budget, fixed, warps, scb1, scb2, &fs->sb, &fs->g1, &fs->g2)) continue;
+    if (warps == 8 && fs->sb < kFusedMinStageTwoPerSm) continue;
+    fs->smem = fused_plan(R, l->E, nkc * sc, fs->ng_max, fs->sb, warps).total;
+    if (fs->smem > budget) continue;
+    // the logits are staged in the ring area before the rings start
+    if ((int64_t)T * l->E * 4 > (int64_t)warps * kFusedStages * fs->sb) continue;
+    fs->warps = warps;
+    fs->ctas_per_sm = warps == 8 ? 2 : 1;
+    return true;
+  }
+  return false;
 }
 
-qmoe_status forward_fused(qmoe_layer* l, const void* x, const float* logits, void* out, int64_t T, int smem,
-                          cudaStream_t s) {
-  const int R = (int)(T * l->k);
-  const int grid_max = 2 * l->num_sms;
+qmoe_status forward_fused(qmoe_layer* l, const void* x, const float* logits, void* out, int64_t T,
+                          const FusedShape& fs, cudaStream_t s) {
   FusedArgs a{};
   a.logits = logits;
   a.x = x;
@@ -327,8 +368,6 @@ qmoe_status forward_fused(qmoe_layer* l, const void* x, const float* logits, voi
   a.H = l->H;
   a.I = l->I;
   a.gated = act_gated(l->act) ? 1 : 0;
-  // one group of routed rows per expert that receives any (more above 16 rows)
-  const long long nrg_est = R < l->E ? R : l->E;
   for (int f = 0; f < 2; ++f) {
     const Proj& p = l->proj[f];
     FusedProj& q = a.p[f];
@@ -336,8 +375,8 @@ qmoe_status forward_fused(qmoe_layer* l, const void* x, const float* logits, voi
     q.L = p.L;
     q.K = p.K;
     q.ntiles = p.L.ntiles;
+    q.g = f == 0 ? fs.g1 : fs.g2;
     q.bias = l->bias[f];
-    fused_item_shape(q.ntiles, p.L.nkc, nrg_est, grid_max, &q.tpi, &q.ks);
   }
   a.act = act_params(l);
   a.zp_mode = l->zp_mode;
@@ -352,19 +391,18 @@ qmoe_status forward_fused(qmoe_layer* l, const void* x, const float* logits, voi
   a.hbuf = l->hbuf;
   a.ybuf = l->ybuf;
   a.sync = l->sync;
-  a.n_mg = (a.p[1].ntiles + a.p[1].tpi - 1) / a.p[1].tpi;
+  a.max_seg = fused_max_segments(l, l->cap_T);
+  a.ng_max = fs.ng_max;
+  a.sb = fs.sb;
   a.wait = WaitCfg{l->status, l->wait_limit};
   a.inject_stall = l->inject_stall;
-  // no more CTAs than the largest possible item count keeps busy
-  const long long nrg_max = nrg_est + R / kFusedRowsPerGroup;
-  const long long items_max = nrg_max * ((a.p[0].ntiles + a.p[0].tpi - 1) / a.p[0].tpi + a.n_mg);
-  const int grid = (int)(items_max < grid_max ? items_max : grid_max);
   l->last_T = T;
   l->last_path = QMOE_PATH_FUSED;
   l->last_tb[0] = kFusedRowsPerGroup;
   l->last_tb[1] = 128;
   trace(l, QMOE_TRACE_BEGIN, s);
-  QMOE_CUDA(l, launch_fused(a, l->bits[0], l->bits[1], l->dtype == QMOE_BF16, l->proj[0].L.SC, grid, smem, s),
+  QMOE_CUDA(l, launch_fused(a, l->bits[0], l->bits[1], l->dtype == QMOE_BF16, l->proj[0].L.SC,
+                            l->num_sms * fs.ctas_per_sm, fs.warps, fs.smem, s),
             "launch the single-launch decode forward");
   for (int i = QMOE_TRACE_ROUTED; i <= QMOE_TRACE_END; ++i) trace(l, i, s);
   return QMOE_OK;
@@ -507,13 +545,19 @@ qmoe_status qmoe_set_gemm_min_rows(qmoe_layer* l, int min_rows) {
   return QMOE_OK;
 }
 
-qmoe_status qmoe_set_fused_decode(qmoe_layer* l, int enable) {
-  if (!l) return QMOE_ERR_INVALID_ARG;
-  l->fused = enable ? 1 : 0;
+qmoe_status qmoe_set_fused_decode(qmoe_layer* l, int mode) {
+  if (!l || mode < 0 || mode > 2) return QMOE_ERR_INVALID_ARG;
+  l->fused = mode;
   return QMOE_OK;
 }
 
 int qmoe_last_forward_path(const qmoe_layer* l) { return l ? l->last_path : QMOE_PATH_NONE; }
+
+qmoe_status qmoe_set_deterministic(qmoe_layer* l, int enable) {
+  if (!l) return QMOE_ERR_INVALID_ARG;
+  l->deterministic = enable ? 1 : 0;
+  return QMOE_OK;
+}
 
 qmoe_status qmoe_set_wait_limit(qmoe_layer* l, int64_t iterations) {
   if (!l || iterations < 0) return QMOE_ERR_INVALID_ARG;
@@ -670,15 +714,14 @@ qmoe_status qmoe_forward(qmoe_layer* l, const void* x, const float* logits, void
     const qmoe_status st = ensure_workspace(l, T);
     if (st != QMOE_OK) return st;
   }
-  int fsmem = 0;
-  if (fused_applies(l, T, &fsmem)) return forward_fused(l, x, logits, out, T, fsmem, s);
+  FusedShape fs{};
+  if (fused_applies(l, T, &fs)) return forward_fused(l, x, logits, out, T, fs, s);
   int tb0, tb1;
   item_heights(l, T, &tb0, &tb1);
   l->last_T = T;
   l->last_path = QMOE_PATH_SEPARATE;
   l->last_tb[0] = tb0;
   l->last_tb[1] = tb1;
-  const int R = (int)(T * l->k);
   const WaitCfg wait{l->status, l->wait_limit};
   // An expert can receive at most T rows: only when T exceeds the threshold
   // can the grouped-GEMM class be non-empty.
@@ -769,7 +812,7 @@ qmoe_status qmoe_forward(qmoe_layer* l, const void* x, const float* logits, void
       da.wait = wait;
       da.pdl = 1;
       da.inject_stall = l->inject_stall;
-      da.atomic = gemm && f == 1;
+      da.atomic = gemm && f == 1 && !l->deterministic;
       da.out_acc = l->out_acc;
       da.w = l->w;
       QMOE_CUDA(l, launch_decode_mma(da, s), "launch decode projection");
@@ -795,6 +838,7 @@ qmoe_status qmoe_forward(qmoe_layer* l, const void* x, const float* logits, void
         ga.htiles = l->ht;
         ga.h_ksteps = (l->I + 63) / 64;
         ga.out_acc = l->out_acc;
+        ga.ybuf = f == 1 && l->deterministic ? l->ybuf : nullptr;
         ga.perm = l->perm;
         ga.w = l->w;
         ga.k = l->k;
@@ -807,7 +851,7 @@ qmoe_status qmoe_forward(qmoe_layer* l, const void* x, const float* logits, void
     trace(l, f == 0 ? QMOE_TRACE_FC1 : QMOE_TRACE_FC2, s);
   }
 
-  if (gemm) {
+  if (gemm && !l->deterministic) {
     QMOE_CUDA(l, launch_finalize_acc(l->out_acc, out, (size_t)T * l->H, l->dtype, s), "launch combine");
   } else {
     FinalizeArgs fa{};

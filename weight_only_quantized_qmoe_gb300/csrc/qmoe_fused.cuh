@@ -18,22 +18,27 @@
 // path of ferrum moe.rs (SingleTokenDirectMarlin).
 //
 // GB300 design (ours):
+//   * one CTA of 16 warps per SM, launched cooperatively (all CTAs resident:
+//     fc2 waits on other CTAs' fc1 results);
 //   * every CTA routes all tokens itself (a warp per token, warp-wide
 //     redux.sync arg-max per slot) and builds the grouping in shared memory,
 //     so no CTA waits on another before it streams weights;
-//   * work items are handed out by one atomic ticket counter in a fixed order
-//     (all fc1 items expert by expert, then all fc2 items): an item only ever
-//     waits on items with smaller tickets, which running CTAs hold, so the
-//     kernel needs no co-residency guarantee;
-//   * an item = (expert, group of <= 16 routed rows, group of 16-row weight
-//     tiles); its 8 warps split the tiles and K; each warp streams its part of
-//     the prepacked tile straight from HBM into registers (128-bit
-//     non-coherent loads, a ring of 2 super-chunks in flight) and feeds
-//     mma.m16n8k16 with fp32 accumulation, the routed rows staged once per item
-//     in shared memory in B-fragment order;
-//   * fc2 items of an expert start as soon as that expert's fc1 items are done
-//     (a per-expert counter, bounded wait); the last fc2 item of each group of
-//     output rows adds the k slots in order and rounds into D;
+//   * the work is a list of 16-row weight tiles per phase (fc1 tiles of every
+//     (expert, group of <= 16 routed rows) segment, then the fc2 tiles);
+//     each CTA takes a contiguous, equal share of each phase, cut at segment
+//     boundaries into blocks; the 16 warps split a block's tiles (and K, when
+//     a block has fewer tiles than warps);
+//   * each warp streams its tiles through a private shared-memory ring of
+//     cp.async stages that runs ahead across blocks and phases (weights never
+//     wait on anything), dequantises in registers and feeds mma.m16n8k16 with
+//     fp32 accumulation; the routed rows of the block's segment are staged
+//     once per block in B-fragment order;
+//   * a block ends with one CTA barrier: split-K partials are added in a fixed
+//     order, fc1 publishes h and bumps the segment's counter (release), fc2
+//     writes y;
+//   * once every CTA is done with fc2 (a grid-wide arrival counter), each CTA
+//     adds the k slots in order for an equal share of the outputs and rounds
+//     into D;
 //   * the last CTA to leave clears the counters for the next launch.
 #pragma once
 #include <climits>
@@ -48,10 +53,12 @@ constexpr int kFusedMaxTokens = 64;
 constexpr int kFusedMaxExperts = 256;
 constexpr int kFusedMaxRoutes = 512;
 constexpr int kFusedMaxK = 32;
-constexpr int kFusedThreads = 256;   // 8 warps
+constexpr int kFusedMaxWarps = 16;   // warps per CTA: 16 (one CTA per SM) or 8 (two)
 constexpr int kFusedRowsPerGroup = 16;
-// Counters in the sync buffer: [0] ticket, [1] exit, [2] a flag nothing sets
-// (the injected stall waits on it), then done1[E], then done2[M-groups].
+constexpr int kFusedStages = 4;      // cp.async ring stages per warp (3 in flight)
+// Counters in the sync buffer: [0] unused, [1] exit, [2] a flag nothing sets
+// (the injected stall waits on it), [3] CTAs done with fc2, then
+// done1[segment].
 constexpr int kSyncHeader = 4;
 
 struct FusedProj {
@@ -59,7 +66,7 @@ struct FusedProj {
   DecodeLayout L;
   int K;                // real K
   int ntiles;           // 16-row tiles (fc1: feature tiles, gate + up when gated)
-  int tpi, ks;          // weight tiles per item, K-splits (tpi * ks == 8)
+  int g;                // super-chunks per ring stage
   const float* bias;    // fc1 gated: [E, I, 2]; fc1 plain: [E, I]; fc2: [E, H]; or null
 };
 
@@ -83,22 +90,33 @@ struct FusedArgs {
   int* n_items;
   void* hbuf;           // [R, I] D, by route
   float* ybuf;          // [R, H] f32, by route
-  int* sync;            // kSyncHeader + E + n_mg ints, zero between launches
-  int n_mg;             // fc2 groups of output rows (= ceil(fc2 tiles / fc2 tpi))
+  int* sync;            // kSyncHeader + max segments ints, zero between launches
+  int max_seg;          // capacity of done1
+  int ng_max;           // token groups of 8 the B staging is sized for (1 or 2)
+  int sb;               // bytes per ring stage
   WaitCfg wait;
   int inject_stall;
 };
 
 // Shared-memory plan of one CTA (the front of dynamic shared memory).
 struct FusedPlan {
-  int ids_off, w_off, perm_off, cnt_off, off_off, cur_off, act_off, rgb_off, bop_off, total;
+  int ids_off, w_off, perm_off, cnt_off, off_off, cur_off, act_off, rgb_off, bop_off, ring_off, total;
 };
 
 __host__ __device__ inline int fused_align16(int v) { return (v + 15) & ~15; }
 
-__host__ __device__ inline FusedPlan fused_plan(int R, int E, int bop_bytes) {
+// Bytes of the B-operand staging (>= the split-K reduction it is reused for).
+__host__ __device__ inline int fused_bop_bytes(int Kp_max, int ng_max, int warps) {
+  const int bop = Kp_max / 16 * ng_max * 32 * 8;   // k-tiles x token groups x 32 lanes x 8 B
+  const int red = warps * 32 * (2 * 2 * 4) * 4;   // warps x 32 lanes x acc[2][2][4] floats
+  return bop > red ? bop : red;
+}
+
+// Shared memory: broadcast ints, routing and grouping, the B staging, then
+// one ring of kFusedStages stages of sb bytes per warp.
+__host__ __device__ inline FusedPlan fused_plan(int R, int E, int Kp_max, int ng_max, int sb, int warps) {
   FusedPlan p;
-  int o = 64;   // a few broadcast ints first
+  int o = 64;
   p.ids_off = o;  o = fused_align16(o + 4 * R);
   p.w_off = o;    o = fused_align16(o + 4 * R);
   p.perm_off = o; o = fused_align16(o + 4 * R);
@@ -109,15 +127,11 @@ __host__ __device__ inline FusedPlan fused_plan(int R, int E, int bop_bytes) {
   p.rgb_off = o;  o = fused_align16(o + 4 * (E + 1));
   o = (o + 127) & ~127;
   p.bop_off = o;
-  p.total = o + bop_bytes;
+  o += fused_bop_bytes(Kp_max, ng_max, warps);
+  o = (o + 127) & ~127;
+  p.ring_off = o;
+  p.total = o + warps * kFusedStages * sb;
   return p;
-}
-
-// Bytes of the B-operand staging (>= the split-K reduction it is reused for).
-__host__ __device__ inline int fused_bop_bytes(int Kp_max) {
-  const int bop = Kp_max / 16 * 2 * 32 * 8;           // k-tiles x 2 token groups x 32 lanes x 8 B
-  const int red = 8 * 32 * (2 * 2 * 4) * 4;           // 8 warps x 32 lanes x acc[2][2][4] floats
-  return bop > red ? bop : red;
 }
 
 __device__ __forceinline__ int redux_max_s32(int v) {
@@ -136,11 +150,10 @@ __device__ __forceinline__ int fused_order_key(float v) {
   return b ^ ((b >> 31) & 0x7fffffff);
 }
 
-// One warp ranks the E (<= 256) logits of one token: ids[0..k) in rank order
-// and their weights.
-__device__ __forceinline__ void fused_route_token(const float* __restrict__ lg, int E, int k, int normalize,
-                                                  int* ids, float* w) {
-  constexpr int NPL = kFusedMaxExperts / 32;
+// One warp ranks the E <= 32 * NPL logits of one token (in shared memory):
+// ids[0..k) in rank order and their weights.
+template <int NPL>
+__device__ __forceinline__ void fused_route_token(const float* lg, int E, int k, int normalize, int* ids, float* w) {
   const int lane = threadIdx.x & 31;
   int key[NPL];
   uint32_t taken = 0;
@@ -148,12 +161,12 @@ __device__ __forceinline__ void fused_route_token(const float* __restrict__ lg, 
 #pragma unroll
   for (int i = 0; i < NPL; ++i) {
     const int e = lane + 32 * i;
+    key[i] = INT_MIN;
     if (e < E) {
       const float v = lg[e];
       key[i] = fused_order_key(v);
       mx = fmaxf(mx, v);
     } else {
-      key[i] = INT_MIN;
       taken |= 1u << i;
     }
   }
@@ -189,6 +202,14 @@ __device__ __forceinline__ void fused_route_token(const float* __restrict__ lg, 
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) sum_sel += __shfl_xor_sync(0xffffffffu, sum_sel, o);
   if (lane < k) w[lane] = p / (normalize ? sum_sel : sum_all);
+}
+
+// Every token of the forward, a warp each, with the key count per lane
+// fixed at compile time for E's size class.
+template <int NPL>
+__device__ __noinline__ void fused_route_all(const float* lg_s, int T, int E, int k, int normalize, int* ids_s,
+                                             float* w_s, int warp, int W) {
+  for (int t = warp; t < T; t += W) fused_route_token<NPL>(lg_s + t * E, E, k, normalize, ids_s + t * k, w_s + t * k);
 }
 
 // ----------------------------------------------------------------------------
@@ -227,6 +248,7 @@ struct FusedGeom {
   bool has_zp;    // packed uint8 zero points present
 };
 
+// One super-chunk of the ring (shared memory) into registers.
 template <int BITS, int SC, int NSUB>
 __device__ __forceinline__ void fused_load_chunk(FusedChunk<BITS, SC, NSUB>& c, const uint8_t* ch,
                                                  const FusedGeom& gm, int lane) {
@@ -238,39 +260,32 @@ __device__ __forceinline__ void fused_load_chunk(FusedChunk<BITS, SC, NSUB>& c, 
     if constexpr (C::WPL % 4 == 0) {
 #pragma unroll
       for (int w = 0; w < C::WPL; w += 4) {
-        const uint4 q = ld_nc_v4(base + lane * C::WPL + w);
+        const uint4 q = *reinterpret_cast<const uint4*>(base + lane * C::WPL + w);
         c.cw[s][w] = q.x; c.cw[s][w + 1] = q.y; c.cw[s][w + 2] = q.z; c.cw[s][w + 3] = q.w;
       }
     } else if constexpr (C::WPL == 2) {
-      const uint2 q = ld_nc_v2(base + lane * 2);
+      const uint2 q = *reinterpret_cast<const uint2*>(base + lane * 2);
       c.cw[s][0] = q.x; c.cw[s][1] = q.y;
     } else {
       static_assert(C::WPL == 1, "code words per lane");
-      c.cw[s][0] = ld_nc_u32(base + lane);
+      c.cw[s][0] = base[lane];
     }
     if constexpr (BITS == 3) {
-      if constexpr (C::WPH == 2) {
-        const uint2 q = ld_nc_v2(base + 32 * C::WPL + lane * 2);
-        c.hw[s][0] = q.x; c.hw[s][1] = q.y;
-      } else {
-        c.hw[s][0] = ld_nc_u32(base + 32 * C::WPL + lane);
-      }
+#pragma unroll
+      for (int w = 0; w < C::WPH; ++w) c.hw[s][w] = base[32 * C::WPL + lane * C::WPH + w];
     }
     const uint8_t* sp = ch + NSUB * gm.code_bytes + s * gm.scale_bytes;
-    c.sp[s][0] = ld_nc_u32(sp + g * 4);
-    if constexpr (C::NBKM == 2) c.sp[s][1] = gm.nbk == 2 ? ld_nc_u32(sp + 32 + g * 4) : c.sp[s][0];
+    c.sp[s][0] = *reinterpret_cast<const uint32_t*>(sp + g * 4);
+    if constexpr (C::NBKM == 2) c.sp[s][1] = gm.nbk == 2 ? *reinterpret_cast<const uint32_t*>(sp + 32 + g * 4) : c.sp[s][0];
     if (gm.has_zp) {
       const uint8_t* zp = ch + NSUB * (gm.code_bytes + gm.scale_bytes) + s * gm.zp_bytes;
 #pragma unroll
       for (int b = 0; b < C::NBKM; ++b) {
-        if (b == 0 || gm.nbk == 2) {
-          if constexpr (BITS == 8)
-            c.zb[s][b] = ld_nc_u8(zp + b * 16 + 2 * g) | (ld_nc_u8(zp + b * 16 + 2 * g + 1) << 8);
-          else
-            c.zb[s][b] = ld_nc_u8(zp + b * 8 + g);
-        } else {
-          c.zb[s][b] = c.zb[s][0];
-        }
+        const int bb = (b == 0 || gm.nbk == 2) ? b : 0;
+        if constexpr (BITS == 8)
+          c.zb[s][b] = (uint32_t)zp[bb * 16 + 2 * g] | ((uint32_t)zp[bb * 16 + 2 * g + 1] << 8);
+        else
+          c.zb[s][b] = zp[bb * 8 + g];
       }
     }
   }
@@ -306,10 +321,67 @@ __device__ __forceinline__ void fused_compute_chunk(const FusedChunk<BITS, SC, N
         zz[s][b][0] = zz[s][b][1] = ZSYM;
       }
     }
+  // fp16 with 2- or 4-bit codes: each code is masked where it sits (one shift
+  // per four pairs) over the magic exponent, giving M + m q for a power of two
+  // m; one exact fma by 1/m minus (M/m + z) leaves q - z.  cz[s][b][i] holds
+  // -(M/m_i + z) of position i (i = 1..3 for 2-bit, i = 1 for 4-bit codes).
+  constexpr bool MASKED = !BF16 && (BITS == 2 || BITS == 4);
+  uint32_t cz[NSUB][C::NBKM][4];
+  if constexpr (MASKED) {
+    // -(M/m) for m = 4, 16, 64 (2-bit) or 16 (4-bit); M = 1024, or 512 for
+    // the half-unit magic of a fractional zero point
+    constexpr uint32_t NEG2[3] = {OFFS ? 0xD800D800u : 0xDC00DC00u, OFFS ? 0xD000D000u : 0xD400D400u,
+                                  OFFS ? 0xC800C800u : 0xCC00CC00u};
+    constexpr uint32_t NEG4 = OFFS ? 0xD000D000u : 0xD400D400u;
+#pragma unroll
+    for (int s = 0; s < NSUB; ++s)
+#pragma unroll
+      for (int b = 0; b < C::NBKM; ++b) {
+        // z of row g (even pairs) and row g + 8 (odd pairs), exact in fp16
+        const uint32_t zg = OFFS ? sub2<false>(zoff2, Magic<false>::half) : sub2<false>(zz[s][b][0], MAGIC);
+        const uint32_t zg8 = OFFS ? zg : sub2<false>(zz[s][b][1], MAGIC);
+        if constexpr (BITS == 2) {
+          cz[s][b][1] = sub2<false>(NEG2[0], zg8);
+          cz[s][b][2] = sub2<false>(NEG2[1], zg);
+          cz[s][b][3] = sub2<false>(NEG2[2], zg8);
+        } else {
+          cz[s][b][1] = sub2<false>(NEG4, zg8);
+        }
+        cz[s][b][0] = OFFS ? zoff2 : zz[s][b][0];
+      }
+  }
 #pragma unroll
   for (int j = 0; j < KT; ++j) {
     const int b = (C::NBKM == 2 && j >= KT / 2) ? 1 : 0;
     uint32_t afrag[NSUB][4];
+    if constexpr (MASKED) {
+      constexpr uint32_t BASE = OFFS ? Magic<false>::half : MAGIC;
+#pragma unroll
+      for (int s = 0; s < NSUB; ++s) {
+        uint32_t v[4];
+        if constexpr (BITS == 2) {
+          // positions 0-3 (even k-tile) or 4-7 (odd) of the word, brought to
+          // bits 0-7 (bits 1-8 for the half-unit magic)
+          const uint32_t wd = c.cw[s][j >> 1];
+          const uint32_t W = (j & 1) ? (OFFS ? wd >> 7 : wd >> 8) : (OFFS ? wd << 1 : wd);
+          constexpr uint32_t M0 = OFFS ? 0x00060006u : 0x00030003u;
+          constexpr uint32_t SC2[4] = {0u, 0x34003400u, 0x2C002C00u, 0x24002400u};   // 1, 1/4, 1/16, 1/64
+          v[0] = sub2<false>((W & M0) | BASE, cz[s][b][0]);
+#pragma unroll
+          for (int i = 1; i < 4; ++i) v[i] = fma2<false>((W & (M0 << (2 * i))) | BASE, SC2[i], cz[s][b][i]);
+        } else {
+          const uint32_t wd = c.cw[s][j];
+          const uint32_t W0 = OFFS ? wd << 1 : wd, W1 = OFFS ? wd >> 7 : wd >> 8;
+          constexpr uint32_t M0 = OFFS ? 0x001E001Eu : 0x000F000Fu;
+          v[0] = sub2<false>((W0 & M0) | BASE, cz[s][b][0]);
+          v[1] = fma2<false>((W0 & (M0 << 4)) | BASE, 0x2C002C00u, cz[s][b][1]);
+          v[2] = sub2<false>((W1 & M0) | BASE, cz[s][b][0]);
+          v[3] = fma2<false>((W1 & (M0 << 4)) | BASE, 0x2C002C00u, cz[s][b][1]);
+        }
+#pragma unroll
+        for (int r = 0; r < 4; ++r) afrag[s][r] = mul2<false>(v[r], ss[s][b][r & 1]);
+      }
+    } else {
 #pragma unroll
     for (int s = 0; s < NSUB; ++s) {
 #pragma unroll
@@ -329,6 +401,7 @@ __device__ __forceinline__ void fused_compute_chunk(const FusedChunk<BITS, SC, N
         afrag[s][r] = mul2<BF16>(v, ss[s][b][r & 1]);
       }
     }
+    }
 #pragma unroll
     for (int n = 0; n < 2; ++n) {
       if (n < NG) {
@@ -340,61 +413,6 @@ __device__ __forceinline__ void fused_compute_chunk(const FusedChunk<BITS, SC, N
   }
 }
 
-// Accumulators of one warp: [sub-tile][token group][mma fragment].
-struct FusedAcc {
-  float v[2][2][4];
-};
-
-// Stream nck super-chunks starting at `src` (a ring of U chunks in flight).
-// Not inlined: the hot loop then gets the registers to itself and the item
-// loop's state is saved once per call instead of competing with the ring.
-template <int BITS, bool BF16, int SC, int NSUB, bool OFFS>
-__device__ __noinline__ FusedAcc fused_stream(const uint8_t* __restrict__ src, int nck, FusedGeom gm,
-                                              const uint32_t* __restrict__ bop_lane, int NG, bool uint8_zp,
-                                              uint32_t zoff2) {
-  constexpr int U = 2;
-  constexpr int KT = SC / 16;
-  const int lane = threadIdx.x & 31;
-  float acc[2][2][4];
-#pragma unroll
-  for (int s = 0; s < 2; ++s)
-#pragma unroll
-    for (int n = 0; n < 2; ++n)
-#pragma unroll
-      for (int q = 0; q < 4; ++q) acc[s][n][q] = 0.f;
-  FusedChunk<BITS, SC, NSUB> ring[U];
-#pragma unroll
-  for (int u = 0; u < U; ++u)
-    if (u < nck) fused_load_chunk<BITS, SC, NSUB>(ring[u], src + (size_t)u * gm.scb, gm, lane);
-  for (int c0 = 0; c0 < nck; c0 += U) {
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const int c = c0 + u;
-      if (c < nck) {
-        fused_compute_chunk<BITS, BF16, SC, NSUB, OFFS>(ring[u], bop_lane + c * KT * NG * 64, NG, uint8_zp,
-                                                         zoff2, acc);
-        if (c + U < nck) fused_load_chunk<BITS, SC, NSUB>(ring[u], src + (size_t)(c + U) * gm.scb, gm, lane);
-      }
-    }
-  }
-  FusedAcc r;
-#pragma unroll
-  for (int s = 0; s < 2; ++s)
-#pragma unroll
-    for (int n = 0; n < 2; ++n)
-#pragma unroll
-      for (int q = 0; q < 4; ++q) r.v[s][n][q] = acc[s][n][q];
-  return r;
-}
-
-template <int BITS, bool BF16, int SC, int NSUB>
-__device__ __forceinline__ FusedAcc fused_stream_zp(const uint8_t* src, int nck, const FusedGeom& gm,
-                                                    const uint32_t* bop_lane, int NG, int zp_mode,
-                                                    uint32_t zoff2) {
-  if (zp_mode == QMOE_ZP_OFFSET)
-    return fused_stream<BITS, BF16, SC, NSUB, true>(src, nck, gm, bop_lane, NG, false, zoff2);
-  return fused_stream<BITS, BF16, SC, NSUB, false>(src, nck, gm, bop_lane, NG, zp_mode == QMOE_ZP_UINT8, zoff2);
-}
 
 __device__ __forceinline__ FusedGeom fused_geom(const DecodeLayout& L) {
   FusedGeom g;
@@ -428,16 +446,124 @@ __device__ __forceinline__ uint4 ld_cg_v4(const void* p) {
   return r;
 }
 
+__device__ __forceinline__ void cp_async16(void* smem_dst, const void* gsrc) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(smem_dst)), "l"(gsrc) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
+// K-splits of a block of n tiles (a power of two): as many as keep every warp
+// busy with at most one unit and every unit at least two super-chunks long.
+__host__ __device__ inline int fused_ks(int n, int nkc, int warps) {
+  int ks = 1;
+  while (ks < warps && n * ks * 2 <= warps && nkc >= ks * 4) ks *= 2;
+  return ks;
+}
+
+// Active expert of segment `seg` (binary search over the row-group prefix).
+__device__ __forceinline__ int fused_seg_expert(int seg, const int* rgb_s, int nact) {
+  int lo = 0, hi = nact - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (rgb_s[mid] <= seg) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
+// The ring stages one warp consumes, in order: for phase fc1 then fc2, for
+// each block of this CTA's range (a block = tiles of one segment), for each
+// of this warp's units (tile, K-slice) of the block, its super-chunks g at a
+// time.  The producer runs the same walk kFusedStages - 1 stages ahead; a
+// unit is one contiguous byte run of the prepacked tile, so a stage is a
+// pointer bump.
+struct FusedCursor {
+  int p;                  // phase; 2 = exhausted
+  int u, u_end;           // block start (tile index within the phase) and range end
+  int n, ksl2;            // tiles of the block, log2 of its K-splits
+  int v;                  // unit within the block (warp, warp + warps, ...)
+  const uint8_t* src;     // next byte of the current unit
+  int left;               // bytes of the unit not yet issued
+};
+
+struct FusedRanges {
+  int u0[2], u1[2];       // this CTA's tile range per phase
+  int ntiles[2], nkc[2];
+  int stage_bytes[2];     // g * scb of each phase
+};
+
+// Super-chunk range [kc0, kc0 + len) of K-slice ksl of ks = 2^ksl2.
+__device__ __forceinline__ void fused_kslice(int nkc, int ksl, int ksl2, int* kc0, int* len) {
+  *kc0 = (ksl * nkc) >> ksl2;
+  *len = (((ksl + 1) * nkc) >> ksl2) - *kc0;
+}
+
+// Move to the first unit at or after the cursor that exists; sets src / left.
+__device__ __forceinline__ void fused_cursor_settle(FusedCursor& q, const FusedRanges& rg, const FusedArgs& a,
+                                                 int warp, int warps, const int* rgb_s, const int* act_s,
+                                                 int nact) {
+  for (;;) {
+    if (q.p >= 2) return;
+    if (q.u >= q.u_end) {
+      ++q.p;
+      if (q.p < 2) {
+        q.u = rg.u0[q.p];
+        q.u_end = rg.u1[q.p];
+        q.v = warp;
+      }
+      continue;
+    }
+    const int nt = rg.ntiles[q.p];
+    const int seg = q.u / nt, t0 = q.u - seg * nt;
+    q.n = min(q.u_end - q.u, nt - t0);
+    const int ks = fused_ks(q.n, rg.nkc[q.p], warps);
+    q.ksl2 = __ffs(ks) - 1;
+    if (q.v >= q.n * ks) {
+      q.u += q.n;
+      q.v = warp;
+      continue;
+    }
+    const FusedProj& P = a.p[q.p];
+    const int e = act_s[fused_seg_expert(seg, rgb_s, nact)];
+    int kc0, len;
+    fused_kslice(rg.nkc[q.p], q.v & (ks - 1), q.ksl2, &kc0, &len);
+    const int tile = t0 + (q.v >> q.ksl2);
+    q.src = P.wpk + (size_t)e * P.L.expert_bytes + (size_t)tile * P.L.tile_bytes + (size_t)kc0 * P.L.scb;
+    q.left = len * P.L.scb;
+    return;
+  }
+}
+
+// Issue the producer's next stage into `slot` (every lane copies 16-byte
+// pieces) and advance; commits one cp.async group either way.
+__device__ __forceinline__ void fused_issue(FusedCursor& q, const FusedRanges& rg, const FusedArgs& a, uint8_t* slot,
+                                            int lane, int warp, int warps, const int* rgb_s, const int* act_s,
+                                            int nact) {
+  if (q.p < 2) {
+    const int bytes = min(rg.stage_bytes[q.p], q.left);
+    for (int off = lane * 16; off < bytes; off += 512) cp_async16(slot + off, q.src + off);
+    q.src += bytes;
+    q.left -= bytes;
+    if (q.left == 0) {
+      q.v += warps;
+      fused_cursor_settle(q, rg, a, warp, warps, rgb_s, act_s, nact);
+    }
+  }
+  cp_async_commit();
+}
+
 // ----------------------------------------------------------------------------
 // The kernel.
 // ----------------------------------------------------------------------------
 template <int B1, int B2, bool BF16, int SC>
-__global__ void __launch_bounds__(kFusedThreads, 2) fused_decode_kernel(const FusedArgs a) {
+__global__ void __launch_bounds__(kFusedMaxWarps * 32, 1) fused_decode_kernel(const FusedArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
+  constexpr int KT = SC / 16;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int NT = blockDim.x, W = NT >> 5;
   const int T = a.T, E = a.E, k = a.k, R = T * k;
   const int Kp_max = (a.p[0].L.nkc > a.p[1].L.nkc ? a.p[0].L.nkc : a.p[1].L.nkc) * SC;
-  const FusedPlan pl = fused_plan(R, E, fused_bop_bytes(Kp_max));
+  const FusedPlan pl = fused_plan(R, E, Kp_max, a.ng_max, a.sb, W);
   int* bc = reinterpret_cast<int*>(smem);                       // broadcast ints
   int* ids_s = reinterpret_cast<int*>(smem + pl.ids_off);
   float* w_s = reinterpret_cast<float*>(smem + pl.w_off);
@@ -449,15 +575,25 @@ __global__ void __launch_bounds__(kFusedThreads, 2) fused_decode_kernel(const Fu
   int* rgb_s = reinterpret_cast<int*>(smem + pl.rgb_off);      // row-group prefix over active experts
   uint32_t* bop = reinterpret_cast<uint32_t*>(smem + pl.bop_off);
   float* red = reinterpret_cast<float*>(smem + pl.bop_off);
+  uint8_t* ring = smem + pl.ring_off + (size_t)warp * kFusedStages * a.sb;
   int* done1 = a.sync + kSyncHeader;
-  int* done2 = done1 + E;
 
-  // ---- routing (every CTA, all tokens) ----
-  for (int t = warp; t < T; t += kFusedThreads / 32)
-    fused_route_token(a.logits + (size_t)t * E, E, k, a.normalize, ids_s + t * k, w_s + t * k);
-  for (int i = tid; i < E; i += kFusedThreads) cnt_s[i] = 0;
+  // ---- routing (every CTA, all tokens): the logits first land in the
+  //      (still empty) ring area with one coalesced pass ----
+  float* lg_s = reinterpret_cast<float*>(smem + pl.ring_off);
+  {
+    const int n4 = T * E / 4;   // E is a multiple of 4 on this path
+    const float4* src4 = reinterpret_cast<const float4*>(a.logits);
+    for (int i = tid; i < n4; i += NT) reinterpret_cast<float4*>(lg_s)[i] = __ldg(src4 + i);
+  }
+  for (int i = tid; i < E; i += NT) cnt_s[i] = 0;
   __syncthreads();
-  for (int r = tid; r < R; r += kFusedThreads) atomicAdd(&cnt_s[ids_s[r]], 1);
+  if (E <= 32) fused_route_all<1>(lg_s, T, E, k, a.normalize, ids_s, w_s, warp, W);
+  else if (E <= 64) fused_route_all<2>(lg_s, T, E, k, a.normalize, ids_s, w_s, warp, W);
+  else if (E <= 128) fused_route_all<4>(lg_s, T, E, k, a.normalize, ids_s, w_s, warp, W);
+  else fused_route_all<8>(lg_s, T, E, k, a.normalize, ids_s, w_s, warp, W);
+  __syncthreads();
+  for (int r = tid; r < R; r += NT) atomicAdd(&cnt_s[ids_s[r]], 1);
   __syncthreads();
   // ---- grouping: offsets, active experts, row-group prefix (warp 0) ----
   if (warp == 0) {
@@ -499,7 +635,7 @@ __global__ void __launch_bounds__(kFusedThreads, 2) fused_decode_kernel(const Fu
     for (int base = 0; base < R; base += 32) {
       const int r = base + lane;
       const int e = r < R ? ids_s[r] : -1;
-      const unsigned peers = __match_any_sync(0xffffffffu, e);
+      const unsigned peers = peers_of(e, id_bits(E));
       if (e >= 0) perm_s[cur_s[e] + __popc(peers & lt)] = r;
       __syncwarp();
       if (e >= 0 && lane == __ffs(peers) - 1) cur_s[e] += __popc(peers);
@@ -509,18 +645,42 @@ __global__ void __launch_bounds__(kFusedThreads, 2) fused_decode_kernel(const Fu
   __syncthreads();
   const int nact = bc[0], NRG = bc[1];
 
+  // ---- this CTA's share of the tiles of each phase; start the weight ring ----
+  FusedRanges rg;
+  for (int p = 0; p < 2; ++p) {
+    rg.ntiles[p] = a.p[p].ntiles;
+    rg.nkc[p] = a.p[p].L.nkc;
+    rg.stage_bytes[p] = a.p[p].g * a.p[p].L.scb;
+    const long long N = (long long)NRG * rg.ntiles[p];
+    rg.u0[p] = (int)(N * blockIdx.x / gridDim.x);
+    rg.u1[p] = (int)(N * (blockIdx.x + 1) / gridDim.x);
+  }
+  FusedCursor prod;
+  prod.p = 0;
+  prod.u = rg.u0[0];
+  prod.u_end = rg.u1[0];
+  prod.v = warp;
+  prod.n = 0;
+  prod.ksl2 = 0;
+  prod.src = nullptr;
+  prod.left = 0;
+  fused_cursor_settle(prod, rg, a, warp, W, rgb_s, act_s, nact);
+  for (int s = 0; s < kFusedStages - 1; ++s)
+    fused_issue(prod, rg, a, ring + s * a.sb, lane, warp, W, rgb_s, act_s, nact);
+  int stage = 0;   // ring stages this warp has consumed
+
   // CTA 0 keeps the routing and the row-group work-list for the host.
   if (blockIdx.x == 0) {
-    for (int r = tid; r < R; r += kFusedThreads) {
+    for (int r = tid; r < R; r += NT) {
       a.ids[r] = ids_s[r];
       a.w[r] = w_s[r];
       a.perm[r] = perm_s[r];
     }
-    for (int e = tid; e <= E; e += kFusedThreads) {
+    for (int e = tid; e <= E; e += NT) {
       a.offsets[e] = off_s[e];
       if (e < E) a.counts[e] = cnt_s[e];
     }
-    for (int ai = tid; ai < nact; ai += kFusedThreads) {
+    for (int ai = tid; ai < nact; ai += NT) {
       const int e = act_s[ai], c = cnt_s[e];
       for (int g = 0; g * kFusedRowsPerGroup < c; ++g) {
         Item it;
@@ -537,10 +697,6 @@ __global__ void __launch_bounds__(kFusedThreads, 2) fused_decode_kernel(const Fu
     }
   }
 
-  // ---- the work-item loop ----
-  const int ntg1 = (a.p[0].ntiles + a.p[0].tpi - 1) / a.p[0].tpi;
-  const int ntg2 = a.n_mg;
-  const int n1 = NRG * ntg1, n2 = NRG * ntg2;
   // Fractional zero point: the half-unit magic offset (M/2 + z, M/2 + z);
   // 8-bit codes in bf16 take the integer pair (z, z) instead.
   uint32_t zoff_half = 0u, zoff_int = 0u;
@@ -548,258 +704,274 @@ __global__ void __launch_bounds__(kFusedThreads, 2) fused_decode_kernel(const Fu
     zoff_half = half_magic_offset<BF16>(a.zp_offset);
     zoff_int = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(a.zp_offset)) * 0x00010001u;
   }
-  int staged = -1;   // (phase, row group) whose rows are in bop
-  for (;;) {
-    if (tid == 0) bc[2] = atomicAdd(&a.sync[0], 1);
-    __syncthreads();
-    const int ticket = bc[2];
-    if (ticket >= n1 + n2) break;
-    const int ph = ticket < n1 ? 0 : 1;
-    const int tt = ph == 0 ? ticket : ticket - n1;
-    const int ntg = ph == 0 ? ntg1 : ntg2;
-    const int rgg = tt / ntg, tg = tt % ntg;
-    // active expert of row group rgg (binary search over the prefix)
-    int lo = 0, hi = nact - 1;
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if (rgb_s[mid] <= rgg) lo = mid; else hi = mid - 1;
-    }
-    const int ai = lo, e = act_s[ai], c = cnt_s[e];
-    const int rg = rgg - rgb_s[ai];
-    const int j0 = rg * kFusedRowsPerGroup;
-    const int nrows = min(kFusedRowsPerGroup, c - j0);
-    const int NG = (nrows + 7) >> 3;
+  const bool offs = a.zp_mode == QMOE_ZP_OFFSET;
+  const bool uint8_zp = a.zp_mode == QMOE_ZP_UINT8;
+  int staged = -1;   // (phase, segment) whose rows are in bop
+
+  for (int ph = 0; ph < 2; ++ph) {
     const FusedProj& P = a.p[ph];
-    const int K = P.K;
-    const int Kp = P.L.nkc * SC;
-    bool ok = true;
+    const int nt = P.ntiles, nkc = P.L.nkc, K = P.K, Kp = nkc * SC;
+    const FusedGeom gm = fused_geom(P.L);
+    for (int u = rg.u0[ph]; u < rg.u1[ph];) {
+      // ---- one block: tiles [t0, t0 + n) of segment seg ----
+      const int seg = u / nt, t0 = u % nt;
+      const int n = min(rg.u1[ph] - u, nt - t0);
+      const int ks = fused_ks(n, nkc, W);
+      const int ksl2 = __ffs(ks) - 1;
+      const int ai = fused_seg_expert(seg, rgb_s, nact);
+      const int e = act_s[ai], c = cnt_s[e];
+      const int j0 = (seg - rgb_s[ai]) * kFusedRowsPerGroup;
+      const int nrows = min(kFusedRowsPerGroup, c - j0);
+      const int NG = (nrows + 7) >> 3;
 
-    if (ph == 1) {
-      // fc2 of this expert needs all its fc1 items
-      const int nrg_e = rgb_s[ai + 1] - rgb_s[ai];
-      if (tid == 0) {
-        const bool w8 = a.inject_stall ? fused_wait_geq(a.sync + 2, 1, a.wait)
-                                       : fused_wait_geq(done1 + e, nrg_e * ntg1, a.wait);
-        bc[3] = w8 ? 1 : 0;
+      if (ph == 1) {
+        // the h rows of this segment: every fc1 tile of the segment done
+        if (tid == 0)
+          bc[3] = (a.inject_stall ? fused_wait_geq(a.sync + 2, 1, a.wait)
+                                  : fused_wait_geq(done1 + seg, rg.ntiles[0], a.wait)) ? 1 : 0;
+        __syncthreads();
+      }
+      const int key = ph * 65536 + seg;
+      if (key != staged) {
+        const int vrow = K / 8;   // 16-byte vectors per row
+        const int nvec = nrows * vrow;
+        for (int i = tid; i < nvec; i += NT) {
+          const int nn = i / vrow, kv = i % vrow;
+          const int r = perm_s[off_s[e] + j0 + nn];
+          const uint4 v = ph == 0 ? ld_nc_v4(static_cast<const uint16_t*>(a.x) + (size_t)(r / k) * K + kv * 8)
+                                  : ld_cg_v4(static_cast<const uint16_t*>(a.hbuf) + (size_t)r * K + kv * 8);
+          const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const int kk = kv * 8 + 2 * q, kt = kk >> 4, within = kk & 15;
+            const int t4 = (within & 7) >> 1, h8 = within >> 3;
+            bop[((kt * NG + (nn >> 3)) * 32 + (nn & 7) * 4 + t4) * 2 + h8] = w4[q];
+          }
+        }
+        if (Kp > K) {
+          // K padding meets zero-code weights that are not zero: zero it
+          const int pad2 = (Kp - K) / 2;
+          for (int i = tid; i < NG * 8 * pad2; i += NT) {
+            const int nn = i / pad2, kk = K + 2 * (i % pad2);
+            const int kt = kk >> 4, within = kk & 15;
+            const int t4 = (within & 7) >> 1, h8 = within >> 3;
+            bop[((kt * NG + (nn >> 3)) * 32 + (nn & 7) * 4 + t4) * 2 + h8] = 0u;
+          }
+        }
+        staged = key;
       }
       __syncthreads();
-      ok = bc[3] != 0;
-    }
 
-    // ---- stage the item's rows (x for fc1, h for fc2) in B-fragment order ----
-    const int key = ph * 65536 + rgg;
-    if (ok && key != staged) {
-      const int vrow = K / 8;   // 16-byte vectors per row
-      const int nvec = nrows * vrow;
-      for (int i = tid; i < nvec; i += kFusedThreads) {
-        const int n = i / vrow, kv = i % vrow;
-        const int r = perm_s[off_s[e] + j0 + n];
-        uint4 v;
-        if (ph == 0)
-          v = ld_nc_v4(static_cast<const uint16_t*>(a.x) + (size_t)(r / k) * K + kv * 8);
-        else
-          v = ld_cg_v4(static_cast<const uint16_t*>(a.hbuf) + (size_t)r * K + kv * 8);
-        const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+      const bool gated1 = ph == 0 && a.gated;
+      const uint32_t zo = ((ph == 0 ? B1 : B2) == 8 && BF16) ? zoff_int : zoff_half;
+      float acc[2][2][4];
+      int my_tile = -1, my_ksl = 0;
+      auto epilogue = [&](int tile) {
+        const int g = lane >> 2, t4 = lane & 3;
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const int kk = kv * 8 + 2 * q, kt = kk >> 4, within = kk & 15;
-          const int t4 = (within & 7) >> 1, h8 = within >> 3;
-          bop[((kt * NG + (n >> 3)) * 32 + (n & 7) * 4 + t4) * 2 + h8] = w4[q];
-        }
-      }
-      if (Kp > K) {
-        // K padding meets zero-code weights that are not zero: zero it
-        const int pad2 = (Kp - K) / 2;
-        for (int i = tid; i < NG * 8 * pad2; i += kFusedThreads) {
-          const int n = i / pad2, kk = K + 2 * (i % pad2);
-          const int kt = kk >> 4, within = kk & 15;
-          const int t4 = (within & 7) >> 1, h8 = within >> 3;
-          bop[((kt * NG + (n >> 3)) * 32 + (n & 7) * 4 + t4) * 2 + h8] = 0u;
-        }
-      }
-      staged = key;
-    }
-    __syncthreads();
-
-    // ---- stream this warp's share of the item's tiles ----
-    const int tile = tg * P.tpi + warp / P.ks;
-    const int ksl = warp % P.ks;
-    const bool gated1 = ph == 0 && a.gated;
-    const bool act_warp = ok && tile < P.ntiles;
-    FusedAcc fa;
+        for (int nn = 0; nn < 2; ++nn) {
 #pragma unroll
-    for (int s = 0; s < 2; ++s)
-#pragma unroll
-      for (int n = 0; n < 2; ++n)
-#pragma unroll
-        for (int q = 0; q < 4; ++q) fa.v[s][n][q] = 0.f;
-    if (act_warp) {
-      const int kc0 = ksl * P.L.nkc / P.ks, kc1 = (ksl + 1) * P.L.nkc / P.ks;
-      const uint8_t* src = P.wpk + (size_t)e * P.L.expert_bytes + (size_t)tile * P.L.tile_bytes +
-                           (size_t)kc0 * P.L.scb;
-      const FusedGeom gm = fused_geom(P.L);
-      const uint32_t* bop_lane = bop + (size_t)kc0 * (SC / 16) * NG * 64 + lane * 2;
-      if (ph == 0) {
-        const uint32_t zo = (B1 == 8 && BF16) ? zoff_int : zoff_half;
-        if (gated1)
-          fa = fused_stream_zp<B1, BF16, SC, 2>(src, kc1 - kc0, gm, bop_lane, NG, a.zp_mode, zo);
-        else
-          fa = fused_stream_zp<B1, BF16, SC, 1>(src, kc1 - kc0, gm, bop_lane, NG, a.zp_mode, zo);
-      } else {
-        const uint32_t zo = (B2 == 8 && BF16) ? zoff_int : zoff_half;
-        fa = fused_stream_zp<B2, BF16, SC, 1>(src, kc1 - kc0, gm, bop_lane, NG, a.zp_mode, zo);
-      }
-    }
-    __syncthreads();   // every warp is done with bop
-    if (P.ks > 1) staged = -1;   // the split-K reduction reuses bop
-    auto& acc = fa.v;
-
-    // ---- split-K reduction (fixed order) ----
-    if (P.ks > 1) {
-      if (act_warp && ksl != 0) {
-        float* dst = red + (warp * 32 + lane) * 16;
-#pragma unroll
-        for (int s = 0; s < 2; ++s)
-#pragma unroll
-          for (int n = 0; n < 2; ++n)
-#pragma unroll
-            for (int q = 0; q < 4; ++q) dst[(s * 2 + n) * 4 + q] = acc[s][n][q];
-      }
-      __syncthreads();
-      if (act_warp && ksl == 0) {
-        for (int o = 1; o < P.ks; ++o) {
-          const float* srcr = red + ((warp + o) * 32 + lane) * 16;
-#pragma unroll
-          for (int s = 0; s < 2; ++s)
-#pragma unroll
-            for (int n = 0; n < 2; ++n)
-#pragma unroll
-              for (int q = 0; q < 4; ++q) acc[s][n][q] += srcr[(s * 2 + n) * 4 + q];
-        }
-      }
-    }
-
-    // ---- epilogue: acc[s][n][q] = row g + 8 (q >> 1) of the tile, routed row n*8 + 2t + (q & 1) ----
-    if (act_warp && ksl == 0) {
-      const int g = lane >> 2, t4 = lane & 3;
-#pragma unroll
-      for (int n = 0; n < 2; ++n) {
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const int row = n * 8 + 2 * t4 + (q & 1);
-          const int f = tile * 16 + g + 8 * (q >> 1);
-          if (n < NG && row < nrows) {
-            const int r = perm_s[off_s[e] + j0 + row];
-            if (ph == 0) {
-              float hv;
-              if (gated1) {
-                float gv = acc[0][n][q], uv = acc[1][n][q];
-                if (P.bias) {
-                  gv += P.bias[((size_t)e * a.I + f) * 2];
-                  uv += P.bias[((size_t)e * a.I + f) * 2 + 1];
+          for (int q = 0; q < 4; ++q) {
+            const int row = nn * 8 + 2 * t4 + (q & 1);
+            const int f = tile * 16 + g + 8 * (q >> 1);
+            if (nn < NG && row < nrows) {
+              const int r = perm_s[off_s[e] + j0 + row];
+              if (ph == 0) {
+                float hv;
+                if (gated1) {
+                  float gv = acc[0][nn][q], uv = acc[1][nn][q];
+                  if (P.bias) {
+                    gv += P.bias[((size_t)e * a.I + f) * 2];
+                    uv += P.bias[((size_t)e * a.I + f) * 2 + 1];
+                  }
+                  hv = glu(a.act, gv, uv);
+                } else {
+                  float vv = acc[0][nn][q];
+                  if (P.bias) vv += P.bias[(size_t)e * a.I + f];
+                  hv = act_single(a.act, vv);
                 }
-                hv = glu(a.act, gv, uv);
+                if (BF16) static_cast<__nv_bfloat16*>(a.hbuf)[(size_t)r * a.I + f] = __float2bfloat16_rn(hv);
+                else static_cast<__half*>(a.hbuf)[(size_t)r * a.I + f] = __float2half_rn(hv);
               } else {
-                float v = acc[0][n][q];
-                if (P.bias) v += P.bias[(size_t)e * a.I + f];
-                hv = act_single(a.act, v);
+                float vv = acc[0][nn][q];
+                if (P.bias) vv += P.bias[(size_t)e * a.H + f];
+                a.ybuf[(size_t)r * a.H + f] = vv;
               }
-              if (BF16) static_cast<__nv_bfloat16*>(a.hbuf)[(size_t)r * a.I + f] = __float2bfloat16_rn(hv);
-              else static_cast<__half*>(a.hbuf)[(size_t)r * a.I + f] = __float2half_rn(hv);
-            } else {
-              float v = acc[0][n][q];
-              if (P.bias) v += P.bias[(size_t)e * a.H + f];
-              a.ybuf[(size_t)r * a.H + f] = v;
             }
           }
         }
-      }
-      __threadfence();
-    }
-    __syncthreads();
+      };
 
-    // ---- completion: fc1 -> per-expert counter; fc2 -> per output-row group,
-    //      the last item of a group adds the k slots in order ----
-    if (tid == 0) {
-      __threadfence();
-      if (ph == 0) {
-        atomicAdd(done1 + e, 1);
-        bc[4] = 0;
+      for (int v = warp; v < n * ks; v += W) {
+        const int tile = t0 + (v >> ksl2), ksl = v & (ks - 1);
+        int kc0, len;
+        fused_kslice(nkc, ksl, ksl2, &kc0, &len);
+#pragma unroll
+        for (int s = 0; s < 2; ++s)
+#pragma unroll
+          for (int nn = 0; nn < 2; ++nn)
+#pragma unroll
+            for (int q = 0; q < 4; ++q) acc[s][nn][q] = 0.f;
+        for (int cc = 0; cc < len;) {
+          const int nck = min(P.g, len - cc);
+          // stage `stage` of the ring holds super-chunks [kc0 + cc, kc0 + cc + nck)
+          // stages 0..stage have landed (the kFusedStages - 2 newer ones may not)
+          cp_async_wait<kFusedStages - 2>();
+          __syncwarp();
+          const uint8_t* slot = ring + (stage % kFusedStages) * a.sb;
+          // refill the stage consumed last (the slot before this one)
+          fused_issue(prod, rg, a, ring + ((stage + kFusedStages - 1) % kFusedStages) * a.sb, lane, warp, W, rgb_s, act_s,
+                      nact);
+          for (int x = 0; x < nck; ++x) {
+            const uint8_t* ch = slot + x * gm.scb;
+            const uint32_t* bl = bop + (size_t)(kc0 + cc + x) * KT * NG * 64 + lane * 2;
+            if (ph == 0) {
+              if (gated1) {
+                FusedChunk<B1, SC, 2> cr;
+                fused_load_chunk<B1, SC, 2>(cr, ch, gm, lane);
+                if (offs) fused_compute_chunk<B1, BF16, SC, 2, true>(cr, bl, NG, false, zo, acc);
+                else fused_compute_chunk<B1, BF16, SC, 2, false>(cr, bl, NG, uint8_zp, zo, acc);
+              } else {
+                FusedChunk<B1, SC, 1> cr;
+                fused_load_chunk<B1, SC, 1>(cr, ch, gm, lane);
+                if (offs) fused_compute_chunk<B1, BF16, SC, 1, true>(cr, bl, NG, false, zo, acc);
+                else fused_compute_chunk<B1, BF16, SC, 1, false>(cr, bl, NG, uint8_zp, zo, acc);
+              }
+            } else {
+              FusedChunk<B2, SC, 1> cr;
+              fused_load_chunk<B2, SC, 1>(cr, ch, gm, lane);
+              if (offs) fused_compute_chunk<B2, BF16, SC, 1, true>(cr, bl, NG, false, zo, acc);
+              else fused_compute_chunk<B2, BF16, SC, 1, false>(cr, bl, NG, uint8_zp, zo, acc);
+            }
+          }
+          __syncwarp();
+          ++stage;
+          cc += nck;
+        }
+        if (ks == 1) epilogue(tile);
+        else {
+          my_tile = tile;
+          my_ksl = ksl;
+        }
+      }
+      __syncthreads();   // every warp is done with bop
+
+      // ---- split-K partials, added in a fixed order ----
+      if (ks > 1) {
+        if (my_tile >= 0 && my_ksl != 0) {
+          float* dst = red + (warp * 32 + lane) * 16;
+#pragma unroll
+          for (int s = 0; s < 2; ++s)
+#pragma unroll
+            for (int nn = 0; nn < 2; ++nn)
+#pragma unroll
+              for (int q = 0; q < 4; ++q) dst[(s * 2 + nn) * 4 + q] = acc[s][nn][q];
+        }
+        __syncthreads();
+        if (my_tile >= 0 && my_ksl == 0) {
+          for (int o = 1; o < ks; ++o) {
+            const float* srcr = red + ((warp + o) * 32 + lane) * 16;
+#pragma unroll
+            for (int s = 0; s < 2; ++s)
+#pragma unroll
+              for (int nn = 0; nn < 2; ++nn)
+#pragma unroll
+                for (int q = 0; q < 4; ++q) acc[s][nn][q] += srcr[(s * 2 + nn) * 4 + q];
+          }
+          epilogue(my_tile);
+        }
+        staged = -1;   // bop now holds partials
+      }
+      __syncthreads();   // the block's h / y stores are issued
+
+      // ---- completion: fc1 publishes the segment's h rows (release) ----
+      if (ph == 0 && tid == 0)
+        asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(done1 + seg), "r"(n) : "memory");
+      u += n;
+    }
+  }
+  cp_async_wait<0>();   // the producer's trailing (empty) groups
+
+  // ---- every y row is written once all CTAs arrive; then each CTA adds the
+  //      k slots in order for its equal share of the outputs ----
+  __syncthreads();
+  if (tid == 0) {
+    asm volatile("red.release.gpu.global.add.s32 [%0], 1;" ::"l"(a.sync + 3) : "memory");
+    fused_wait_geq(a.sync + 3, (int)gridDim.x, a.wait);
+  }
+  __syncthreads();
+  {
+    const int H4 = a.H / 4;
+    const long long N = (long long)T * H4;
+    const int i0 = (int)(N * blockIdx.x / gridDim.x), i1 = (int)(N * (blockIdx.x + 1) / gridDim.x);
+    for (int idx = i0 + tid; idx < i1; idx += NT) {
+      const int t = idx / H4, m = 4 * (idx % H4);
+      float4 s4 = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int j = 0; j < k; ++j) {
+        const int r = t * k + j;
+        const float wr = w_s[r];
+        const uint4 uu = ld_cg_v4(a.ybuf + (size_t)r * a.H + m);
+        s4.x = fmaf(wr, __uint_as_float(uu.x), s4.x);
+        s4.y = fmaf(wr, __uint_as_float(uu.y), s4.y);
+        s4.z = fmaf(wr, __uint_as_float(uu.z), s4.z);
+        s4.w = fmaf(wr, __uint_as_float(uu.w), s4.w);
+      }
+      const size_t o = (size_t)t * a.H + m;
+      if (BF16) {
+        store_d<QMOE_BF16>(a.out, o, s4.x); store_d<QMOE_BF16>(a.out, o + 1, s4.y);
+        store_d<QMOE_BF16>(a.out, o + 2, s4.z); store_d<QMOE_BF16>(a.out, o + 3, s4.w);
       } else {
-        bc[4] = atomicAdd(done2 + tg, 1) == NRG - 1 ? 1 : 0;
+        store_d<QMOE_F16>(a.out, o, s4.x); store_d<QMOE_F16>(a.out, o + 1, s4.y);
+        store_d<QMOE_F16>(a.out, o + 2, s4.z); store_d<QMOE_F16>(a.out, o + 3, s4.w);
       }
     }
-    __syncthreads();
-    if (bc[4]) {
-      __threadfence();
-      const int m0 = tg * a.p[1].tpi * 16;
-      const int m1 = min(a.H, m0 + a.p[1].tpi * 16);
-      const int w4n = (m1 - m0) / 4;
-      for (int i = tid; i < T * w4n; i += kFusedThreads) {
-        const int t = i / w4n, m = m0 + 4 * (i % w4n);
-        float4 s4 = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int j = 0; j < k; ++j) {
-          const int r = t * k + j;
-          const float wr = w_s[r];
-          const uint4 u = ld_cg_v4(a.ybuf + (size_t)r * a.H + m);
-          s4.x = fmaf(wr, __uint_as_float(u.x), s4.x);
-          s4.y = fmaf(wr, __uint_as_float(u.y), s4.y);
-          s4.z = fmaf(wr, __uint_as_float(u.z), s4.z);
-          s4.w = fmaf(wr, __uint_as_float(u.w), s4.w);
-        }
-        const size_t o = (size_t)t * a.H + m;
-        if (BF16) {
-          store_d<QMOE_BF16>(a.out, o, s4.x); store_d<QMOE_BF16>(a.out, o + 1, s4.y);
-          store_d<QMOE_BF16>(a.out, o + 2, s4.z); store_d<QMOE_BF16>(a.out, o + 3, s4.w);
-        } else {
-          store_d<QMOE_F16>(a.out, o, s4.x); store_d<QMOE_F16>(a.out, o + 1, s4.y);
-          store_d<QMOE_F16>(a.out, o + 2, s4.z); store_d<QMOE_F16>(a.out, o + 3, s4.w);
-        }
-      }
-    }
-    __syncthreads();
   }
 
   // ---- the last CTA out clears the counters for the next launch ----
   __syncthreads();
   if (tid == 0) {
-    __threadfence();
-    bc[5] = atomicAdd(&a.sync[1], 1) == (int)gridDim.x - 1 ? 1 : 0;
+    int old;
+    asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], 1;" : "=r"(old) : "l"(a.sync + 1) : "memory");
+    bc[5] = old == (int)gridDim.x - 1 ? 1 : 0;
   }
   __syncthreads();
   if (bc[5]) {
-    __threadfence();
-    const int n = kSyncHeader + E + a.n_mg;
-    for (int i = tid; i < n; i += kFusedThreads) a.sync[i] = 0;
+    const int nsync = kSyncHeader + a.max_seg;
+    for (int i = tid; i < nsync; i += NT) a.sync[i] = 0;
     __threadfence();
   }
 }
 
-}  // namespace qmoe
-
-namespace qmoe {
-
 // Launch of one instantiated width pair (explicitly instantiated in
-// qmoe_fused_w<b1><b2>.cu).
+// qmoe_fused_w<b1><b2>.cu): cooperative, so every CTA is resident.
 template <int B1, int B2>
-cudaError_t launch_fused_pair(const FusedArgs& a, bool bf16, int sc, int grid, int smem, cudaStream_t s) {
+cudaError_t launch_fused_pair(const FusedArgs& a, bool bf16, int sc, int grid, int warps, int smem, cudaStream_t s) {
   auto go = [&](auto kern) {
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (err != cudaSuccess) return err;
-    kern<<<grid, kFusedThreads, smem, s>>>(a);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(warps * 32);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, a);
   };
   if (bf16) return sc == 64 ? go(fused_decode_kernel<B1, B2, true, 64>) : go(fused_decode_kernel<B1, B2, true, 128>);
   return sc == 64 ? go(fused_decode_kernel<B1, B2, false, 64>) : go(fused_decode_kernel<B1, B2, false, 128>);
 }
 
-}  // namespace qmoe
-
-namespace qmoe {
 // Host side (qmoe_fused.cu).
 bool fused_widths_supported(int b1, int b2);
-int fused_smem_bytes(int R, int E, int Kp_max);
-void fused_item_shape(int ntiles, int nkc, long long nrg_est, int grid, int* tpi, int* ks);
-cudaError_t launch_fused(const FusedArgs& a, int b1, int b2, bool bf16, int sc, int grid, int smem,
+// Bytes per ring stage and super-chunks per stage of each projection for the
+// shared memory left after `fixed_bytes`; false if a stage cannot hold one
+// super-chunk.
+bool fused_ring_shape(int budget, int fixed_bytes, int warps, int scb1, int scb2, int* sb, int* g1, int* g2);
+cudaError_t launch_fused(const FusedArgs& a, int b1, int b2, bool bf16, int sc, int grid, int warps, int smem,
                          cudaStream_t s);
+
 }  // namespace qmoe

@@ -247,6 +247,28 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
   return false;
 }
 
+// Lanes of the warp holding the same expert id as this lane (ids in
+// [0, 2^nbits) or negative = none): one ballot per bit of the id, the same
+// mask match.any.sync gives, without its cost.  Negative ids match only
+// other negative ids.
+__device__ __forceinline__ unsigned peers_of(int e, int nbits) {
+  const unsigned valid = __ballot_sync(0xffffffffu, e >= 0);
+  unsigned peers = e >= 0 ? valid : ~valid;
+  for (int b = 0; b < nbits; ++b) {
+    const bool bit = (e >> b) & 1;
+    const unsigned m = __ballot_sync(0xffffffffu, bit);
+    peers &= bit ? m : ~m;
+  }
+  return peers;
+}
+
+// Bits of an expert id for E experts.
+__host__ __device__ __forceinline__ int id_bits(int E) {
+  int b = 0;
+  while ((1 << b) < E) ++b;
+  return b;
+}
+
 __device__ __forceinline__ void pdl_wait() {
   asm volatile("griddepcontrol.wait;" ::: "memory");
 }

@@ -165,11 +165,10 @@ cudaError_t launch_repack_gemm(const GemmRepackArgs& a, cudaStream_t s) {
 // Gather of x into the tiled token layout (fc1 B operand), and the combine of
 // the fp32 accumulator.
 // ----------------------------------------------------------------------------
-// kGatherParts CTAs per GEMM-class item (grid y), each taking every
-// kGatherParts-th group of 16-byte chunks (8 values) of the item's rows;
-// chunks past H (K padding up to 64) and rows past the item's count up to the
-// next multiple of 8 (copied with the tile) are written as zeros, so the MMA
-// never reads undefined values.
+// kGatherParts CTAs per GEMM-class item (grid y); their warps take the item's
+// rows in turn; chunks past H (K padding up to 64) and rows past the item's
+// count up to the next multiple of 8 (copied with the tile) are written as
+// zeros, so the MMA never reads undefined values.
 constexpr int kGatherParts = 8;
 
 __global__ void __launch_bounds__(256) gather_tiles_kernel(const void* __restrict__ x, const int* __restrict__ perm,
@@ -179,35 +178,34 @@ __global__ void __launch_bounds__(256) gather_tiles_kernel(const void* __restric
   if ((int)blockIdx.x >= *n_items) return;
   const Item it = items[blockIdx.x];
   const int ksteps = (H + 63) / 64;
-  const int cpr = ksteps * 8;                 // chunks per row (padded)
+  const int cpr = ksteps * 8;                 // 16-byte chunks per row (padded to 64 values)
   const int hv = H / 8;                       // real chunks per row
+  const int rows = (it.rows + 7) & ~7;        // rows up to a multiple of 8 (the copy unit)
+  const int lane = threadIdx.x & 31;
+  const int nw = (int)gridDim.y * (blockDim.x >> 5);
   const uint4* src = static_cast<const uint4*>(x);
-  const int n = ((it.rows + 7) & ~7) * cpr;   // rows up to a multiple of 8 (the copy unit)
+  uint8_t* tile0 = xt + tok_tile_offset(blockIdx.x, ksteps, 0);
+  // A warp copies whole rows: one token lookup per row, lanes across the row
+  // (coalesced 16-byte loads; each 8-lane group stores one swizzled 128-byte
+  // row of a k-step tile).
   constexpr int U = 4;
-  const int stride = (int)(gridDim.y * blockDim.x);
-  for (int base = (int)(blockIdx.y * blockDim.x + threadIdx.x); base < n; base += U * stride) {
-    uint4 v[U];
-    int cc[U], ch[U];
+  for (int row = (int)blockIdx.y * (blockDim.x >> 5) + (threadIdx.x >> 5); row < rows; row += nw) {
+    const bool real = row < it.rows;
+    const uint4* srow = src + (size_t)(real ? perm[it.start + row] / k : 0) * hv;
+    uint8_t* drow = tile0 + row * 128;
+    for (int c0 = lane; c0 < cpr; c0 += 32 * U) {
+      uint4 v[U];
 #pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const int i = base + u * stride;
-      cc[u] = -1;
-      if (i < n) {
-        cc[u] = i / cpr;
-        ch[u] = i % cpr;
-        v[u] = make_uint4(0u, 0u, 0u, 0u);
-        if (ch[u] < hv && cc[u] < it.rows) {
-          const int t = perm[it.start + cc[u]] / k;
-          v[u] = src[(size_t)t * hv + ch[u]];
-        }
+      for (int u = 0; u < U; ++u) {
+        const int c = c0 + 32 * u;
+        v[u] = (real && c < hv) ? srow[c] : make_uint4(0u, 0u, 0u, 0u);
       }
-    }
 #pragma unroll
-    for (int u = 0; u < U; ++u) {
-      if (cc[u] < 0) continue;
-      uint8_t* dst = xt + tok_tile_offset(blockIdx.x, ksteps, ch[u] >> 3) + cc[u] * 128 +
-                     (((ch[u] & 7) ^ (cc[u] & 7)) << 4);
-      *reinterpret_cast<uint4*>(dst) = v[u];
+      for (int u = 0; u < U; ++u) {
+        const int c = c0 + 32 * u;
+        if (c < cpr)
+          *reinterpret_cast<uint4*>(drow + (size_t)(c >> 3) * kTokTileBytes + (((c & 7) ^ (row & 7)) << 4)) = v[u];
+      }
     }
   }
   pdl_launch_dependents();
@@ -843,7 +841,7 @@ __global__ void __launch_bounds__((Ring<DEC, BITS>::threads), 1)
         int my_tok = 0;
         float my_w = 0.f;
         const bool col_ok = c0 + lane < it.rows;
-        if (EPI == 0 && col_ok) {
+        if (EPI == 0 && col_ok && !a.ybuf) {
           const int route = a.perm[it.start + c0 + lane];
           my_tok = route / a.k;
           my_w = a.w[route];
@@ -903,11 +901,19 @@ __global__ void __launch_bounds__((Ring<DEC, BITS>::threads), 1)
           const float* src = tile32 + lane * kEpiPitch;
           if (EPI == 0) {
             if (col_ok && mbase < a.N_out) {
-              float* dst = a.out_acc + (size_t)my_tok * a.N_out + mbase;
+              if (a.ybuf) {
+                // slot-ordered combine later: the y row of this route, grouped order
+                float* dst = a.ybuf + (size_t)(it.start + c0 + lane) * a.N_out + mbase;
 #pragma unroll
-              for (int i = 0; i < 8; ++i) {
-                const float4 y = *reinterpret_cast<const float4*>(src + 4 * i);
-                red_add_v4_f32(dst + 4 * i, my_w * y.x, my_w * y.y, my_w * y.z, my_w * y.w);
+                for (int i = 0; i < 8; ++i)
+                  *reinterpret_cast<float4*>(dst + 4 * i) = *reinterpret_cast<const float4*>(src + 4 * i);
+              } else {
+                float* dst = a.out_acc + (size_t)my_tok * a.N_out + mbase;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                  const float4 y = *reinterpret_cast<const float4*>(src + 4 * i);
+                  red_add_v4_f32(dst + 4 * i, my_w * y.x, my_w * y.y, my_w * y.z, my_w * y.w);
+                }
               }
             }
           } else {

@@ -62,7 +62,9 @@ struct GemmArgs {
   const uint8_t* btiles;   // B operand in the tiled token layout (L.ksteps steps per item)
   uint8_t* htiles;         // fc1: h written in the tiled token layout for fc2
   int h_ksteps;            // fc1: k-steps of h (ceil(I / 64))
-  float* out_acc;          // fc2: fp32 [T, H] combine accumulator
+  float* out_acc;          // fc2: fp32 [T, H] combine accumulator (fp32 reductions of w * y)
+  float* ybuf;             // fc2, or null: y rows [R, H] fp32 in grouped order instead, for the
+                           // slot-ordered (deterministic) combine
   const int* perm;
   const float* w;
   int k;

@@ -135,6 +135,7 @@ __global__ void __launch_bounds__(1024) group_kernel(const RouteArgs a, int do_r
   int* ws = off + E;           // [32]
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int R = a.T * a.k;
+  const int nb = id_bits(E);
 
   if (do_route) {
     for (int t = warp; t < a.T; t += 32)
@@ -161,7 +162,7 @@ __global__ void __launch_bounds__(1024) group_kernel(const RouteArgs a, int do_r
 #pragma unroll
     for (int u = 0; u < kU; ++u) {
       const int e = ev[u];
-      const unsigned peers = __match_any_sync(0xffffffffu, e);
+      const unsigned peers = peers_of(e, nb);
       if (e >= 0 && lane == __ffs(peers) - 1) cnt[warp * E + e] += __popc(peers);
       __syncwarp();
     }
@@ -202,7 +203,7 @@ __global__ void __launch_bounds__(1024) group_kernel(const RouteArgs a, int do_r
     for (int u = 0; u < kU; ++u) {
       const int r = base + 32 * u + lane;
       const int e = ev[u];
-      const unsigned peers = __match_any_sync(0xffffffffu, e);
+      const unsigned peers = peers_of(e, nb);
       if (e >= 0) {
         const int p = cnt[warp * E + e] + __popc(peers & lt);
         a.perm[p] = r;
