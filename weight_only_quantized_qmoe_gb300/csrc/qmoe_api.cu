@@ -306,6 +306,8 @@ void trace(qmoe_layer* l, int i, cudaStream_t s) {
 // CTA's barriers are then covered by the other's work), else one 16-warp CTA.
 constexpr int kFusedSmemTwoPerSm = 113 * 1024;
 constexpr int kFusedSmemOnePerSm = 227 * 1024;
+// Weights up to this size are prefetched into the L2 during routing.
+constexpr size_t kFusedPrefetchMaxBytes = 64ull << 20;
 // Smallest ring stage worth two CTAs per SM (16 warps x 3 stages in flight).
 constexpr int kFusedMinStageTwoPerSm = 1024;
 
@@ -396,6 +398,9 @@ qmoe_status forward_fused(qmoe_layer* l, const void* x, const float* logits, voi
   a.sb = fs.sb;
   a.wait = WaitCfg{l->status, l->wait_limit};
   a.inject_stall = l->inject_stall;
+  // weights that fit the L2 (129 MB) with room to spare are prefetched while
+  // the CTAs route (decode layouts are multiples of 16 bytes per expert)
+  a.prefetch_l2 = (size_t)l->E * (l->proj[0].L.expert_bytes + l->proj[1].L.expert_bytes) <= kFusedPrefetchMaxBytes;
   l->last_T = T;
   l->last_path = QMOE_PATH_FUSED;
   l->last_tb[0] = kFusedRowsPerGroup;

@@ -96,6 +96,7 @@ struct FusedArgs {
   int sb;               // bytes per ring stage
   WaitCfg wait;
   int inject_stall;
+  int prefetch_l2;      // every expert's prepacked weights fit the L2: prefetch them during routing
 };
 
 // Shared-memory plan of one CTA (the front of dynamic shared memory).
@@ -492,6 +493,13 @@ struct FusedRanges {
   int stage_bytes[2];     // g * scb of each phase
 };
 
+// Element p (0 or 1) of a two-entry array without a runtime-indexed access
+// (which would move the array, or the kernel parameters, to local memory).
+template <typename X>
+__device__ __forceinline__ X sel2(const X (&v)[2], int p) {
+  return p == 0 ? v[0] : v[1];
+}
+
 // Super-chunk range [kc0, kc0 + len) of K-slice ksl of ks = 2^ksl2.
 __device__ __forceinline__ void fused_kslice(int nkc, int ksl, int ksl2, int* kc0, int* len) {
   *kc0 = (ksl * nkc) >> ksl2;
@@ -500,36 +508,40 @@ __device__ __forceinline__ void fused_kslice(int nkc, int ksl, int ksl2, int* kc
 
 // Move to the first unit at or after the cursor that exists; sets src / left.
 __device__ __forceinline__ void fused_cursor_settle(FusedCursor& q, const FusedRanges& rg, const FusedArgs& a,
-                                                 int warp, int warps, const int* rgb_s, const int* act_s,
-                                                 int nact) {
+                                                    int warp, int warps, const int* rgb_s, const int* act_s,
+                                                    int nact) {
   for (;;) {
     if (q.p >= 2) return;
     if (q.u >= q.u_end) {
       ++q.p;
       if (q.p < 2) {
-        q.u = rg.u0[q.p];
-        q.u_end = rg.u1[q.p];
+        q.u = rg.u0[1];
+        q.u_end = rg.u1[1];
         q.v = warp;
       }
       continue;
     }
-    const int nt = rg.ntiles[q.p];
+    const int nt = sel2(rg.ntiles, q.p), nkc = sel2(rg.nkc, q.p);
     const int seg = q.u / nt, t0 = q.u - seg * nt;
     q.n = min(q.u_end - q.u, nt - t0);
-    const int ks = fused_ks(q.n, rg.nkc[q.p], warps);
+    const int ks = fused_ks(q.n, nkc, warps);
     q.ksl2 = __ffs(ks) - 1;
     if (q.v >= q.n * ks) {
       q.u += q.n;
       q.v = warp;
       continue;
     }
-    const FusedProj& P = a.p[q.p];
     const int e = act_s[fused_seg_expert(seg, rgb_s, nact)];
     int kc0, len;
-    fused_kslice(rg.nkc[q.p], q.v & (ks - 1), q.ksl2, &kc0, &len);
+    fused_kslice(nkc, q.v & (ks - 1), q.ksl2, &kc0, &len);
     const int tile = t0 + (q.v >> q.ksl2);
-    q.src = P.wpk + (size_t)e * P.L.expert_bytes + (size_t)tile * P.L.tile_bytes + (size_t)kc0 * P.L.scb;
-    q.left = len * P.L.scb;
+    const bool f1 = q.p == 0;
+    const uint8_t* wpk = f1 ? a.p[0].wpk : a.p[1].wpk;
+    const size_t eb = f1 ? a.p[0].L.expert_bytes : a.p[1].L.expert_bytes;
+    const size_t tb = f1 ? a.p[0].L.tile_bytes : a.p[1].L.tile_bytes;
+    const int scb = f1 ? a.p[0].L.scb : a.p[1].L.scb;
+    q.src = wpk + (size_t)e * eb + (size_t)tile * tb + (size_t)kc0 * scb;
+    q.left = len * scb;
     return;
   }
 }
@@ -540,7 +552,7 @@ __device__ __forceinline__ void fused_issue(FusedCursor& q, const FusedRanges& r
                                             int lane, int warp, int warps, const int* rgb_s, const int* act_s,
                                             int nact) {
   if (q.p < 2) {
-    const int bytes = min(rg.stage_bytes[q.p], q.left);
+    const int bytes = min(sel2(rg.stage_bytes, q.p), q.left);
     for (int off = lane * 16; off < bytes; off += 512) cp_async16(slot + off, q.src + off);
     q.src += bytes;
     q.left -= bytes;
@@ -588,6 +600,22 @@ __global__ void __launch_bounds__(kFusedMaxWarps * 32, 1) fused_decode_kernel(co
   }
   for (int i = tid; i < E; i += NT) cnt_s[i] = 0;
   __syncthreads();
+  // ---- a layer whose weights fit the L2 many times over (small decode
+  //      layers) has them pulled into the L2 while the CTAs route (issued
+  //      once the logits are in, so it does not delay them): each CTA
+  //      prefetches its equal slice of every expert's prepacked bytes ----
+  if (a.prefetch_l2 && tid == NT - 32) {   // the last warp: warp 0 groups, the first T warps route
+    for (int p = 0; p < 2; ++p) {
+      const size_t total = (size_t)E * a.p[p].L.expert_bytes;
+      const size_t per = ((total + gridDim.x - 1) / gridDim.x + 15) & ~(size_t)15;
+      const size_t b0 = per * blockIdx.x;
+      if (b0 < total) {
+        const uint32_t bytes = (uint32_t)(total - b0 < per ? total - b0 : per);
+        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(a.p[p].wpk + b0), "r"(bytes) : "memory");
+      }
+    }
+  }
+
   if (E <= 32) fused_route_all<1>(lg_s, T, E, k, a.normalize, ids_s, w_s, warp, W);
   else if (E <= 64) fused_route_all<2>(lg_s, T, E, k, a.normalize, ids_s, w_s, warp, W);
   else if (E <= 128) fused_route_all<4>(lg_s, T, E, k, a.normalize, ids_s, w_s, warp, W);
@@ -651,7 +679,8 @@ __global__ void __launch_bounds__(kFusedMaxWarps * 32, 1) fused_decode_kernel(co
     rg.ntiles[p] = a.p[p].ntiles;
     rg.nkc[p] = a.p[p].L.nkc;
     rg.stage_bytes[p] = a.p[p].g * a.p[p].L.scb;
-    const long long N = (long long)NRG * rg.ntiles[p];
+    // N <= (E + R / 16 + 1) * 512 and gridDim.x <= 152 * 2: the products fit 32 bits
+    const unsigned N = (unsigned)NRG * (unsigned)rg.ntiles[p];
     rg.u0[p] = (int)(N * blockIdx.x / gridDim.x);
     rg.u1[p] = (int)(N * (blockIdx.x + 1) / gridDim.x);
   }
@@ -708,6 +737,7 @@ __global__ void __launch_bounds__(kFusedMaxWarps * 32, 1) fused_decode_kernel(co
   const bool uint8_zp = a.zp_mode == QMOE_ZP_UINT8;
   int staged = -1;   // (phase, segment) whose rows are in bop
 
+#pragma unroll   // compile-time phase: the projection's parameters stay in the constant bank
   for (int ph = 0; ph < 2; ++ph) {
     const FusedProj& P = a.p[ph];
     const int nt = P.ntiles, nkc = P.L.nkc, K = P.K, Kp = nkc * SC;
