@@ -59,6 +59,9 @@ def parse():
                          "launch wherever it applies, or the separate kernels")
     ap.add_argument("--deterministic", action="store_true",
                     help="slot-ordered combine on the tensor-core path (qmoe_set_deterministic)")
+    ap.add_argument("--l2", default="rotate", choices=["rotate", "flush"],
+                    help="keep the timed steps' inputs out of the L2 by rotating over copies of the layer "
+                         "larger than the L2 together (default), or by flushing it before each step")
     ap.add_argument("--only-headline", action="store_true",
                     help="time only --workload (no `workloads` block)")
     return ap.parse_args()
@@ -288,67 +291,114 @@ def launches_per_step(cfg, path, min_rows):
     return (1 if cfg.T <= 64 else 2) + (3 if gemm_on else 0) + (2 if decode_on else 0) + 1
 
 
+def replicas_for(cfg, args):
+    """Copies of the layer (weights, x, logits) the timed steps rotate over so
+    that between two uses of one copy the other copies stream at least twice
+    the L2's size: every step then reads inputs the L2 does not hold."""
+    if args.l2 != "rotate":
+        return 1
+    from qmoe_inputs import expert_fc_bytes
+    per = cfg.E * (expert_fc_bytes(cfg, 1) + expert_fc_bytes(cfg, 2))
+    return 1 + -(-2 * L2_BYTES // per)
+
+
 def measure(q, cfg, args, dev, stream, flush, steps, warmup, fused=1, min_rows=0):
-    """Time one workload: graph-replayed (or eager) forwards with the L2
-    flushed before each, CUDA events on the launching stream around each
-    step; a separate traced pass for the per-stage times of the separate
-    kernels; the host-buffer entry point end to end."""
+    """Time one workload: graph-replayed (or eager) forwards, CUDA events on
+    the launching stream around each step.  The primary figure rotates over
+    enough copies of the layer that no step finds its inputs in the L2; a
+    second figure runs one copy with the L2 flushed (a 258 MB write) before
+    every step, which also evicts the kernels' code.  Then a traced pass for
+    the per-stage times of the separate kernels, and the host-buffer entry
+    point end to end."""
     import torch
     from qmoe_inputs import DTYPES, make_inputs
     inp = make_inputs(cfg)
-    layer = q.QMoELayer.from_config(cfg)
-    layer.set_fused_decode(fused)
-    layer.set_gemm_min_rows(min_rows)
-    layer.set_deterministic(1 if args.deterministic else 0)
-    layer.reserve(cfg.T)
-    x, logits = q.load_inputs(layer, inp, device=dev)
-    out = torch.empty_like(x)
+    nrep = replicas_for(cfg, args)
+    reps = []
+    for _ in range(nrep):
+        layer = q.QMoELayer.from_config(cfg)
+        layer.set_fused_decode(fused)
+        layer.set_gemm_min_rows(min_rows)
+        layer.set_deterministic(1 if args.deterministic else 0)
+        layer.reserve(cfg.T)
+        x, logits = q.load_inputs(layer, inp, device=dev)
+        reps.append((layer, x, logits, torch.empty_like(x)))
+    layer, x, logits, out = reps[0]
 
-    def make_step(traced):
+    def make_step(traced, rep):
+        lay, xx, lg, oo = rep
         ev = [torch.cuda.Event(enable_timing=True) for _ in range(q.QMOE_TRACE_NUM_EVENTS)]
-        layer.set_trace_events(ev if traced else None)
+        lay.set_trace_events(ev if traced else None)
         with torch.cuda.stream(stream):
-            layer.forward(x, logits, out, stream=stream)
+            lay.forward(xx, lg, oo, stream=stream)
         torch.cuda.synchronize()
         graph = None
         if args.mode == "graph":
             graph = torch.cuda.CUDAGraph()
             with torch.cuda.graph(graph, stream=stream):
-                layer.forward(x, logits, out, stream=stream)
+                lay.forward(xx, lg, oo, stream=stream)
             torch.cuda.synchronize()
 
         def step():
             if graph is not None:
                 graph.replay()
             else:
-                layer.forward(x, logits, out, stream=stream)
+                lay.forward(xx, lg, oo, stream=stream)
         return step, ev
+
+    def timed(step_fns, n, flush_each):
+        """Per-step device times of n steps.  Flushed: each step after its
+        own flush, one step per host round trip (the flush keeps the device
+        busy while the host enqueues the step).  Rotating: the steps are
+        enqueued back to back with an event between each two, after warm-up
+        steps in the same queue, so the device never waits on the host."""
+        with torch.cuda.stream(stream):
+            for i in range(max(3, warmup)):
+                if flush_each:
+                    flush.zero_()
+                step_fns[i % len(step_fns)]()
+        torch.cuda.synchronize()
+        per = []
+        if flush_each:
+            t_beg = torch.cuda.Event(enable_timing=True)
+            t_end = torch.cuda.Event(enable_timing=True)
+            with torch.cuda.stream(stream):
+                for i in range(n):
+                    flush.zero_()              # L2 flush between timed iterations
+                    t_beg.record(stream)
+                    step_fns[i % len(step_fns)]()
+                    t_end.record(stream)
+                    stream.synchronize()
+                    per.append(t_beg.elapsed_time(t_end))
+        else:
+            ev = [torch.cuda.Event(enable_timing=True) for _ in range(n + 1)]
+            lead = max(3, warmup)
+            with torch.cuda.stream(stream):
+                for i in range(lead):          # keeps the queue ahead of the host
+                    step_fns[(i - lead) % len(step_fns)]()
+                for i in range(n):
+                    ev[i].record(stream)
+                    step_fns[i % len(step_fns)]()
+                ev[n].record(stream)
+            stream.synchronize()
+            per = [ev[i].elapsed_time(ev[i + 1]) for i in range(n)]
+        torch.cuda.synchronize()
+        return per
 
     # Timed steps: no events inside the forward (between the separate kernels
     # they would break the programmatic launch overlap).
-    step, _ = make_step(False)
+    steps_fns = [make_step(False, r)[0] for r in reps]
     path = layer.last_path()
-    with torch.cuda.stream(stream):
-        for _ in range(max(3, warmup)):
-            flush.zero_()
-            step()
-    torch.cuda.synchronize()
-    per_step = []
-    t_beg = torch.cuda.Event(enable_timing=True)
-    t_end = torch.cuda.Event(enable_timing=True)
-    with torch.cuda.stream(stream):
-        for _ in range(steps):
-            flush.zero_()                      # L2 flush between timed iterations
-            t_beg.record(stream)
-            step()
-            t_end.record(stream)
-            stream.synchronize()
-            per_step.append(t_beg.elapsed_time(t_end))
-    torch.cuda.synchronize()
+    if nrep > 1:
+        per_step = timed(steps_fns, steps, False)      # copy i % nrep at step i
+        per_flushed = timed(steps_fns[:1], steps, True)
+    else:
+        per_step = timed(steps_fns, steps, True)
+        per_flushed = per_step
 
     stages = None
     if path == 1:
-        tstep, ev = make_step(True)
+        tstep, ev = make_step(True, reps[0])
         stage_ms = [[] for _ in range(q.QMOE_TRACE_NUM_EVENTS - 1)]
         with torch.cuda.stream(stream):
             for i in range(3 + max(5, steps // 2)):
@@ -361,35 +411,51 @@ def measure(q, cfg, args, dev, stream, flush, steps, warmup, fused=1, min_rows=0
         torch.cuda.synchronize()
         stages = {n: statistics.mean(v) * 1e3 for n, v in
                   zip(["route_group", "fc1", "fc2", "combine"], stage_ms)}
-    layer.set_trace_events(None)
-    status = layer.poll()
-    if status != 0:
-        print(json.dumps({"error": f"{cfg.name}: device status {status} after the timed steps"}), file=sys.stderr)
-        sys.exit(1)
+        layer.set_trace_events(None)
+    for lay, _, _, _ in reps:
+        status = lay.poll()
+        if status != 0:
+            print(json.dumps({"error": f"{cfg.name}: device status {status} after the timed steps"}), file=sys.stderr)
+            sys.exit(1)
 
     _, _, _, offs = layer.routing(cfg.T, stream=None)
     torch.cuda.synchronize()
     o = offs.cpu().tolist()
     counts = [o[i + 1] - o[i] for i in range(cfg.E)]
 
-    # end to end through the host-buffer entry point (pinned memory)
+    # end to end through the host-buffer entry point (pinned memory), rotating
+    # over the same copies
     ds = torch.tensor([], dtype=DTYPES[cfg.dtype]).element_size()
     xh = inp["x"].pin_memory()
     lh = inp["logits"].pin_memory()
     oh = torch.empty_like(xh).pin_memory()
-    for _ in range(3):
-        layer.forward_host(xh, lh, oh, stream=stream)
+    for lay, _, _, _ in reps:
+        lay.forward_host(xh, lh, oh, stream=stream)
     e2e_ms = []
-    for _ in range(steps):
-        flush.zero_()
+    for i in range(steps):
+        lay = reps[i % nrep][0]
+        if nrep == 1:
+            flush.zero_()
         torch.cuda.synchronize()
         t0 = time.perf_counter()
-        layer.forward_host(xh, lh, oh, stream=stream)
+        lay.forward_host(xh, lh, oh, stream=stream)
         e2e_ms.append((time.perf_counter() - t0) * 1e3)
-    layer.close()
+    for lay, _, _, _ in reps:
+        lay.close()
+    reps.clear()
     return {"ms": statistics.mean(per_step), "ms_median": statistics.median(per_step), "path": path,
+            "ms_l2_flushed": statistics.mean(per_flushed), "replicas": nrep,
             "stages_us": stages, "counts": counts, "e2e_ms": statistics.mean(e2e_ms),
             "h2d": cfg.T * cfg.H * ds + cfg.T * cfg.E * 4, "d2h": cfg.T * cfg.H * ds}
+
+
+def l2_note(cfg, m):
+    from qmoe_inputs import expert_fc_bytes
+    if m["replicas"] == 1:
+        return "flushed between timed steps (258 MB write)"
+    per = cfg.E * (expert_fc_bytes(cfg, 1) + expert_fc_bytes(cfg, 2))
+    return (f"inputs larger than L2: {m['replicas']} copies of the layer (weights, x, logits; "
+            f"{per * m['replicas'] / 2**20:.0f} MB of weights) rotated step by step")
 
 
 def roofline_of(cfg, m, hbm_peak, bf16_peak, peak_kind):
@@ -425,6 +491,7 @@ def roofline_of(cfg, m, hbm_peak, bf16_peak, peak_kind):
 def workload_summary(cfg, m, hbm_peak, bf16_peak, peak_kind, world):
     roof, by, fl = roofline_of(cfg, m, hbm_peak, bf16_peak, peak_kind)
     d = {"us_per_layer": m["ms"] * 1e3, "tokens_per_s": job_throughput(cfg.T, world, m["ms"]),
+         "l2": l2_note(cfg, m), "us_per_layer_l2_flushed": m["ms_l2_flushed"] * 1e3,
          "path": PATH_NAMES.get(m["path"], "?"), "active_experts": by["active"],
          "layer_bytes": by["layer"], "layer_flops": fl["layer"],
          "layer_hbm_frac": by["layer"] / (m["ms"] * 1e-3) / 1e9 / hbm_peak,
@@ -494,7 +561,8 @@ def run_ours(args):
         "config": {"workload": cfg.name, "tokens": cfg.T, "hidden": cfg.H, "inter": cfg.I,
                    "experts": cfg.E, "top_k": cfg.k, "bits": [cfg.bits1, cfg.bits2],
                    "block_size": cfg.B, "zp": cfg.zp_mode, "act": cfg.act,
-                   "mode": args.mode, "l2": "flushed between timed steps (258 MB write)",
+                   "mode": args.mode, "l2": l2_note(cfg, head),
+                   "us_per_layer_l2_flushed": head["ms_l2_flushed"] * 1e3,
                    "path": PATH_NAMES.get(head["path"], "?"),
                    "us_per_layer": ms * 1e3, "active_experts": by["active"],
                    "layer_bytes": by["layer"],

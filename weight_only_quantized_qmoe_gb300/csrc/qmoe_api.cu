@@ -348,8 +348,8 @@ bool fused_applies(const qmoe_layer* l, int64_t T, FusedShape* fs) {
     if (warps == 8 && fs->sb < kFusedMinStageTwoPerSm) continue;
     fs->smem = fused_plan(R, l->E, nkc * sc, fs->ng_max, fs->sb, warps).total;
     if (fs->smem > budget) continue;
-    // the logits are staged in the ring area before the rings start
-    if ((int64_t)T * l->E * 4 > (int64_t)warps * kFusedStages * fs->sb) continue;
+    // the routing and grouping scratch sits in the ring area before the rings start
+    if (R > 32 * warps || fused_prologue((int)T, l->E, R).total > warps * kFusedStages * fs->sb) continue;
     fs->warps = warps;
     fs->ctas_per_sm = warps == 8 ? 2 : 1;
     return true;

@@ -20,22 +20,24 @@
 // GB300 design (ours):
 //   * one CTA of 16 warps per SM, launched cooperatively (all CTAs resident:
 //     fc2 waits on other CTAs' fc1 results);
-//   * every CTA routes all tokens itself (a warp per token, warp-wide
-//     redux.sync arg-max per slot) and builds the grouping in shared memory,
-//     so no CTA waits on another before it streams weights;
+//   * every CTA routes all tokens itself (qmoe_topk.cuh: a warp per two
+//     tokens, per-lane sorted logits, redux.sync per rank) and builds the
+//     grouping in shared memory with every warp at once, so no CTA waits on
+//     another before it streams weights;
 //   * the work is a list of 16-row weight tiles per phase (fc1 tiles of every
 //     (expert, group of <= 16 routed rows) segment, then the fc2 tiles);
 //     each CTA takes a contiguous, equal share of each phase, cut at segment
-//     boundaries into blocks; the 16 warps split a block's tiles (and K, when
-//     a block has fewer tiles than warps);
+//     boundaries into blocks; a block's tiles, laid end to end with K inside,
+//     are cut into equal runs of super-chunks, one per warp;
 //   * each warp streams its tiles through a private shared-memory ring of
 //     cp.async stages that runs ahead across blocks and phases (weights never
 //     wait on anything), dequantises in registers and feeds mma.m16n8k16 with
 //     fp32 accumulation; the routed rows of the block's segment are staged
 //     once per block in B-fragment order;
-//   * a block ends with one CTA barrier: split-K partials are added in a fixed
-//     order, fc1 publishes h and bumps the segment's counter (release), fc2
-//     writes y;
+//   * a warp finishes the tiles it holds whole; a tile cut between warps is
+//     finished, after one CTA barrier, by the warp that holds its first
+//     super-chunk, adding the later warps' parked pieces in warp order; then
+//     fc1 publishes h and bumps the segment's counter (release), fc2 writes y;
 //   * once every CTA is done with fc2 (a grid-wide arrival counter), each CTA
 //     adds the k slots in order for an equal share of the outputs and rounds
 //     into D;
@@ -45,6 +47,7 @@
 
 #include "qmoe_internal.cuh"
 #include "qmoe_decode_kernel.cuh"
+#include "qmoe_topk.cuh"
 
 namespace qmoe {
 
@@ -101,20 +104,21 @@ struct FusedArgs {
 
 // Shared-memory plan of one CTA (the front of dynamic shared memory).
 struct FusedPlan {
-  int ids_off, w_off, perm_off, cnt_off, off_off, cur_off, act_off, rgb_off, bop_off, ring_off, total;
+  int ids_off, w_off, perm_off, cnt_off, off_off, act_off, rgb_off, bop_off, slot_off, ring_off, total;
 };
 
 __host__ __device__ inline int fused_align16(int v) { return (v + 15) & ~15; }
 
-// Bytes of the B-operand staging (>= the split-K reduction it is reused for).
-__host__ __device__ inline int fused_bop_bytes(int Kp_max, int ng_max, int warps) {
-  const int bop = Kp_max / 16 * ng_max * 32 * 8;   // k-tiles x token groups x 32 lanes x 8 B
-  const int red = warps * 32 * (2 * 2 * 4) * 4;   // warps x 32 lanes x acc[2][2][4] floats
-  return bop > red ? bop : red;
-}
+// Bytes of the B-operand staging: k-tiles x token groups x 32 lanes x 8 B.
+__host__ __device__ inline int fused_bop_bytes(int Kp_max, int ng_max) { return Kp_max / 16 * ng_max * 32 * 8; }
 
-// Shared memory: broadcast ints, routing and grouping, the B staging, then
-// one ring of kFusedStages stages of sb bytes per warp.
+// fp32 partial sums one warp parks for another (a tile piece that does not
+// start the tile): per lane acc[sub][group][4] for 2 sub-tiles x ng_max groups.
+__host__ __device__ inline int fused_slot_floats(int ng_max) { return 2 * ng_max * 4; }
+
+// Shared memory: broadcast ints, routing and grouping, the B staging, the
+// warps' partial-sum slots, then one ring of kFusedStages stages of sb bytes
+// per warp.
 __host__ __device__ inline FusedPlan fused_plan(int R, int E, int Kp_max, int ng_max, int sb, int warps) {
   FusedPlan p;
   int o = 64;
@@ -123,94 +127,40 @@ __host__ __device__ inline FusedPlan fused_plan(int R, int E, int Kp_max, int ng
   p.perm_off = o; o = fused_align16(o + 4 * R);
   p.cnt_off = o;  o = fused_align16(o + 4 * E);
   p.off_off = o;  o = fused_align16(o + 4 * (E + 1));
-  p.cur_off = o;  o = fused_align16(o + 4 * E);
   p.act_off = o;  o = fused_align16(o + 4 * E);
   p.rgb_off = o;  o = fused_align16(o + 4 * (E + 1));
   o = (o + 127) & ~127;
   p.bop_off = o;
-  o += fused_bop_bytes(Kp_max, ng_max, warps);
+  o += fused_bop_bytes(Kp_max, ng_max);
+  p.slot_off = o;
+  o += warps * 32 * fused_slot_floats(ng_max) * 4;
   o = (o + 127) & ~127;
   p.ring_off = o;
   p.total = o + warps * kFusedStages * sb;
   return p;
 }
 
-__device__ __forceinline__ int redux_max_s32(int v) {
-  int r;
-  asm volatile("redux.sync.max.s32 %0, %1, 0xffffffff;" : "=r"(r) : "r"(v));
-  return r;
-}
-__device__ __forceinline__ int redux_min_s32(int v) {
-  int r;
-  asm volatile("redux.sync.min.s32 %0, %1, 0xffffffff;" : "=r"(r) : "r"(v));
-  return r;
-}
-
-__device__ __forceinline__ int fused_order_key(float v) {
-  const int b = __float_as_int(v);
-  return b ^ ((b >> 31) & 0x7fffffff);
-}
-
-// One warp ranks the E <= 32 * NPL logits of one token (in shared memory):
-// ids[0..k) in rank order and their weights.
-template <int NPL>
-__device__ __forceinline__ void fused_route_token(const float* lg, int E, int k, int normalize, int* ids, float* w) {
-  const int lane = threadIdx.x & 31;
-  int key[NPL];
-  uint32_t taken = 0;
-  float mx = -INFINITY;
-#pragma unroll
-  for (int i = 0; i < NPL; ++i) {
-    const int e = lane + 32 * i;
-    key[i] = INT_MIN;
-    if (e < E) {
-      const float v = lg[e];
-      key[i] = fused_order_key(v);
-      mx = fmaxf(mx, v);
-    } else {
-      taken |= 1u << i;
-    }
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-  float sum_all = 0.f;
-#pragma unroll
-  for (int i = 0; i < NPL; ++i) {
-    const int e = lane + 32 * i;
-    if (e < E) sum_all += expf(lg[e] - mx);
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) sum_all += __shfl_xor_sync(0xffffffffu, sum_all, o);
-
-  for (int slot = 0; slot < k; ++slot) {
-    int bk = INT_MIN, bi = INT_MAX;
-#pragma unroll
-    for (int i = 0; i < NPL; ++i) {
-      const int e = lane + 32 * i;
-      if (!((taken >> i) & 1u) && (key[i] > bk || (key[i] == bk && e < bi))) {
-        bk = key[i];
-        bi = e;
-      }
-    }
-    const int m = redux_max_s32(bk);
-    const int sel = redux_min_s32(bk == m ? bi : INT_MAX);
-    if ((sel & 31) == lane) taken |= 1u << (sel >> 5);
-    if (lane == 0) ids[slot] = sel;
-  }
-  __syncwarp();
-  const float p = lane < k ? expf(lg[ids[lane]] - mx) : 0.f;
-  float sum_sel = p;
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) sum_sel += __shfl_xor_sync(0xffffffffu, sum_sel, o);
-  if (lane < k) w[lane] = p / (normalize ? sum_sel : sum_all);
+// Scratch of the routing and grouping, in the ring area before the rings
+// start: the logits [T, E], the per-chunk expert counts [ceil(R / 32), E]
+// (a chunk = 32 consecutive routes), the per-warp totals of the offset scan
+// (3 x 8 ints).
+struct FusedPrologue {
+  int cntw_off, tot_off, total;
+};
+__host__ __device__ inline FusedPrologue fused_prologue(int T, int E, int R) {
+  FusedPrologue q;
+  q.cntw_off = fused_align16(T * E * 4);
+  q.tot_off = fused_align16(q.cntw_off + (R + 31) / 32 * E * 4);
+  q.total = q.tot_off + 3 * 8 * 4;
+  return q;
 }
 
-// Every token of the forward, a warp each, with the key count per lane
-// fixed at compile time for E's size class.
+// Every token of the forward, two per warp pass, with the key count per
+// lane fixed at compile time for E's size class.
 template <int NPL>
 __device__ __noinline__ void fused_route_all(const float* lg_s, int T, int E, int k, int normalize, int* ids_s,
                                              float* w_s, int warp, int W) {
-  for (int t = warp; t < T; t += W) fused_route_token<NPL>(lg_s + t * E, E, k, normalize, ids_s + t * k, w_s + t * k);
+  for (int t = 2 * warp; t < T; t += 2 * W) topk_route_tokens<NPL, 2>(lg_s, t, T, E, k, normalize, ids_s, w_s);
 }
 
 // ----------------------------------------------------------------------------
@@ -454,13 +404,9 @@ __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commi
 template <int N>
 __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 
-// K-splits of a block of n tiles (a power of two): as many as keep every warp
-// busy with at most one unit and every unit at least two super-chunks long.
-__host__ __device__ inline int fused_ks(int n, int nkc, int warps) {
-  int ks = 1;
-  while (ks < warps && n * ks * 2 <= warps && nkc >= ks * 4) ks *= 2;
-  return ks;
-}
+// Super-chunk range of warp w in a block of `total` super-chunks: the block's
+// tiles laid end to end (tile-major, K inside) and cut into equal runs.
+__device__ __forceinline__ int fused_warp_begin(int w, int total, int warps) { return w * total / warps; }
 
 // Active expert of segment `seg` (binary search over the row-group prefix).
 __device__ __forceinline__ int fused_seg_expert(int seg, const int* rgb_s, int nact) {
@@ -473,18 +419,17 @@ __device__ __forceinline__ int fused_seg_expert(int seg, const int* rgb_s, int n
 }
 
 // The ring stages one warp consumes, in order: for phase fc1 then fc2, for
-// each block of this CTA's range (a block = tiles of one segment), for each
-// of this warp's units (tile, K-slice) of the block, its super-chunks g at a
-// time.  The producer runs the same walk kFusedStages - 1 stages ahead; a
-// unit is one contiguous byte run of the prepacked tile, so a stage is a
-// pointer bump.
+// each block of this CTA's range (a block = tiles of one segment), the
+// warp's equal run of the block's super-chunks, cut at tile boundaries into
+// pieces, each piece g super-chunks at a time.  The producer runs the same
+// walk kFusedStages - 1 stages ahead; the tiles of an expert are contiguous
+// in the prepacked layout, so a stage is a pointer bump.
 struct FusedCursor {
   int p;                  // phase; 2 = exhausted
   int u, u_end;           // block start (tile index within the phase) and range end
-  int n, ksl2;            // tiles of the block, log2 of its K-splits
-  int v;                  // unit within the block (warp, warp + warps, ...)
-  const uint8_t* src;     // next byte of the current unit
-  int left;               // bytes of the unit not yet issued
+  int c, c_end;           // next super-chunk of the warp's run in the block, run end; c = -1: block not entered
+  const uint8_t* src;     // next byte of the current piece
+  int left;               // bytes of the piece not yet issued
 };
 
 struct FusedRanges {
@@ -500,13 +445,7 @@ __device__ __forceinline__ X sel2(const X (&v)[2], int p) {
   return p == 0 ? v[0] : v[1];
 }
 
-// Super-chunk range [kc0, kc0 + len) of K-slice ksl of ks = 2^ksl2.
-__device__ __forceinline__ void fused_kslice(int nkc, int ksl, int ksl2, int* kc0, int* len) {
-  *kc0 = (ksl * nkc) >> ksl2;
-  *len = (((ksl + 1) * nkc) >> ksl2) - *kc0;
-}
-
-// Move to the first unit at or after the cursor that exists; sets src / left.
+// Move to the next piece at or after the cursor that exists; sets src / left.
 __device__ __forceinline__ void fused_cursor_settle(FusedCursor& q, const FusedRanges& rg, const FusedArgs& a,
                                                     int warp, int warps, const int* rgb_s, const int* act_s,
                                                     int nact) {
@@ -517,31 +456,33 @@ __device__ __forceinline__ void fused_cursor_settle(FusedCursor& q, const FusedR
       if (q.p < 2) {
         q.u = rg.u0[1];
         q.u_end = rg.u1[1];
-        q.v = warp;
+        q.c = -1;
       }
       continue;
     }
     const int nt = sel2(rg.ntiles, q.p), nkc = sel2(rg.nkc, q.p);
     const int seg = q.u / nt, t0 = q.u - seg * nt;
-    q.n = min(q.u_end - q.u, nt - t0);
-    const int ks = fused_ks(q.n, nkc, warps);
-    q.ksl2 = __ffs(ks) - 1;
-    if (q.v >= q.n * ks) {
-      q.u += q.n;
-      q.v = warp;
+    const int n = min(q.u_end - q.u, nt - t0);
+    if (q.c < 0) {
+      q.c = fused_warp_begin(warp, n * nkc, warps);
+      q.c_end = fused_warp_begin(warp + 1, n * nkc, warps);
+    }
+    if (q.c >= q.c_end) {
+      q.u += n;
+      q.c = -1;
       continue;
     }
     const int e = act_s[fused_seg_expert(seg, rgb_s, nact)];
-    int kc0, len;
-    fused_kslice(nkc, q.v & (ks - 1), q.ksl2, &kc0, &len);
-    const int tile = t0 + (q.v >> q.ksl2);
+    const int tile = q.c / nkc;
+    const int pend = min(q.c_end, (tile + 1) * nkc);
     const bool f1 = q.p == 0;
     const uint8_t* wpk = f1 ? a.p[0].wpk : a.p[1].wpk;
     const size_t eb = f1 ? a.p[0].L.expert_bytes : a.p[1].L.expert_bytes;
     const size_t tb = f1 ? a.p[0].L.tile_bytes : a.p[1].L.tile_bytes;
     const int scb = f1 ? a.p[0].L.scb : a.p[1].L.scb;
-    q.src = wpk + (size_t)e * eb + (size_t)tile * tb + (size_t)kc0 * scb;
-    q.left = len * scb;
+    q.src = wpk + (size_t)e * eb + (size_t)(t0 + tile) * tb + (size_t)(q.c - tile * nkc) * scb;
+    q.left = (pend - q.c) * scb;
+    q.c = pend;
     return;
   }
 }
@@ -556,10 +497,7 @@ __device__ __forceinline__ void fused_issue(FusedCursor& q, const FusedRanges& r
     for (int off = lane * 16; off < bytes; off += 512) cp_async16(slot + off, q.src + off);
     q.src += bytes;
     q.left -= bytes;
-    if (q.left == 0) {
-      q.v += warps;
-      fused_cursor_settle(q, rg, a, warp, warps, rgb_s, act_s, nact);
-    }
+    if (q.left == 0) fused_cursor_settle(q, rg, a, warp, warps, rgb_s, act_s, nact);
   }
   cp_async_commit();
 }
@@ -582,29 +520,46 @@ __global__ void __launch_bounds__(kFusedMaxWarps * 32, 1) fused_decode_kernel(co
   int* perm_s = reinterpret_cast<int*>(smem + pl.perm_off);
   int* cnt_s = reinterpret_cast<int*>(smem + pl.cnt_off);
   int* off_s = reinterpret_cast<int*>(smem + pl.off_off);
-  int* cur_s = reinterpret_cast<int*>(smem + pl.cur_off);
   int* act_s = reinterpret_cast<int*>(smem + pl.act_off);      // active experts, ascending
   int* rgb_s = reinterpret_cast<int*>(smem + pl.rgb_off);      // row-group prefix over active experts
   uint32_t* bop = reinterpret_cast<uint32_t*>(smem + pl.bop_off);
-  float* red = reinterpret_cast<float*>(smem + pl.bop_off);
+  float* slot_s = reinterpret_cast<float*>(smem + pl.slot_off);
+  const int SLOTF = fused_slot_floats(a.ng_max);
   uint8_t* ring = smem + pl.ring_off + (size_t)warp * kFusedStages * a.sb;
   int* done1 = a.sync + kSyncHeader;
 
   // ---- routing (every CTA, all tokens): the logits first land in the
   //      (still empty) ring area with one coalesced pass ----
   float* lg_s = reinterpret_cast<float*>(smem + pl.ring_off);
+  // the token rows every CTA stages for fc1 come from the L2 by then: each
+  // CTA prefetches an equal 16-byte-aligned slice of x while it routes
+  if (tid == NT - 32 && (reinterpret_cast<uintptr_t>(a.x) & 15) == 0) {
+    const size_t total = (size_t)T * a.H * 2;   // 16-bit activations; H is a multiple of 32
+    const size_t per = ((total + gridDim.x - 1) / gridDim.x + 15) & ~(size_t)15;
+    const size_t b0 = per * blockIdx.x;
+    if (b0 < total) {
+      const uint32_t bytes = (uint32_t)(total - b0 < per ? total - b0 : per);
+      asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(static_cast<const uint8_t*>(a.x) + b0),
+                   "r"(bytes)
+                   : "memory");
+    }
+  }
   {
     const int n4 = T * E / 4;   // E is a multiple of 4 on this path
     const float4* src4 = reinterpret_cast<const float4*>(a.logits);
     for (int i = tid; i < n4; i += NT) reinterpret_cast<float4*>(lg_s)[i] = __ldg(src4 + i);
   }
-  for (int i = tid; i < E; i += NT) cnt_s[i] = 0;
+  const FusedPrologue pq = fused_prologue(T, E, R);
+  int* cntw_s = reinterpret_cast<int*>(smem + pl.ring_off + pq.cntw_off);
+  int* tot_s = reinterpret_cast<int*>(smem + pl.ring_off + pq.tot_off);
+  const int NCH = (R + 31) / 32;   // route chunks (<= warps: R <= 32 * warps)
+  for (int i = tid; i < NCH * E; i += NT) cntw_s[i] = 0;
   __syncthreads();
   // ---- a layer whose weights fit the L2 many times over (small decode
   //      layers) has them pulled into the L2 while the CTAs route (issued
   //      once the logits are in, so it does not delay them): each CTA
   //      prefetches its equal slice of every expert's prepacked bytes ----
-  if (a.prefetch_l2 && tid == NT - 32) {   // the last warp: warp 0 groups, the first T warps route
+  if (a.prefetch_l2 && tid == NT - 32) {   // one thread of the last warp (it routes last, if at all)
     for (int p = 0; p < 2; ++p) {
       const size_t total = (size_t)E * a.p[p].L.expert_bytes;
       const size_t per = ((total + gridDim.x - 1) / gridDim.x + 15) & ~(size_t)15;
@@ -621,55 +576,79 @@ __global__ void __launch_bounds__(kFusedMaxWarps * 32, 1) fused_decode_kernel(co
   else if (E <= 128) fused_route_all<4>(lg_s, T, E, k, a.normalize, ids_s, w_s, warp, W);
   else fused_route_all<8>(lg_s, T, E, k, a.normalize, ids_s, w_s, warp, W);
   __syncthreads();
-  for (int r = tid; r < R; r += NT) atomicAdd(&cnt_s[ids_s[r]], 1);
+  // ---- grouping, every warp at once ----
+  // (1) each route chunk's count per expert, and each route's rank among the
+  //     chunk's routes of its expert (ballot-built peer masks)
+  const unsigned lt = (1u << lane) - 1u;
+  const int nb = id_bits(E);
+  int my_e = -1, my_rank = 0;
+  if (warp < NCH) {
+    const int r = warp * 32 + lane;
+    my_e = r < R ? ids_s[r] : -1;
+    const unsigned peers = peers_of(my_e, nb);
+    my_rank = __popc(peers & lt);
+    if (my_e >= 0 && my_rank == 0) cntw_s[warp * E + my_e] = __popc(peers);
+  }
   __syncthreads();
-  // ---- grouping: offsets, active experts, row-group prefix (warp 0) ----
-  if (warp == 0) {
-    const unsigned lt = (1u << lane) - 1u;
-    int run = 0, nact = 0, nrg = 0;
-    for (int base = 0; base < E; base += 32) {
-      const int e = base + lane;
-      const int c = e < E ? cnt_s[e] : 0;
-      const int g = (c + kFusedRowsPerGroup - 1) / kFusedRowsPerGroup;
-      int ic = c, ig = g;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int nc = __shfl_up_sync(0xffffffffu, ic, o);
-        const int ng = __shfl_up_sync(0xffffffffu, ig, o);
-        if (lane >= o) { ic += nc; ig += ng; }
+  // (2) a lane per expert: counts = sum over chunks (chunk entries become
+  //     exclusive prefixes); per 32 experts, scans of rows and row groups
+  //     and the ballot of active experts
+  const int NEW = (E + 31) / 32;
+  int sc_c = 0, sc_g = 0, my_c = 0, my_g = 0;
+  unsigned act_mask = 0;
+  if (warp < NEW) {
+    const int e = warp * 32 + lane;
+    if (e < E) {
+      for (int ch = 0; ch < NCH; ++ch) {
+        const int v = cntw_s[ch * E + e];
+        cntw_s[ch * E + e] = my_c;
+        my_c += v;
       }
-      const unsigned act = __ballot_sync(0xffffffffu, c > 0);
-      if (e < E) {
-        off_s[e] = run + ic - c;
-        cur_s[e] = run + ic - c;
-      }
-      if (c > 0) {
-        const int ai = nact + __popc(act & lt);
-        act_s[ai] = e;
-        rgb_s[ai] = nrg + ig - g;
-      }
-      run += __shfl_sync(0xffffffffu, ic, 31);
-      nrg += __shfl_sync(0xffffffffu, ig, 31);
-      nact += __popc(act);
+      cnt_s[e] = my_c;
     }
-    if (lane == 0) {
-      off_s[E] = run;
+    my_g = (my_c + kFusedRowsPerGroup - 1) / kFusedRowsPerGroup;
+    sc_c = my_c;
+    sc_g = my_g;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int nc = __shfl_up_sync(0xffffffffu, sc_c, o);
+      const int ng = __shfl_up_sync(0xffffffffu, sc_g, o);
+      if (lane >= o) { sc_c += nc; sc_g += ng; }
+    }
+    act_mask = __ballot_sync(0xffffffffu, my_c > 0);
+    if (lane == 31) {
+      tot_s[warp] = sc_c;
+      tot_s[8 + warp] = sc_g;
+      tot_s[16 + warp] = __popc(act_mask);
+    }
+  }
+  __syncthreads();
+  // (3) offsets, the active-expert list and the row-group prefix
+  if (warp < NEW) {
+    int pc = 0, pg = 0, pa = 0;
+    for (int w2 = 0; w2 < warp; ++w2) {
+      pc += tot_s[w2];
+      pg += tot_s[8 + w2];
+      pa += tot_s[16 + w2];
+    }
+    const int e = warp * 32 + lane;
+    if (e < E) off_s[e] = pc + sc_c - my_c;
+    if (my_c > 0) {
+      const int ai = pa + __popc(act_mask & lt);
+      act_s[ai] = e;
+      rgb_s[ai] = pg + sc_g - my_g;
+    }
+    if (warp == NEW - 1 && lane == 31) {
+      const int nact = pa + __popc(act_mask), nrg = pg + sc_g;
+      off_s[E] = pc + sc_c;
       rgb_s[nact] = nrg;
       bc[0] = nact;
       bc[1] = nrg;
     }
-    __syncwarp();
-    // stable permutation: routes of an expert in ascending route order
-    for (int base = 0; base < R; base += 32) {
-      const int r = base + lane;
-      const int e = r < R ? ids_s[r] : -1;
-      const unsigned peers = peers_of(e, id_bits(E));
-      if (e >= 0) perm_s[cur_s[e] + __popc(peers & lt)] = r;
-      __syncwarp();
-      if (e >= 0 && lane == __ffs(peers) - 1) cur_s[e] += __popc(peers);
-      __syncwarp();
-    }
   }
+  __syncthreads();
+  // (4) the stable permutation: routes of an expert in ascending route order
+  if (my_e >= 0) perm_s[off_s[my_e] + cntw_s[warp * E + my_e] + my_rank] = warp * 32 + lane;
   __syncthreads();
   const int nact = bc[0], NRG = bc[1];
 
@@ -688,9 +667,8 @@ __global__ void __launch_bounds__(kFusedMaxWarps * 32, 1) fused_decode_kernel(co
   prod.p = 0;
   prod.u = rg.u0[0];
   prod.u_end = rg.u1[0];
-  prod.v = warp;
-  prod.n = 0;
-  prod.ksl2 = 0;
+  prod.c = -1;
+  prod.c_end = 0;
   prod.src = nullptr;
   prod.left = 0;
   fused_cursor_settle(prod, rg, a, warp, W, rgb_s, act_s, nact);
@@ -746,8 +724,6 @@ __global__ void __launch_bounds__(kFusedMaxWarps * 32, 1) fused_decode_kernel(co
       // ---- one block: tiles [t0, t0 + n) of segment seg ----
       const int seg = u / nt, t0 = u % nt;
       const int n = min(rg.u1[ph] - u, nt - t0);
-      const int ks = fused_ks(n, nkc, W);
-      const int ksl2 = __ffs(ks) - 1;
       const int ai = fused_seg_expert(seg, rgb_s, nact);
       const int e = act_s[ai], c = cnt_s[e];
       const int j0 = (seg - rgb_s[ai]) * kFusedRowsPerGroup;
@@ -795,7 +771,6 @@ __global__ void __launch_bounds__(kFusedMaxWarps * 32, 1) fused_decode_kernel(co
       const bool gated1 = ph == 0 && a.gated;
       const uint32_t zo = ((ph == 0 ? B1 : B2) == 8 && BF16) ? zoff_int : zoff_half;
       float acc[2][2][4];
-      int my_tile = -1, my_ksl = 0;
       auto epilogue = [&](int tile) {
         const int g = lane >> 2, t4 = lane & 3;
 #pragma unroll
@@ -832,10 +807,13 @@ __global__ void __launch_bounds__(kFusedMaxWarps * 32, 1) fused_decode_kernel(co
         }
       };
 
-      for (int v = warp; v < n * ks; v += W) {
-        const int tile = t0 + (v >> ksl2), ksl = v & (ks - 1);
-        int kc0, len;
-        fused_kslice(nkc, ksl, ksl2, &kc0, &len);
+      // ---- this warp's run of the block's super-chunks, piece by piece ----
+      const int total = n * nkc;
+      const int cb1 = fused_warp_begin(warp + 1, total, W);
+      int own_tile = -1;   // a tile this warp started but did not finish
+      for (int ci = fused_warp_begin(warp, total, W); ci < cb1;) {
+        const int tile = ci / nkc, kc0 = ci - tile * nkc;
+        const int pend = min(cb1, (tile + 1) * nkc), len = pend - ci;
 #pragma unroll
         for (int s = 0; s < 2; ++s)
 #pragma unroll
@@ -844,14 +822,14 @@ __global__ void __launch_bounds__(kFusedMaxWarps * 32, 1) fused_decode_kernel(co
             for (int q = 0; q < 4; ++q) acc[s][nn][q] = 0.f;
         for (int cc = 0; cc < len;) {
           const int nck = min(P.g, len - cc);
-          // stage `stage` of the ring holds super-chunks [kc0 + cc, kc0 + cc + nck)
+          // stage `stage` of the ring holds super-chunks [kc0 + cc, kc0 + cc + nck) of the tile
           // stages 0..stage have landed (the kFusedStages - 2 newer ones may not)
           cp_async_wait<kFusedStages - 2>();
           __syncwarp();
           const uint8_t* slot = ring + (stage % kFusedStages) * a.sb;
           // refill the stage consumed last (the slot before this one)
-          fused_issue(prod, rg, a, ring + ((stage + kFusedStages - 1) % kFusedStages) * a.sb, lane, warp, W, rgb_s, act_s,
-                      nact);
+          fused_issue(prod, rg, a, ring + ((stage + kFusedStages - 1) % kFusedStages) * a.sb, lane, warp, W, rgb_s,
+                      act_s, nact);
           for (int x = 0; x < nck; ++x) {
             const uint8_t* ch = slot + x * gm.scb;
             const uint32_t* bl = bop + (size_t)(kc0 + cc + x) * KT * NG * 64 + lane * 2;
@@ -878,41 +856,46 @@ __global__ void __launch_bounds__(kFusedMaxWarps * 32, 1) fused_decode_kernel(co
           ++stage;
           cc += nck;
         }
-        if (ks == 1) epilogue(tile);
-        else {
-          my_tile = tile;
-          my_ksl = ksl;
-        }
-      }
-      __syncthreads();   // every warp is done with bop
-
-      // ---- split-K partials, added in a fixed order ----
-      if (ks > 1) {
-        if (my_tile >= 0 && my_ksl != 0) {
-          float* dst = red + (warp * 32 + lane) * 16;
+        if (len == nkc) {
+          epilogue(t0 + tile);                 // the whole tile
+        } else if (kc0 > 0) {
+          // the tail of a tile an earlier warp started (only a run's first
+          // piece can be one): park it for that warp
+          float* dst = slot_s + (warp * 32 + lane) * SLOTF;
 #pragma unroll
-          for (int s = 0; s < 2; ++s)
+          for (int s2 = 0; s2 < 2; ++s2)
 #pragma unroll
             for (int nn = 0; nn < 2; ++nn)
+              if (nn < NG)
 #pragma unroll
-              for (int q = 0; q < 4; ++q) dst[(s * 2 + nn) * 4 + q] = acc[s][nn][q];
+                for (int q = 0; q < 4; ++q) dst[(s2 * NG + nn) * 4 + q] = acc[s2][nn][q];
+        } else {
+          own_tile = tile;                     // the head of a tile (only a run's last piece)
         }
-        __syncthreads();
-        if (my_tile >= 0 && my_ksl == 0) {
-          for (int o = 1; o < ks; ++o) {
-            const float* srcr = red + ((warp + o) * 32 + lane) * 16;
-#pragma unroll
-            for (int s = 0; s < 2; ++s)
-#pragma unroll
-              for (int nn = 0; nn < 2; ++nn)
-#pragma unroll
-                for (int q = 0; q < 4; ++q) acc[s][nn][q] += srcr[(s * 2 + nn) * 4 + q];
-          }
-          epilogue(my_tile);
-        }
-        staged = -1;   // bop now holds partials
+        ci = pend;
       }
-      __syncthreads();   // the block's h / y stores are issued
+      __syncthreads();   // every warp is done with bop; the parked pieces are visible
+
+      // ---- a tile split over warps: its first warp adds the later pieces in
+      //      warp order (each later warp's run begins inside the tile) ----
+      if (own_tile >= 0) {
+        const int tile_end = (own_tile + 1) * nkc;
+        for (int w2 = warp + 1; w2 < W; ++w2) {
+          const int b0 = fused_warp_begin(w2, total, W);
+          if (b0 >= tile_end) break;
+          if (fused_warp_begin(w2 + 1, total, W) == b0) continue;   // an empty run
+          const float* src = slot_s + (w2 * 32 + lane) * SLOTF;
+#pragma unroll
+          for (int s2 = 0; s2 < 2; ++s2)
+#pragma unroll
+            for (int nn = 0; nn < 2; ++nn)
+              if (nn < NG)
+#pragma unroll
+                for (int q = 0; q < 4; ++q) acc[s2][nn][q] += src[(s2 * NG + nn) * 4 + q];
+        }
+        epilogue(t0 + own_tile);
+      }
+      __syncthreads();   // the block's h / y stores are issued; the slots are free
 
       // ---- completion: fc1 publishes the segment's h rows (release) ----
       if (ph == 0 && tid == 0)

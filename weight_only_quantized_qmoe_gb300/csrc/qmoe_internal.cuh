@@ -161,7 +161,9 @@ struct FinalizeArgs {
 };
 cudaError_t launch_finalize(const FinalizeArgs& a, cudaStream_t s);
 
-size_t group_smem_bytes(int E);
+// Dynamic shared memory of the grouping CTA (routing T tokens in it: T > 0)
+// for R routes.
+size_t group_smem_bytes(int E, int T, int R);
 
 }  // namespace qmoe
 

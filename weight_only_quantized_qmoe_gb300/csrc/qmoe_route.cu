@@ -5,8 +5,9 @@
 // total_order_key / route_value_is_better / qmoe_route): experts are ranked
 // by a total-order key of the fp32 logit, ties to the lower index; the
 // weight of a selected expert is exp(l - max_all) divided by the sum over all
-// E experts, or over the k chosen when renormalising.  Here one warp ranks
-// one token (k warp-wide arg-max rounds) instead of one thread per token.
+// E experts, or over the k chosen when renormalising.  Here one warp ranks a
+// token (qmoe_topk.cuh for E <= 256; k warp-wide shuffle arg-max rounds
+// above) instead of one thread per token.
 //
 // Grouping replaces that page's count / 1-thread prefix / atomic-cursor
 // assignment with one CTA that builds a *stable* permutation (routes of an
@@ -16,6 +17,7 @@
 #include <climits>
 
 #include "qmoe_internal.cuh"
+#include "qmoe_topk.cuh"
 
 namespace qmoe {
 
@@ -25,7 +27,8 @@ __device__ __forceinline__ int total_order_key(float v) {
 }
 
 // One warp ranks the E logits of one token and writes ids[0..k) and
-// w[0..k).  NPL = logits held per lane (E <= 32 * NPL).
+// w[0..k).  NPL = logits held per lane (E <= 32 * NPL); used for E > 256,
+// where sorting each lane's logits would not pay.
 template <int NPL>
 __device__ void route_token(const float* __restrict__ lg, int E, int k, int normalize,
                             int* __restrict__ ids, float* __restrict__ w) {
@@ -85,12 +88,24 @@ __device__ void route_token(const float* __restrict__ lg, int E, int k, int norm
   for (int slot = lane; slot < k; slot += 32) w[slot] = expf(lg[ids[slot]] - mx) / denom;
 }
 
+// Tokens [t0, t0 + TOK) of the forward (those < T) by one warp.
+template <int NPL, int TOK>
+__device__ __forceinline__ void route_warp(const float* lg, int t0, const RouteArgs& a) {
+  if constexpr (NPL <= 8) {
+    topk_route_tokens<NPL, TOK>(lg, t0, a.T, a.E, a.k, a.normalize, a.ids, a.w);
+  } else {
+#pragma unroll
+    for (int u = 0; u < TOK; ++u)
+      if (t0 + u < a.T)
+        route_token<NPL>(lg + (size_t)(t0 + u) * a.E, a.E, a.k, a.normalize, a.ids + (size_t)(t0 + u) * a.k,
+                         a.w + (size_t)(t0 + u) * a.k);
+  }
+}
+
 template <int NPL>
 __global__ void __launch_bounds__(256) route_kernel(const RouteArgs a) {
   const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
-  if (t < a.T)
-    route_token<NPL>(a.logits + (size_t)t * a.E, a.E, a.k, a.normalize, a.ids + (size_t)t * a.k,
-                     a.w + (size_t)t * a.k);
+  if (t < a.T) route_warp<NPL, 1>(a.logits, t, a);
   pdl_launch_dependents();
 }
 
@@ -122,6 +137,39 @@ __device__ int block_exclusive_scan(int v, int* ws, int* total) {
   return excl;
 }
 
+// The single-CTA routing stages the logits when they take at most 64 KB.
+__host__ __device__ inline bool group_stages_logits(int T, int E) { return (int64_t)T * E <= 16384; }
+// The grouping CTA builds the permutation of R > 1024 routes in shared
+// memory when cnt, off, ws and the R ints take at most 200 KB.
+__host__ __device__ inline bool group_perm_in_smem(int R, int E) {
+  return R > 1024 && (int64_t)(33 * E + 32 + R) * 4 <= 200 * 1024;
+}
+
+// Work-lists: class 0 (decode kernel) for experts with 1..threshold rows,
+// class 1 (grouped GEMM) above; each cut into items of tb[cls] rows.  Thread
+// e < E holds expert e's row count and row offset; all threads call it.
+__device__ void build_worklists(const RouteArgs& a, int count, int excl, int* ws) {
+  const int tid = threadIdx.x;
+  for (int cls = 0; cls < 2; ++cls) {
+    const int tb = a.tb[cls];
+    int nb = 0;
+    if (tid < a.E && count > 0 && ((count > a.threshold) == (cls == 1))) nb = (count + tb - 1) / tb;
+    int ntot;
+    const int ib = block_exclusive_scan(nb, ws, &ntot);
+    for (int i = 0; i < nb; ++i) {
+      if (ib + i < a.cap[cls]) {
+        Item it;
+        it.e = tid;
+        it.start = excl + i * tb;
+        it.rows = min(tb, count - i * tb);
+        it.pad = 0;
+        a.items[cls][ib + i] = it;
+      }
+    }
+    if (tid == 0) a.n_items[cls] = min(ntot, a.cap[cls]);
+  }
+}
+
 // One CTA of 1024 threads: optional routing of all tokens (small T), then
 // counts, offsets, the stable permutation, its inverse and both work-lists.
 // Shared memory: cnt[32][E] (per-warp, per-expert counts, later bases),
@@ -133,19 +181,63 @@ __global__ void __launch_bounds__(1024) group_kernel(const RouteArgs a, int do_r
   int* cnt = smem;             // [32][E]
   int* off = smem + 32 * E;    // [E]
   int* ws = off + E;           // [32]
+  float* lg_s = reinterpret_cast<float*>(ws + 32);   // [T, E] when staged
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int R = a.T * a.k;
   const int nb = id_bits(E);
 
   if (do_route) {
-    for (int t = warp; t < a.T; t += 32)
-      route_token<NPL>(a.logits + (size_t)t * E, E, a.k, a.normalize, a.ids + (size_t)t * a.k,
-                       a.w + (size_t)t * a.k);
+    // the logits in shared memory when they fit (one coalesced pass), then
+    // two tokens per warp
+    const float* lg = a.logits;
+    if (group_stages_logits(a.T, E)) {
+      for (int i = tid; i < a.T * E; i += blockDim.x) lg_s[i] = a.logits[i];
+      __syncthreads();
+      lg = lg_s;
+    }
+    for (int t = 2 * warp; t < a.T; t += 64) route_warp<NPL, 2>(lg, t, a);
   } else {
     pdl_wait();
   }
   for (int i = tid; i < 32 * E; i += blockDim.x) cnt[i] = 0;
   __syncthreads();
+
+  if (R <= 32 * 32) {
+    // ---- up to 32 chunks of 32 routes, a warp each, all at once ----
+    const unsigned lt = (1u << lane) - 1u;
+    const int r = warp * 32 + lane;
+    const int e = r < R ? a.ids[r] : -1;
+    const unsigned peers = peers_of(e, nb);
+    const int rank = __popc(peers & lt);
+    if (e >= 0 && rank == 0) cnt[warp * E + e] = __popc(peers);
+    __syncthreads();
+    int count = 0;
+    if (tid < E) {
+      const int nch = (R + 31) / 32;
+      for (int w = 0; w < nch; ++w) {
+        const int c = cnt[w * E + tid];
+        cnt[w * E + tid] = count;
+        count += c;
+      }
+    }
+    int total;
+    const int excl = block_exclusive_scan(count, ws, &total);
+    if (tid < E) {
+      off[tid] = excl;
+      a.counts[tid] = count;
+      a.offsets[tid] = excl;
+    }
+    if (tid == 0) a.offsets[E] = total;
+    __syncthreads();
+    if (e >= 0) {
+      const int p = off[e] + cnt[warp * E + e] + rank;
+      a.perm[p] = r;
+      a.pos[r] = p;
+    }
+    build_worklists(a, count, excl, ws);
+    pdl_launch_dependents();
+    return;
+  }
 
   // Pass 1: each warp counts its contiguous segment of routes per expert.
   // Loads are issued kU 32-route groups at a time so their latencies overlap.
@@ -190,7 +282,10 @@ __global__ void __launch_bounds__(1024) group_kernel(const RouteArgs a, int do_r
   for (int i = tid; i < 32 * E; i += blockDim.x) cnt[i] += off[i % E];
   __syncthreads();
 
-  // Pass 2: stable placement, walking each segment in route order.
+  // Pass 2: stable placement, walking each segment in route order.  The
+  // permutation is scattered by expert: it is built in shared memory when it
+  // fits (after cnt, off and ws) and written out in one coalesced pass.
+  int* perm_s = group_perm_in_smem(R, E) ? ws + 32 : nullptr;
   const unsigned lt = (1u << lane) - 1u;
   for (int base = beg; base < end; base += 32 * kU) {
     int ev[kU];
@@ -206,7 +301,8 @@ __global__ void __launch_bounds__(1024) group_kernel(const RouteArgs a, int do_r
       const unsigned peers = peers_of(e, nb);
       if (e >= 0) {
         const int p = cnt[warp * E + e] + __popc(peers & lt);
-        a.perm[p] = r;
+        if (perm_s) perm_s[p] = r;
+        else a.perm[p] = r;
         a.pos[r] = p;
       }
       __syncwarp();
@@ -215,34 +311,24 @@ __global__ void __launch_bounds__(1024) group_kernel(const RouteArgs a, int do_r
     }
   }
 
-  // Work-lists: class 0 (decode kernel) for experts with 1..threshold rows,
-  // class 1 (grouped GEMM) above; each cut into items of tb[cls] rows.
-  for (int cls = 0; cls < 2; ++cls) {
-    const int tb = a.tb[cls];
-    int nb = 0;
-    if (tid < E && count > 0 && ((count > a.threshold) == (cls == 1))) nb = (count + tb - 1) / tb;
-    int ntot;
-    const int ib = block_exclusive_scan(nb, ws, &ntot);
-    for (int i = 0; i < nb; ++i) {
-      if (ib + i < a.cap[cls]) {
-        Item it;
-        it.e = tid;
-        it.start = excl + i * tb;
-        it.rows = min(tb, count - i * tb);
-        it.pad = 0;
-        a.items[cls][ib + i] = it;
-      }
-    }
-    if (tid == 0) a.n_items[cls] = min(ntot, a.cap[cls]);
+  if (perm_s) {
+    __syncthreads();
+    for (int i = tid; i < R; i += blockDim.x) a.perm[i] = perm_s[i];
   }
+  build_worklists(a, count, excl, ws);
   pdl_launch_dependents();
 }
 
-size_t group_smem_bytes(int E) { return (size_t)(33 * E + 32) * sizeof(int); }
+size_t group_smem_bytes(int E, int T, int R) {
+  size_t extra = 0;
+  if (T > 0 && group_stages_logits(T, E)) extra = (size_t)T * E * sizeof(float);
+  if (group_perm_in_smem(R, E) && (size_t)R * sizeof(int) > extra) extra = (size_t)R * sizeof(int);
+  return (size_t)(33 * E + 32) * sizeof(int) + extra;
+}
 
 template <int NPL>
 static cudaError_t launch_rg(const RouteArgs& a, bool fused, cudaStream_t s) {
-  const size_t smem = group_smem_bytes(a.E);
+  const size_t smem = group_smem_bytes(a.E, fused ? a.T : 0, a.T * a.k);
   cudaError_t err =
       cudaFuncSetAttribute(group_kernel<NPL>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (err != cudaSuccess) return err;
