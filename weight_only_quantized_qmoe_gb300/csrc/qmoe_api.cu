@@ -78,6 +78,8 @@ struct qmoe_layer {
   int* offsets = nullptr;
   int* perm = nullptr;
   int* pos = nullptr;
+  int* cntg = nullptr;         // spread grouping: route count / first position per (routing CTA, expert)
+  int* rnk = nullptr;          // spread grouping: rank of each route within its routing CTA and expert
   int* n_items = nullptr;
   Item* items[2] = {nullptr, nullptr};
   int cap_items[2] = {0, 0};
@@ -189,7 +191,7 @@ cudaError_t launch_half_bias(const float* src, float* dst, size_t n, int half, c
 void free_workspace(qmoe_layer* l) {
   void* bufs[] = {l->ids, l->w, l->counts, l->offsets, l->perm, l->pos, l->n_items, l->items[0],
                   l->items[1], l->hbuf, l->ybuf, l->status, l->x_stage, l->logits_stage,
-                  l->out_stage, l->xt, l->ht, l->out_acc, l->sync};
+                  l->out_stage, l->xt, l->ht, l->out_acc, l->sync, l->cntg, l->rnk};
   for (void* b : bufs)
     if (b) cudaFree(b);
   l->ids = nullptr;
@@ -206,6 +208,7 @@ void free_workspace(qmoe_layer* l) {
   l->ht = nullptr;
   l->out_acc = nullptr;
   l->sync = nullptr;
+  l->cntg = l->rnk = nullptr;
   l->tiles_ok = false;
   l->cap_T = 0;
 }
@@ -246,6 +249,9 @@ qmoe_status ensure_workspace(qmoe_layer* l, int64_t T) {
   QMOE_CUDA(l, dalloc(&l->offsets, (l->E + 1) * sizeof(int)), "allocate workspace");
   QMOE_CUDA(l, dalloc(&l->perm, R * sizeof(int)), "allocate workspace");
   QMOE_CUDA(l, dalloc(&l->pos, R * sizeof(int)), "allocate workspace");
+  // spread grouping: per routing CTA (8 tokens) and expert, per route
+  QMOE_CUDA(l, dalloc(&l->cntg, (size_t)((T + 7) / 8) * l->E * sizeof(int)), "allocate workspace");
+  QMOE_CUDA(l, dalloc(&l->rnk, R * sizeof(int)), "allocate workspace");
   QMOE_CUDA(l, dalloc(&l->n_items, 2 * sizeof(int)), "allocate workspace");
   for (int c = 0; c < 2; ++c) {
     const int64_t cap = items_cap(l, c, T, 4);
@@ -746,6 +752,8 @@ qmoe_status qmoe_forward(qmoe_layer* l, const void* x, const float* logits, void
   ra.offsets = l->offsets;
   ra.perm = l->perm;
   ra.pos = l->pos;
+  ra.cntg = l->cntg;
+  ra.rnk = l->rnk;
   ra.items[0] = l->items[0];
   ra.items[1] = l->items[1];
   ra.n_items = l->n_items;

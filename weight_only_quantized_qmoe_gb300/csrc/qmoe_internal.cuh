@@ -76,7 +76,19 @@ struct RouteArgs {
   int tb[2];             // rows per item of each class
   int threshold;         // experts with > threshold rows go to class 1
   int cap[2];            // capacity of each item list
+  // Grouping spread over the routing CTAs (many routes): per routing CTA and
+  // expert, its route count, then the expert's first position for that CTA
+  // [ceil(T / 8), E]; per route its rank among its CTA's routes of its
+  // expert [R].  Null: one CTA groups.
+  int* cntg;
+  int* rnk;
 };
+
+// Routes per routing CTA (8 tokens of k routes) and whether a forward of T
+// tokens takes the grouping spread over the routing CTAs.
+__host__ __device__ inline bool route_spread_grouping(const RouteArgs& a, bool fused) {
+  return !fused && a.cntg && a.rnk && (long long)a.T * a.k > 1024 && a.k <= 32;
+}
 
 cudaError_t launch_route_group(const RouteArgs& a, bool fused, cudaStream_t s);
 
@@ -163,7 +175,7 @@ cudaError_t launch_finalize(const FinalizeArgs& a, cudaStream_t s);
 
 // Dynamic shared memory of the grouping CTA (routing T tokens in it: T > 0)
 // for R routes.
-size_t group_smem_bytes(int E, int T, int R);
+size_t group_smem_bytes(int E, int T, int R, bool spread);
 
 }  // namespace qmoe
 

@@ -826,10 +826,28 @@ __global__ void __launch_bounds__((Ring<DEC, BITS>::threads), 1)
     float* tile32 = reinterpret_cast<float*>(smem + RG::epi_off(L.stage_bytes)) + q * 32 * kEpiPitch;
     int tc = 0;
     bool ok = true;
+    constexpr int NCH = RG::tile_n / 32;   // 32-token chunks of a tile
     for (int tile = blockIdx.x; tile < total_tiles && ok; tile += gridDim.x, ++tc) {
       const Item it = a.items[tile / L.ntiles];
       const int nt = tile % L.ntiles;
       const int ab = tc & 1;
+      // fc2 scatter: the token and weight of each of this lane's token
+      // columns, loaded while the tile's MMAs still run
+      int tok_c[NCH];
+      float w_c[NCH];
+#pragma unroll
+      for (int ch = 0; ch < NCH; ++ch) {
+        tok_c[ch] = 0;
+        w_c[ch] = 0.f;
+        if (EPI == 0 && !a.ybuf && ch * 32 + lane < it.rows) tok_c[ch] = a.perm[it.start + ch * 32 + lane];
+      }
+#pragma unroll
+      for (int ch = 0; ch < NCH; ++ch) {
+        if (EPI == 0 && !a.ybuf && ch * 32 + lane < it.rows) {
+          w_c[ch] = a.w[tok_c[ch]];
+          tok_c[ch] /= a.k;
+        }
+      }
       ok = wait_or_abort(&acc_full[ab], (tc >> 1) & 1, a.wait, abort_flag);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
@@ -837,15 +855,16 @@ __global__ void __launch_bounds__((Ring<DEC, BITS>::threads), 1)
       for (int c0 = 0; c0 < it.rows; c0 += 32) {
         uint32_t v[32];
         TC_LD32(tmem + ((uint32_t)(q * 32) << 16) + ab * RG::acc_cols + c0, v);
-        // route of token column c0 + lane
+        // token and weight of token column c0 + lane
         int my_tok = 0;
         float my_w = 0.f;
+#pragma unroll
+        for (int ch = 0; ch < NCH; ++ch)
+          if (ch * 32 == c0) {
+            my_tok = tok_c[ch];
+            my_w = w_c[ch];
+          }
         const bool col_ok = c0 + lane < it.rows;
-        if (EPI == 0 && col_ok && !a.ybuf) {
-          const int route = a.perm[it.start + c0 + lane];
-          my_tok = route / a.k;
-          my_w = a.w[route];
-        }
         __syncwarp();   // converged again before the warp-wide tcgen05.wait
         tc_wait_ld();
         if (GLU) {

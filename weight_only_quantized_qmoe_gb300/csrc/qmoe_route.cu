@@ -92,20 +92,73 @@ __device__ void route_token(const float* __restrict__ lg, int E, int k, int norm
 template <int NPL, int TOK>
 __device__ __forceinline__ void route_warp(const float* lg, int t0, const RouteArgs& a) {
   if constexpr (NPL <= 8) {
-    topk_route_tokens<NPL, TOK>(lg, t0, a.T, a.E, a.k, a.normalize, a.ids, a.w);
-  } else {
-#pragma unroll
-    for (int u = 0; u < TOK; ++u)
-      if (t0 + u < a.T)
-        route_token<NPL>(lg + (size_t)(t0 + u) * a.E, a.E, a.k, a.normalize, a.ids + (size_t)(t0 + u) * a.k,
-                         a.w + (size_t)(t0 + u) * a.k);
+    if (a.k <= 32) {   // a lane per rank
+      topk_route_tokens<NPL, TOK>(lg, t0, a.T, a.E, a.k, a.normalize, a.ids, a.w);
+      return;
+    }
   }
+#pragma unroll
+  for (int u = 0; u < TOK; ++u)
+    if (t0 + u < a.T)
+      route_token<NPL>(lg + (size_t)(t0 + u) * a.E, a.E, a.k, a.normalize, a.ids + (size_t)(t0 + u) * a.k,
+                       a.w + (size_t)(t0 + u) * a.k);
 }
 
+// Eight tokens per CTA, a warp each.  With the spread grouping the CTA then
+// counts its 8k routes per expert (a warp per chunk of 32 routes, ballot-built
+// peer masks) into cntg[blockIdx.x], and stores each route's rank among the
+// CTA's routes of its expert (stable) in rnk.  Dynamic shared memory: [8][E]
+// ints with the spread grouping.
 template <int NPL>
-__global__ void __launch_bounds__(256) route_kernel(const RouteArgs a) {
-  const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
+__global__ void __launch_bounds__(256) route_kernel(const RouteArgs a, int spread) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, tid = threadIdx.x;
+  const int t = blockIdx.x * 8 + warp;
   if (t < a.T) route_warp<NPL, 1>(a.logits, t, a);
+  if (spread) {
+    extern __shared__ int cc[];   // [8][E]
+    const int E = a.E, R = a.T * a.k;
+    for (int i = tid; i < 8 * E; i += 256) cc[i] = 0;
+    __syncthreads();              // also: every ids write of the CTA is visible
+    const int rb0 = blockIdx.x * 8 * a.k, rb1 = min(R, rb0 + 8 * a.k);
+    const int nch = (rb1 - rb0 + 31) / 32;   // <= 8 (k <= 32)
+    const unsigned lt = (1u << lane) - 1u;
+    int e = -1, rank = 0;
+    if (warp < nch) {
+      const int r = rb0 + warp * 32 + lane;
+      e = r < rb1 ? a.ids[r] : -1;
+      const unsigned peers = peers_of(e, id_bits(E));
+      rank = __popc(peers & lt);
+      if (e >= 0 && rank == 0) cc[warp * E + e] = __popc(peers);
+    }
+    __syncthreads();
+    for (int x = tid; x < E; x += 256) {
+      int run = 0;
+      for (int w = 0; w < nch; ++w) {
+        const int c = cc[w * E + x];
+        cc[w * E + x] = run;
+        run += c;
+      }
+      a.cntg[(size_t)blockIdx.x * E + x] = run;
+    }
+    __syncthreads();
+    if (e >= 0) a.rnk[rb0 + warp * 32 + lane] = cc[warp * E + e] + rank;
+  }
+  pdl_launch_dependents();
+}
+
+// Spread grouping, last step: each route's position = its expert's first
+// position for its routing CTA + its rank there; the permutation and its
+// inverse.
+__global__ void __launch_bounds__(256) scatter_kernel(const RouteArgs a) {
+  pdl_wait();
+  const int R = a.T * a.k;
+  const int r = blockIdx.x * 256 + threadIdx.x;
+  if (r < R) {
+    const int e = a.ids[r];
+    const int p = a.cntg[(size_t)(r / (8 * a.k)) * a.E + e] + a.rnk[r];
+    a.perm[p] = r;
+    a.pos[r] = p;
+  }
   pdl_launch_dependents();
 }
 
@@ -178,13 +231,61 @@ template <int NPL>
 __global__ void __launch_bounds__(1024) group_kernel(const RouteArgs a, int do_route) {
   extern __shared__ int smem[];
   const int E = a.E;
-  int* cnt = smem;             // [32][E]
-  int* off = smem + 32 * E;    // [E]
-  int* ws = off + E;           // [32]
-  float* lg_s = reinterpret_cast<float*>(ws + 32);   // [T, E] when staged
+  const bool spread = !do_route && route_spread_grouping(a, false);
+  int* cnt = smem;                                               // [32][E] (spread: [P][E], P * E <= 1024)
+  int* off = smem + (spread ? max(32 * E, 1024) : 32 * E);       // [E]
+  int* ws = off + E;                                             // [32]
+  float* lg_s = reinterpret_cast<float*>(ws + 32);               // [T, E] when staged
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int R = a.T * a.k;
   const int nb = id_bits(E);
+
+  if (spread) {
+    // ---- counts per routing CTA are in cntg: thread (part, e) walks expert
+    //      e's column over a contiguous range of routing CTAs, twice ----
+    pdl_wait();
+    int* psum = cnt;
+    const int nblk = (a.T + 7) / 8;
+    const int P = E >= 1024 ? 1 : 1024 / E;
+    const int e = tid % E, part = tid / E;
+    const bool mine = part < P;
+    const int b0 = mine ? (int)((long long)part * nblk / P) : 0;
+    const int b1 = mine ? (int)((long long)(part + 1) * nblk / P) : 0;
+    int s = 0;
+#pragma unroll 8
+    for (int b = b0; b < b1; ++b) s += a.cntg[(size_t)b * E + e];
+    if (mine) psum[part * E + e] = s;
+    __syncthreads();
+    int count = 0;
+    if (tid < E) {
+      for (int q = 0; q < P; ++q) {
+        const int v = psum[q * E + tid];
+        psum[q * E + tid] = count;
+        count += v;
+      }
+    }
+    int total;
+    const int excl = block_exclusive_scan(count, ws, &total);
+    if (tid < E) {
+      off[tid] = excl;
+      a.counts[tid] = count;
+      a.offsets[tid] = excl;
+    }
+    if (tid == 0) a.offsets[E] = total;
+    __syncthreads();
+    if (mine) {
+      int run = off[e] + psum[part * E + e];
+#pragma unroll 8
+      for (int b = b0; b < b1; ++b) {
+        const int c = a.cntg[(size_t)b * E + e];
+        a.cntg[(size_t)b * E + e] = run;
+        run += c;
+      }
+    }
+    build_worklists(a, count, excl, ws);
+    pdl_launch_dependents();
+    return;
+  }
 
   if (do_route) {
     // the logits in shared memory when they fit (one coalesced pass), then
@@ -319,7 +420,8 @@ __global__ void __launch_bounds__(1024) group_kernel(const RouteArgs a, int do_r
   pdl_launch_dependents();
 }
 
-size_t group_smem_bytes(int E, int T, int R) {
+size_t group_smem_bytes(int E, int T, int R, bool spread) {
+  if (spread) return (size_t)((32 * E > 1024 ? 32 * E : 1024) + E + 32) * sizeof(int);
   size_t extra = 0;
   if (T > 0 && group_stages_logits(T, E)) extra = (size_t)T * E * sizeof(float);
   if (group_perm_in_smem(R, E) && (size_t)R * sizeof(int) > extra) extra = (size_t)R * sizeof(int);
@@ -328,7 +430,8 @@ size_t group_smem_bytes(int E, int T, int R) {
 
 template <int NPL>
 static cudaError_t launch_rg(const RouteArgs& a, bool fused, cudaStream_t s) {
-  const size_t smem = group_smem_bytes(a.E, fused ? a.T : 0, a.T * a.k);
+  const bool spread = route_spread_grouping(a, fused);
+  const size_t smem = group_smem_bytes(a.E, fused ? a.T : 0, a.T * a.k, spread);
   cudaError_t err =
       cudaFuncSetAttribute(group_kernel<NPL>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (err != cudaSuccess) return err;
@@ -336,7 +439,7 @@ static cudaError_t launch_rg(const RouteArgs& a, bool fused, cudaStream_t s) {
     group_kernel<NPL><<<1, 1024, smem, s>>>(a, 1);
     return cudaGetLastError();
   }
-  route_kernel<NPL><<<(a.T + 7) / 8, 256, 0, s>>>(a);
+  route_kernel<NPL><<<(a.T + 7) / 8, 256, spread ? 8 * a.E * sizeof(int) : 0, s>>>(a, spread ? 1 : 0);
   err = cudaGetLastError();
   if (err != cudaSuccess) return err;
   cudaLaunchConfig_t cfg = {};
@@ -349,7 +452,12 @@ static cudaError_t launch_rg(const RouteArgs& a, bool fused, cudaStream_t s) {
   cfg.stream = s;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, group_kernel<NPL>, a, 0);
+  err = cudaLaunchKernelEx(&cfg, group_kernel<NPL>, a, 0);
+  if (err != cudaSuccess || !spread) return err;
+  cfg.gridDim = dim3((a.T * a.k + 255) / 256);
+  cfg.blockDim = dim3(256);
+  cfg.dynamicSmemBytes = 0;
+  return cudaLaunchKernelEx(&cfg, scatter_kernel, a);
 }
 
 cudaError_t launch_route_group(const RouteArgs& a, bool fused, cudaStream_t s) {
