@@ -280,15 +280,19 @@ PATH_NAMES = {1: "separate kernels", 2: "single launch"}
 
 def launches_per_step(cfg, path, min_rows):
     """Kernels one forward launches: the single launch, or the separate
-    sequence -- routing (fused with grouping for T <= 64, else route +
-    group), the x gather and one GEMM per projection when the grouped GEMM
-    runs, one decode-class kernel per projection when any expert can take
-    that class, and the combine."""
+    sequence -- routing (fused with grouping for T <= 64; else route +
+    group, + a scatter of the permutation past 1024 routes), one GEMM per
+    projection when the grouped GEMM runs (+ the x gather for T <= 64; above,
+    fc1 gathers itself), one decode-class kernel per projection when any
+    expert can take that class, and the combine."""
     if path == 2:
         return 1
     gemm_on = cfg.dtype != "f32" and cfg.T > min_rows
     decode_on = not gemm_on or min_rows > 0
-    return (1 if cfg.T <= 64 else 2) + (3 if gemm_on else 0) + (2 if decode_on else 0) + 1
+    R = cfg.T * cfg.k
+    routing = 1 if cfg.T <= 64 else (3 if R > 1024 and cfg.k <= 32 else 2)
+    gemm = (2 + (1 if cfg.T <= 64 else 0)) if gemm_on else 0
+    return routing + gemm + (2 if decode_on else 0) + 1
 
 
 def replicas_for(cfg, args):

@@ -291,6 +291,26 @@ def test_variant_parity(qm, name):
     check_out(out, O.forward(inp), cfg.dtype)
 
 
+# More than 1024 routes with k <= 32 past the single-CTA sizes (T > 64): the
+# grouping is spread over the routing CTAs (per-CTA counts and stable ranks,
+# one prefix CTA, a scatter kernel).
+SPREAD = {
+    "R1032_just_past": dict(T=129, E=8, k=8),
+    "E3_many_ranges": dict(T=400, E=3, k=3),
+    "E1024_k32": dict(T=72, E=1024, k=32, H=64, I=64),
+    "ragged_last_cta_T1001": dict(T=1001, E=64, k=8),
+}
+
+
+@pytest.mark.parametrize("name", sorted(SPREAD))
+def test_spread_grouping_parity(qm, name):
+    cfg = BASE.with_(**SPREAD[name])
+    inp = make_inputs(cfg)
+    layer, out = run_layer(qm, inp, path="gemm")
+    check_routing(layer, inp, path="gemm")
+    check_out(out, O.forward(inp), cfg.dtype)
+
+
 def test_all_tokens_on_one_expert_and_empty_experts(qm):
     cfg = BASE.with_(T=40, k=2, E=8)
     inp = make_inputs(cfg)

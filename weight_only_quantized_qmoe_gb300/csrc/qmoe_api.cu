@@ -80,6 +80,7 @@ struct qmoe_layer {
   int* pos = nullptr;
   int* cntg = nullptr;         // spread grouping: route count / first position per (routing CTA, expert)
   int* rnk = nullptr;          // spread grouping: rank of each route within its routing CTA and expert
+  int* gready = nullptr;       // fc1's overlapped gather: finished units per class-1 item
   int* n_items = nullptr;
   Item* items[2] = {nullptr, nullptr};
   int cap_items[2] = {0, 0};
@@ -191,7 +192,7 @@ cudaError_t launch_half_bias(const float* src, float* dst, size_t n, int half, c
 void free_workspace(qmoe_layer* l) {
   void* bufs[] = {l->ids, l->w, l->counts, l->offsets, l->perm, l->pos, l->n_items, l->items[0],
                   l->items[1], l->hbuf, l->ybuf, l->status, l->x_stage, l->logits_stage,
-                  l->out_stage, l->xt, l->ht, l->out_acc, l->sync, l->cntg, l->rnk};
+                  l->out_stage, l->xt, l->ht, l->out_acc, l->sync, l->cntg, l->rnk, l->gready};
   for (void* b : bufs)
     if (b) cudaFree(b);
   l->ids = nullptr;
@@ -208,7 +209,7 @@ void free_workspace(qmoe_layer* l) {
   l->ht = nullptr;
   l->out_acc = nullptr;
   l->sync = nullptr;
-  l->cntg = l->rnk = nullptr;
+  l->cntg = l->rnk = l->gready = nullptr;
   l->tiles_ok = false;
   l->cap_T = 0;
 }
@@ -259,6 +260,7 @@ qmoe_status ensure_workspace(qmoe_layer* l, int64_t T) {
     l->cap_items[c] = (int)cap;
     QMOE_CUDA(l, dalloc(&l->items[c], cap * sizeof(Item)), "allocate workspace");
   }
+  QMOE_CUDA(l, dalloc(&l->gready, (size_t)l->cap_items[1] * sizeof(int)), "allocate workspace");
   QMOE_CUDA(l, dalloc(&l->hbuf, (size_t)R * l->I * ds), "allocate workspace");
   QMOE_CUDA(l, dalloc(&l->ybuf, (size_t)R * l->H * sizeof(float)), "allocate workspace");
   QMOE_CUDA(l, dalloc(&l->status, sizeof(int)), "allocate workspace");
@@ -767,8 +769,14 @@ qmoe_status qmoe_forward(qmoe_layer* l, const void* x, const float* logits, void
     const int64_t per = ((int64_t)threshold + tb0 - 1) / tb0;
     if ((int64_t)l->E * per < ra.cap[0]) ra.cap[0] = (int)((int64_t)l->E * per);
   }
+  // fc1's grouped GEMM writes its token tiles itself, overlapped with its
+  // MMAs, at prefill shapes (T > 64); decode shapes gather first (measured:
+  // the overlap costs their fc1 more than the gather kernel takes)
+  const bool gemm_gathers = gemm && T > 64;
+  ra.gready = gemm_gathers ? l->gready : nullptr;
+  ra.gready_n = ra.cap[1];
   QMOE_CUDA(l, launch_route_group(ra, T <= 64, s), "launch routing");
-  if (gemm)
+  if (gemm && !gemm_gathers)
     QMOE_CUDA(l, launch_gather_tiles(x, l->perm, l->k, l->H, l->items[1], l->n_items + 1, ra.cap[1], l->xt, s),
               "launch gather");
   trace(l, QMOE_TRACE_ROUTED, s);
@@ -848,6 +856,14 @@ qmoe_status qmoe_forward(qmoe_layer* l, const void* x, const float* logits, void
         ga.bf16 = l->dtype == QMOE_BF16;
         ga.zp_offset = l->zp_offset;
         ga.btiles = f == 0 ? l->xt : l->ht;
+        if (f == 0) {
+          ga.gx = gemm_gathers ? x : nullptr;
+          ga.gH = l->H;
+          ga.gready = l->gready;
+          // fc2 reduces into the accumulator (finalize reads it, no clearing there)
+          ga.zacc = l->deterministic ? nullptr : l->out_acc;
+          ga.zacc_n4 = (size_t)T * l->H / 4;
+        }
         ga.htiles = l->ht;
         ga.h_ksteps = (l->I + 63) / 64;
         ga.out_acc = l->out_acc;

@@ -82,6 +82,10 @@ struct RouteArgs {
   // expert [R].  Null: one CTA groups.
   int* cntg;
   int* rnk;
+  // Unit counts of fc1's overlapped gather, one per class-1 item: cleared
+  // here for the GEMM that follows (or null).
+  int* gready;
+  int gready_n;
 };
 
 // Routes per routing CTA (8 tokens of k routes) and whether a forward of T

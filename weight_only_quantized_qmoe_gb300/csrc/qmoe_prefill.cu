@@ -236,7 +236,6 @@ __global__ void __launch_bounds__(256) finalize_acc_kernel(float* __restrict__ a
     store_d<DT>(out, 4 * i + 1, v.y);
     store_d<DT>(out, 4 * i + 2, v.z);
     store_d<DT>(out, 4 * i + 3, v.w);
-    a4[i] = make_float4(0.f, 0.f, 0.f, 0.f);   // ready for the next forward
   }
 }
 
@@ -385,6 +384,24 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, co
   *abort_flag = 1;
   return false;
 }
+
+// Bounded wait for a global count (acquire), giving up when another role aborted.
+__device__ __forceinline__ bool count_wait_or_abort(const int* p, int target, const WaitCfg& w,
+                                                    volatile int* abort_flag) {
+  for (long long i = 0; i < w.limit; ++i) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    if (v >= target) return true;
+    if ((i & 63) == 63 && *abort_flag) return false;
+    __nanosleep(32);
+  }
+  atomicExch(w.status, DEV_TIMEOUT);
+  *abort_flag = 1;
+  return false;
+}
+
+// Units (of 2 warps x rows) an item's overlapped gather is cut into.
+constexpr int kGatherUnits = 8;
 
 // The same with non-blocking polls: for the MMA-issuing thread, whose loop
 // paces the whole pipeline (a parked poll costs ~250 cycles even when the
@@ -600,7 +617,8 @@ __device__ __forceinline__ void bulk_g2s_elect(void* dst, const void* src, uint3
 // Warp roles (8 + 4 * groups warps):
 //   0      bulk-copy producer (whole warp, elect.sync): W + B of a stage into slot s
 //   1      MMA issuer (whole warp, elect.sync) and TMEM owner
-//   2..3   idle
+//   2..3   fc1: write the items' token tiles from x (overlapped gather) and
+//          clear the fc2 accumulator; otherwise idle
 //   4 ..   dequant groups of 4 warps; group g takes stage steps kc % groups == g,
 //          warp w owns TMEM lanes 32*(w%4)
 //   last 4 epilogue (TMEM lanes 32*(w%4))
@@ -674,6 +692,17 @@ __global__ void __launch_bounds__((Ring<DEC, BITS>::threads), 1)
       // (An L2 bulk prefetch a ring's depth ahead of each copy made the
       // kernel twice as slow: the copies queue behind the prefetches.)
       const TileSrc src = tile_src<DEC, BITS>(a, tile);
+      if (a.gx) {
+        // the item's token tile is written by the gathering warps (of any
+        // CTA): wait for all of its units, then make those generic-proxy
+        // writes visible to this thread's bulk copies
+        int okw = 1;
+        if (lane == 0)
+          okw = count_wait_or_abort(a.gready + tile / L.ntiles, 2 * kGatherUnits, a.wait, abort_flag) ? 1 : 0;
+        ok = __shfl_sync(0xffffffffu, okw, 0) != 0;
+        if (!ok) break;
+        asm volatile("fence.proxy.async.global;" ::: "memory");
+      }
       int kr = src.rot;
       for (int j = 0; j < nss; ++j, ++kc) {
         const int s = kc % kStages;
@@ -775,6 +804,64 @@ __global__ void __launch_bounds__((Ring<DEC, BITS>::threads), 1)
     tc_commit_elect(drain_bar);
     const WaitCfg drain{a.wait.status, kDrainWaitLimit};
     mbar_wait_bounded(drain_bar, 0, drain);
+  } else if (warp == 2 || warp == 3) {
+    // ---------------- fc1: the token tiles from x, overlapped with the MMAs ----------------
+    // Unit u = (item u / kGatherUnits, part u % kGatherUnits) goes to CTA
+    // u % gridDim.x, so the first wave's items are written by many CTAs at
+    // once.  A part is 2 x RPW rows, RPW per warp: a warp copies whole rows
+    // (one token lookup per row, lanes across the row, 16-byte loads, each
+    // 8-lane group storing one swizzled 128-byte row of a k-step tile), rows
+    // past the item's count up to the next multiple of 8 and chunks past H
+    // as zeros.  Then (with or without the gather) the fc2 accumulator is
+    // cleared, a slice per CTA.
+    if (a.gx) {
+      constexpr int RPW = RG::tile_n / (2 * kGatherUnits);
+      constexpr int U = 4;
+      const int cpr = L.ksteps * 8;
+      const int hv = a.gH / 8;
+      const uint4* xsrc = static_cast<const uint4*>(a.gx);
+      const int nunits = n_items * kGatherUnits;
+      for (int u = blockIdx.x; u < nunits; u += gridDim.x) {
+        const int item = u / kGatherUnits, part = u - item * kGatherUnits;
+        const Item it = a.items[item];
+        const int rows8 = (it.rows + 7) & ~7;
+        uint8_t* tile0 = const_cast<uint8_t*>(a.btiles) + tok_tile_offset(item, L.ksteps, 0);
+        for (int rr = 0; rr < RPW; ++rr) {
+          const int row = part * 2 * RPW + (warp - 2) * RPW + rr;
+          if (row >= rows8) break;
+          const bool real = row < it.rows;
+          const uint4* srow = xsrc + (size_t)(real ? a.perm[it.start + row] / a.k : 0) * hv;
+          uint8_t* drow = tile0 + row * 128;
+          for (int c0 = lane; c0 < cpr; c0 += 32 * U) {
+            uint4 v[U];
+#pragma unroll
+            for (int q = 0; q < U; ++q) {
+              const int c = c0 + 32 * q;
+              v[q] = (real && c < hv) ? srow[c] : make_uint4(0u, 0u, 0u, 0u);
+            }
+#pragma unroll
+            for (int q = 0; q < U; ++q) {
+              const int c = c0 + 32 * q;
+              if (c < cpr)
+                *reinterpret_cast<uint4*>(drow + (size_t)(c >> 3) * kTokTileBytes + (((c & 7) ^ (row & 7)) << 4)) =
+                    v[q];
+            }
+          }
+        }
+        __syncwarp();
+        if (lane == 0) {
+          asm volatile("fence.proxy.async.global;" ::: "memory");
+          __threadfence();
+          atomicAdd(a.gready + item, 1);
+        }
+      }
+    }
+    if (a.zacc) {
+      const size_t n4 = a.zacc_n4;
+      const size_t i0 = n4 * blockIdx.x / gridDim.x, i1 = n4 * (blockIdx.x + 1) / gridDim.x;
+      float4* z4 = reinterpret_cast<float4*>(a.zacc);
+      for (size_t i = i0 + (size_t)(warp - 2) * 32 + lane; i < i1; i += 64) z4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
   } else if (warp >= 4 && warp < kEpiWarp0) {
     // ---------------- dequant: packed weights -> 16-bit pairs in TMEM ----------------
     // full[s] also means the A slot is free: the producer refilled stage s

@@ -60,6 +60,17 @@ struct GemmArgs {
   const float* bias;       // fc1: [E, I, 2] (gate, up) pairs ; fc2: [E, H] ; or null
   float zp_offset;
   const uint8_t* btiles;   // B operand in the tiled token layout (L.ksteps steps per item)
+  // fc1 with the gather overlapped (prefill shapes): the kernel's two
+  // otherwise idle warps write btiles from x themselves, one (item, part)
+  // unit at a time spread over the CTAs, and count each item's finished
+  // units in gready; the producer waits for an item's count before its first
+  // copy from it.  (Decode shapes gather in a kernel of their own first:
+  // there the overlap measured slower.)
+  const void* gx;          // x [T, gH] 16-bit, or null: btiles is already written
+  int gH;
+  int* gready;             // [max_items] unit counts, zero at launch
+  float* zacc;             // fc1: the fc2 accumulator to clear meanwhile (zacc_n4 float4), or null
+  size_t zacc_n4;
   uint8_t* htiles;         // fc1: h written in the tiled token layout for fc2
   int h_ksteps;            // fc1: k-steps of h (ceil(I / 64))
   float* out_acc;          // fc2: fp32 [T, H] combine accumulator (fp32 reductions of w * y)

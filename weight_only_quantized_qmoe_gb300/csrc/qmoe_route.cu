@@ -239,6 +239,12 @@ __global__ void __launch_bounds__(1024) group_kernel(const RouteArgs a, int do_r
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int R = a.T * a.k;
   const int nb = id_bits(E);
+  if (a.gready) {
+    // after the previous forward's GEMMs (stream order; launched here after
+    // the routing CTAs' completion when they run first)
+    if (!do_route) pdl_wait();
+    for (int i = tid; i < a.gready_n; i += blockDim.x) a.gready[i] = 0;
+  }
 
   if (spread) {
     // ---- counts per routing CTA are in cntg: thread (part, e) walks expert
