@@ -58,7 +58,8 @@ def parse():
                     help="launch sequence: the library's automatic choice (default), the single "
                          "launch wherever it applies, or the separate kernels")
     ap.add_argument("--deterministic", action="store_true",
-                    help="slot-ordered combine on the tensor-core path (qmoe_set_deterministic)")
+                    help="slot-ordered combine on the tensor-core path at every size "
+                         "(qmoe_set_deterministic; default: automatic, ordered up to 64 tokens)")
     ap.add_argument("--l2", default="rotate", choices=["rotate", "flush"],
                     help="keep the timed steps' inputs out of the L2 by rotating over copies of the layer "
                          "larger than the L2 together (default), or by flushing it before each step")
@@ -323,7 +324,8 @@ def measure(q, cfg, args, dev, stream, flush, steps, warmup, fused=1, min_rows=0
         layer = q.QMoELayer.from_config(cfg)
         layer.set_fused_decode(fused)
         layer.set_gemm_min_rows(min_rows)
-        layer.set_deterministic(1 if args.deterministic else 0)
+        if args.deterministic:
+            layer.set_deterministic(1)   # else the layer's automatic choice
         layer.reserve(cfg.T)
         x, logits = q.load_inputs(layer, inp, device=dev)
         reps.append((layer, x, logits, torch.empty_like(x)))

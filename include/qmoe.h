@@ -194,15 +194,19 @@ qmoe_status qmoe_set_gemm_min_rows(qmoe_layer* layer, int min_rows);
 enum { QMOE_FUSED_OFF = 0, QMOE_FUSED_ON = 1, QMOE_FUSED_AUTO = 2 };
 qmoe_status qmoe_set_fused_decode(qmoe_layer* layer, int mode);
 
-/* The combine of the tensor-core grouped GEMM path: 0 (default) adds each
- * route's w * y into an fp32 [T, H] accumulator with fp32 reductions in the
- * fc2 epilogue (the order of the k additions may vary run to run: a last-bit
- * difference at most after rounding to D); 1 writes the y rows and adds the
- * k slots in ascending order in a separate pass, bitwise deterministic at the
- * cost of writing and reading T * k * H fp32 values.  The single launch and
- * the decode kernels always add the slots in order.  [qmoe.rs
+/* The combine of the tensor-core grouped GEMM path.  QMOE_COMBINE_REDUCE (0)
+ * adds each route's w * y into an fp32 [T, H] accumulator with fp32
+ * reductions in the fc2 epilogue (the order of the k additions may vary run
+ * to run: a last-bit difference at most after rounding to D);
+ * QMOE_COMBINE_ORDERED (1) writes the y rows and adds the k slots in
+ * ascending order in a separate pass, bitwise deterministic at the cost of
+ * writing and reading T * k * H fp32 values; QMOE_COMBINE_AUTO (2, the
+ * default) takes the ordered combine for forwards of at most 64 tokens and
+ * the reductions above.  The single launch and the decode kernels always
+ * add the slots in order.  Other values: INVALID_ARG.  [qmoe.rs
  * qmoe_combine_impl: slots summed in order] */
-qmoe_status qmoe_set_deterministic(qmoe_layer* layer, int enable);
+enum { QMOE_COMBINE_REDUCE = 0, QMOE_COMBINE_ORDERED = 1, QMOE_COMBINE_AUTO = 2 };
+qmoe_status qmoe_set_deterministic(qmoe_layer* layer, int mode);
 
 /* Which launch sequence the last qmoe_forward / qmoe_forward_host used:
  * QMOE_PATH_NONE (no forward with tokens yet), QMOE_PATH_SEPARATE (routing,

@@ -460,6 +460,25 @@ def test_trace_events_bracket_stages(qm):
     layer.set_trace_events(None)
 
 
+def test_automatic_combine_is_ordered_at_decode_sizes(qm):
+    # The default combine mode (QMOE_COMBINE_AUTO) adds the slots in order for
+    # forwards of <= 64 tokens on the tensor-core path too: two forwards agree
+    # bit for bit; an unknown mode is refused.
+    cfg = BASE.with_(T=48, E=16, k=4)
+    inp = make_inputs(cfg)
+    layer = qm.QMoELayer.from_config(cfg)
+    layer.set_fused_decode(0)
+    x, logits = qm.load_inputs(layer, inp)
+    out1 = layer.forward(x, logits).clone()
+    out2 = layer.forward(x, logits)
+    torch.cuda.synchronize()
+    assert layer.poll() == 0
+    assert torch.equal(out1, out2)
+    check_out(out1, O.forward(inp), cfg.dtype)
+    with pytest.raises(qm.QMoEError):
+        layer.set_deterministic(3)
+
+
 @pytest.mark.parametrize("min_rows", [0, 24])
 def test_deterministic_gemm_combine(qm, min_rows):
     # qmoe_set_deterministic: the fc2 GEMM writes y rows and the k slots are

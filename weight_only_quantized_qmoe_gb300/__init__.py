@@ -102,9 +102,11 @@ class QMoELayer:
         """QMOE_FUSED_OFF / QMOE_FUSED_ON / QMOE_FUSED_AUTO (default)."""
         self._check(binding.qmoe_set_fused_decode(self.handle, mode))
 
-    def set_deterministic(self, enable):
-        """Slot-ordered (bitwise deterministic) combine on the tensor-core path."""
-        self._check(binding.qmoe_set_deterministic(self.handle, enable))
+    def set_deterministic(self, mode):
+        """Combine of the tensor-core path: 0 / False = fp32 reductions,
+        1 / True = slot-ordered (bitwise deterministic), 2 = automatic (the
+        default: ordered up to 64 tokens)."""
+        self._check(binding.qmoe_set_deterministic(self.handle, int(mode)))
 
     def last_path(self):
         """QMOE_PATH_SEPARATE or QMOE_PATH_FUSED: the launch sequence of the

@@ -27,6 +27,7 @@ QMOE_F32, QMOE_F16, QMOE_BF16 = 0, 1, 2
 QMOE_TRACE_NUM_EVENTS = 5
 QMOE_PATH_NONE, QMOE_PATH_SEPARATE, QMOE_PATH_FUSED = 0, 1, 2
 QMOE_FUSED_OFF, QMOE_FUSED_ON, QMOE_FUSED_AUTO = 0, 1, 2
+QMOE_COMBINE_REDUCE, QMOE_COMBINE_ORDERED, QMOE_COMBINE_AUTO = 0, 1, 2
 
 _p = ctypes.c_void_p
 _i = ctypes.c_int
@@ -112,8 +113,8 @@ def qmoe_set_fused_decode(layer, mode):
     return load().qmoe_set_fused_decode(layer, int(mode))
 
 
-def qmoe_set_deterministic(layer, enable):
-    return load().qmoe_set_deterministic(layer, int(enable))
+def qmoe_set_deterministic(layer, mode):
+    return load().qmoe_set_deterministic(layer, int(mode))
 
 
 def qmoe_last_forward_path(layer):

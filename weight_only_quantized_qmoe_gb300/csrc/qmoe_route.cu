@@ -489,14 +489,29 @@ __global__ void __launch_bounds__(256) finalize_kernel(const FinalizeArgs a) {
        i += (size_t)gridDim.x * blockDim.x) {
     const int t = (int)(i / H4), m4 = (int)(i % H4);
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int j = 0; j < a.k; ++j) {
-      const int r = t * a.k + j;
-      const float wr = a.w[r];
-      const float4 v = y4[(size_t)a.pos[r] * H4 + m4];
-      acc.x = fmaf(wr, v.x, acc.x);
-      acc.y = fmaf(wr, v.y, acc.y);
-      acc.z = fmaf(wr, v.z, acc.z);
-      acc.w = fmaf(wr, v.w, acc.w);
+    // slots in groups of 8: every load of a group is issued before its adds
+    // (the adds stay in slot order)
+    for (int j0 = 0; j0 < a.k; j0 += 8) {
+      const int nj = min(8, a.k - j0);
+      float wr[8];
+      float4 v[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        if (u < nj) {
+          const int r = t * a.k + j0 + u;
+          wr[u] = a.w[r];
+          v[u] = y4[(size_t)a.pos[r] * H4 + m4];
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        if (u < nj) {
+          acc.x = fmaf(wr[u], v[u].x, acc.x);
+          acc.y = fmaf(wr[u], v[u].y, acc.y);
+          acc.z = fmaf(wr[u], v[u].z, acc.z);
+          acc.w = fmaf(wr[u], v[u].w, acc.w);
+        }
+      }
     }
     const size_t o = (size_t)t * a.H + (size_t)m4 * 4;
     store_d<DT>(a.out, o + 0, acc.x);
