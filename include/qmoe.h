@@ -325,7 +325,7 @@ qmoe_status qmoe_set_wait_limit(qmoe_layer* layer, int64_t iterations);
 #define QMOE_NOALLOC_SCRATCH_BYTES (4u << 20)
 
 /*
- * qmoe_forward without any allocation.  (No counterpart in the paper: this
+ * qmoe_forward without any allocation.  (No counterpart in the pages: this
  * is a convenience of this library.)
  *
  * Who needs it: callers that may not call cudaMalloc at the moment they run

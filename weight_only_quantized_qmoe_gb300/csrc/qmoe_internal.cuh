@@ -93,6 +93,13 @@ struct RouteArgs {
 __host__ __device__ inline bool route_spread_grouping(const RouteArgs& a, bool fused) {
   return !fused && a.cntg && a.rnk && (long long)a.T * a.k > 1024 && a.k <= 32;
 }
+// Tokens per routing CTA (8 warps): 8, or with the spread grouping up to 32
+// while the CTA's routes stay <= 256 (8 chunks of 32, a warp each).
+__host__ __device__ inline int route_tokens_per_cta(const RouteArgs& a, bool spread) {
+  if (!spread) return 8;
+  const int t = (256 / a.k) & ~7;
+  return t > 32 ? 32 : (t < 8 ? 8 : t);
+}
 
 cudaError_t launch_route_group(const RouteArgs& a, bool fused, cudaStream_t s);
 
@@ -465,6 +472,27 @@ __device__ __forceinline__ void store_d<QMOE_F16>(void* p, size_t i, float v) {
 template <>
 __device__ __forceinline__ void store_d<QMOE_BF16>(void* p, size_t i, float v) {
   static_cast<__nv_bfloat16*>(p)[i] = __float2bfloat16_rn(v);
+}
+
+// Four consecutive outputs (element i, i % 4 == 0) rounded into D with one
+// store.
+template <int DT>
+__device__ __forceinline__ void store_d4(void* p, size_t i, float4 v) {
+  if constexpr (DT == QMOE_F32) {
+    *reinterpret_cast<float4*>(static_cast<float*>(p) + i) = v;
+  } else if constexpr (DT == QMOE_F16) {
+    const __half2 a = __floats2half2_rn(v.x, v.y), b = __floats2half2_rn(v.z, v.w);
+    uint2 u;
+    u.x = *reinterpret_cast<const uint32_t*>(&a);
+    u.y = *reinterpret_cast<const uint32_t*>(&b);
+    *reinterpret_cast<uint2*>(static_cast<__half*>(p) + i) = u;
+  } else {
+    const __nv_bfloat162 a = __floats2bfloat162_rn(v.x, v.y), b = __floats2bfloat162_rn(v.z, v.w);
+    uint2 u;
+    u.x = *reinterpret_cast<const uint32_t*>(&a);
+    u.y = *reinterpret_cast<const uint32_t*>(&b);
+    *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(p) + i) = u;
+  }
 }
 
 // Gated activations in fp32 (CUDA's expf / tanhf).

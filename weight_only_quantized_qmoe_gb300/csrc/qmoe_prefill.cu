@@ -231,11 +231,7 @@ __global__ void __launch_bounds__(256) finalize_acc_kernel(float* __restrict__ a
   pdl_wait();
   float4* a4 = reinterpret_cast<float4*>(acc);
   for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n4; i += (size_t)gridDim.x * blockDim.x) {
-    const float4 v = a4[i];
-    store_d<DT>(out, 4 * i + 0, v.x);
-    store_d<DT>(out, 4 * i + 1, v.y);
-    store_d<DT>(out, 4 * i + 2, v.z);
-    store_d<DT>(out, 4 * i + 3, v.w);
+    store_d4<DT>(out, 4 * i, a4[i]);
   }
 }
 
@@ -400,8 +396,9 @@ __device__ __forceinline__ bool count_wait_or_abort(const int* p, int target, co
   return false;
 }
 
-// Units (of 2 warps x rows) an item's overlapped gather is cut into.
-constexpr int kGatherUnits = 8;
+// Units (of 2 warps x rows) an item's overlapped gather is cut into: enough
+// that the first wave's items (the first 152 tiles) are spread over every CTA.
+constexpr int kGatherUnits = 32;
 
 // The same with non-blocking polls: for the MMA-issuing thread, whose loop
 // paces the whole pipeline (a parked poll costs ~250 cycles even when the
@@ -816,7 +813,9 @@ __global__ void __launch_bounds__((Ring<DEC, BITS>::threads), 1)
     // cleared, a slice per CTA.
     if (a.gx) {
       constexpr int RPW = RG::tile_n / (2 * kGatherUnits);
-      constexpr int U = 4;
+      // 16-byte loads in flight per lane (a 4096-wide row per pass); the
+      // decode ring shape never gathers (and has fewer registers to spare)
+      constexpr int U = DEC ? 4 : 16;
       const int cpr = L.ksteps * 8;
       const int hv = a.gH / 8;
       const uint4* xsrc = static_cast<const uint4*>(a.gx);

@@ -104,22 +104,24 @@ __device__ __forceinline__ void route_warp(const float* lg, int t0, const RouteA
                        a.w + (size_t)(t0 + u) * a.k);
 }
 
-// Eight tokens per CTA, a warp each.  With the spread grouping the CTA then
-// counts its 8k routes per expert (a warp per chunk of 32 routes, ballot-built
-// peer masks) into cntg[blockIdx.x], and stores each route's rank among the
-// CTA's routes of its expert (stable) in rnk.  Dynamic shared memory: [8][E]
-// ints with the spread grouping.
+// TPB tokens per CTA (route_tokens_per_cta), two at a time per warp.  With
+// the spread grouping the CTA then counts its TPB * k <= 256 routes per
+// expert (a warp per chunk of 32 routes, ballot-built peer masks) into
+// cntg[blockIdx.x], and stores each route's rank among the CTA's routes of
+// its expert (stable) in rnk.  Dynamic shared memory: [8][E] ints with the
+// spread grouping.
 template <int NPL>
 __global__ void __launch_bounds__(256) route_kernel(const RouteArgs a, int spread) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, tid = threadIdx.x;
-  const int t = blockIdx.x * 8 + warp;
-  if (t < a.T) route_warp<NPL, 1>(a.logits, t, a);
+  const int TPB = route_tokens_per_cta(a, spread != 0);
+  for (int t = blockIdx.x * TPB + 2 * warp; t < min(a.T, (blockIdx.x + 1) * TPB); t += 16)
+    route_warp<NPL, 2>(a.logits, t, a);
   if (spread) {
     extern __shared__ int cc[];   // [8][E]
     const int E = a.E, R = a.T * a.k;
     for (int i = tid; i < 8 * E; i += 256) cc[i] = 0;
     __syncthreads();              // also: every ids write of the CTA is visible
-    const int rb0 = blockIdx.x * 8 * a.k, rb1 = min(R, rb0 + 8 * a.k);
+    const int rb0 = blockIdx.x * TPB * a.k, rb1 = min(R, rb0 + TPB * a.k);
     const int nch = (rb1 - rb0 + 31) / 32;   // <= 8 (k <= 32)
     const unsigned lt = (1u << lane) - 1u;
     int e = -1, rank = 0;
@@ -155,7 +157,7 @@ __global__ void __launch_bounds__(256) scatter_kernel(const RouteArgs a) {
   const int r = blockIdx.x * 256 + threadIdx.x;
   if (r < R) {
     const int e = a.ids[r];
-    const int p = a.cntg[(size_t)(r / (8 * a.k)) * a.E + e] + a.rnk[r];
+    const int p = a.cntg[(size_t)(r / (route_tokens_per_cta(a, true) * a.k)) * a.E + e] + a.rnk[r];
     a.perm[p] = r;
     a.pos[r] = p;
   }
@@ -251,7 +253,8 @@ __global__ void __launch_bounds__(1024) group_kernel(const RouteArgs a, int do_r
     //      e's column over a contiguous range of routing CTAs, twice ----
     pdl_wait();
     int* psum = cnt;
-    const int nblk = (a.T + 7) / 8;
+    const int TPB = route_tokens_per_cta(a, true);
+    const int nblk = (a.T + TPB - 1) / TPB;
     const int P = E >= 1024 ? 1 : 1024 / E;
     const int e = tid % E, part = tid / E;
     const bool mine = part < P;
@@ -445,7 +448,8 @@ static cudaError_t launch_rg(const RouteArgs& a, bool fused, cudaStream_t s) {
     group_kernel<NPL><<<1, 1024, smem, s>>>(a, 1);
     return cudaGetLastError();
   }
-  route_kernel<NPL><<<(a.T + 7) / 8, 256, spread ? 8 * a.E * sizeof(int) : 0, s>>>(a, spread ? 1 : 0);
+  const int tpb = route_tokens_per_cta(a, spread);
+  route_kernel<NPL><<<(a.T + tpb - 1) / tpb, 256, spread ? 8 * a.E * sizeof(int) : 0, s>>>(a, spread ? 1 : 0);
   err = cudaGetLastError();
   if (err != cudaSuccess) return err;
   cudaLaunchConfig_t cfg = {};
