@@ -402,6 +402,29 @@ def measure(q, cfg, args, dev, stream, flush, steps, warmup, fused=1, min_rows=0
         per_step = timed(steps_fns, steps, True)
         per_flushed = per_step
 
+    # the same rotated forwards captured back to back in one graph (as a
+    # model's layers run): no graph launch or event between two forwards
+    seq_ms = None
+    if args.mode == "graph" and nrep > 1:
+        S = 24
+        seq = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(seq, stream=stream):
+            for i in range(S):
+                lay, xx, lg, oo = reps[i % nrep]
+                lay.forward(xx, lg, oo, stream=stream)
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            seq.replay()
+            e0.record(stream)
+            for _ in range(2):
+                seq.replay()
+            e1.record(stream)
+        stream.synchronize()
+        seq_ms = e0.elapsed_time(e1) / (2 * S)
+        del seq
+
     stages = None
     if path == 1:
         tstep, ev = make_step(True, reps[0])
@@ -450,7 +473,7 @@ def measure(q, cfg, args, dev, stream, flush, steps, warmup, fused=1, min_rows=0
         lay.close()
     reps.clear()
     return {"ms": statistics.mean(per_step), "ms_median": statistics.median(per_step), "path": path,
-            "ms_l2_flushed": statistics.mean(per_flushed), "replicas": nrep,
+            "ms_l2_flushed": statistics.mean(per_flushed), "replicas": nrep, "ms_in_sequence": seq_ms,
             "stages_us": stages, "counts": counts, "e2e_ms": statistics.mean(e2e_ms),
             "h2d": cfg.T * cfg.H * ds + cfg.T * cfg.E * 4, "d2h": cfg.T * cfg.H * ds}
 
@@ -498,6 +521,7 @@ def workload_summary(cfg, m, hbm_peak, bf16_peak, peak_kind, world):
     roof, by, fl = roofline_of(cfg, m, hbm_peak, bf16_peak, peak_kind)
     d = {"us_per_layer": m["ms"] * 1e3, "tokens_per_s": job_throughput(cfg.T, world, m["ms"]),
          "l2": l2_note(cfg, m), "us_per_layer_l2_flushed": m["ms_l2_flushed"] * 1e3,
+         "us_per_layer_in_graph_sequence": m["ms_in_sequence"] * 1e3 if m["ms_in_sequence"] else None,
          "path": PATH_NAMES.get(m["path"], "?"), "active_experts": by["active"],
          "layer_bytes": by["layer"], "layer_flops": fl["layer"],
          "layer_hbm_frac": by["layer"] / (m["ms"] * 1e-3) / 1e9 / hbm_peak,
@@ -569,6 +593,8 @@ def run_ours(args):
                    "block_size": cfg.B, "zp": cfg.zp_mode, "act": cfg.act,
                    "mode": args.mode, "l2": l2_note(cfg, head),
                    "us_per_layer_l2_flushed": head["ms_l2_flushed"] * 1e3,
+                   "us_per_layer_in_graph_sequence": (head["ms_in_sequence"] * 1e3
+                                                      if head["ms_in_sequence"] else None),
                    "path": PATH_NAMES.get(head["path"], "?"),
                    "us_per_layer": ms * 1e3, "active_experts": by["active"],
                    "layer_bytes": by["layer"],
