@@ -39,7 +39,7 @@ L2_BYTES = 129 * 1024 * 1024
 WORKLOADS = ["decode_int2", "decode_many_expert_int4", "mixed_int3_int4", "prefill_int4"]
 # DRAM traffic of a kernel is reported only from an ncu capture of the exact
 # sources being run: lines "<kernel> <workload> <sources sha256[:16]> <bytes
-# per launch>" in this file (written from the capture).
+# per launch>" in this file, written from an ncu capture of those sources.
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.txt")
 
 
