@@ -93,7 +93,8 @@ struct qmoe_layer {
   uint8_t* xt = nullptr;       // x of GEMM-class items, tiled token layout (fc1 B operand)
   uint8_t* ht = nullptr;       // h of GEMM-class items, tiled token layout (fc2 B operand)
   float* out_acc = nullptr;    // fp32 [T, H] combine accumulator (mixed forwards)
-  int* sync = nullptr;         // counters of the single-launch decode forward (zero between launches)
+  int* sync = nullptr;         // counters of the single-launch decode forward (zero before the first launch)
+  size_t sync_n = 0;           // ints in sync
   bool tiles_ok = false;
   int num_sms = 0;
 
@@ -283,6 +284,7 @@ qmoe_status ensure_workspace(qmoe_layer* l, int64_t T) {
     const size_t segs = (size_t)(R < l->E ? R : l->E) + R / kFusedRowsPerGroup + 1;
     const size_t n = (size_t)kSyncHeader + segs;
     QMOE_CUDA(l, dalloc(&l->sync, n * sizeof(int)), "allocate workspace");
+    l->sync_n = n;
     QMOE_CUDA(l, cudaMemset(l->sync, 0, n * sizeof(int)), "clear counters");
   }
   if (l->num_sms == 0) {
@@ -999,6 +1001,9 @@ qmoe_status qmoe_poll_device_status(qmoe_layer* l) {
     QMOE_CUDA(l, cudaMemcpy(&v, w, sizeof(int), cudaMemcpyDeviceToHost), "read status");
     if (v != 0) QMOE_CUDA(l, cudaMemset(w, 0, sizeof(int)), "clear status");
     if (v == DEV_TIMEOUT) h = DEV_TIMEOUT;
+    // after a wait of the layer ran out, its single-launch counters start over
+    if (v != 0 && w == l->status && l->sync)
+      QMOE_CUDA(l, cudaMemset(l->sync, 0, l->sync_n * sizeof(int)), "clear counters");
   }
   if (h == DEV_TIMEOUT) return fail(l, QMOE_ERR_TIMEOUT, "a bounded device-side wait ran out");
   return QMOE_OK;

@@ -59,9 +59,10 @@ constexpr int kFusedMaxK = 32;
 constexpr int kFusedMaxWarps = 16;   // warps per CTA: 16 (one CTA per SM) or 8 (two)
 constexpr int kFusedRowsPerGroup = 16;
 constexpr int kFusedStages = 4;      // cp.async ring stages per warp (3 in flight)
-// Counters in the sync buffer: [0] unused, [1] exit, [2] a flag nothing sets
-// (the injected stall waits on it), [3] CTAs done with fc2, then
-// done1[segment].
+// Counters in the sync buffer: [0] launches so far (the epoch), [1] unused,
+// [2] a flag nothing sets (the injected stall waits on it), [3] CTAs done
+// with fc2 over all launches (launch e waits for gridDim * (e + 1)), then
+// done1[segment] (zero between launches).
 constexpr int kSyncHeader = 4;
 
 struct FusedProj {
@@ -93,7 +94,7 @@ struct FusedArgs {
   int* n_items;
   void* hbuf;           // [R, I] D, by route
   float* ybuf;          // [R, H] f32, by route
-  int* sync;            // kSyncHeader + max segments ints, zero between launches
+  int* sync;            // kSyncHeader + max segments ints (zero before the first launch)
   int max_seg;          // capacity of done1
   int ng_max;           // token groups of 8 the B staging is sized for (1 or 2)
   int sb;               // bytes per ring stage
@@ -378,11 +379,13 @@ __device__ __forceinline__ FusedGeom fused_geom(const DecodeLayout& L) {
 
 // Bounded wait of one thread until *p >= target; false (and DEV_TIMEOUT
 // recorded) if it ran out, or at once if the layer already timed out.
+// Bounded acquire wait until *p reaches target (wrap-around safe: the grid
+// arrival counter only grows).
 __device__ __forceinline__ bool fused_wait_geq(const int* p, int target, const WaitCfg& w) {
   for (long long i = 0; i < w.limit; ++i) {
     int v;
     asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-    if (v >= target) return true;
+    if ((int)((unsigned)v - (unsigned)target) >= 0) return true;
     if ((i & 63) == 63 && *reinterpret_cast<volatile int*>(w.status) != 0) return false;
     __nanosleep(64);
   }
@@ -554,6 +557,7 @@ __global__ void __launch_bounds__(kFusedMaxWarps * 32, 1) fused_decode_kernel(co
   int* tot_s = reinterpret_cast<int*>(smem + pl.ring_off + pq.tot_off);
   const int NCH = (R + 31) / 32;   // route chunks (<= warps: R <= 32 * warps)
   for (int i = tid; i < NCH * E; i += NT) cntw_s[i] = 0;
+  if (tid == 0) bc[6] = *reinterpret_cast<volatile const int*>(a.sync);   // this launch's epoch
   __syncthreads();
   // ---- a layer whose weights fit the L2 many times over (small decode
   //      layers) has them pulled into the L2 while the CTAs route (issued
@@ -906,11 +910,22 @@ __global__ void __launch_bounds__(kFusedMaxWarps * 32, 1) fused_decode_kernel(co
   cp_async_wait<0>();   // the producer's trailing (empty) groups
 
   // ---- every y row is written once all CTAs arrive; then each CTA adds the
-  //      k slots in order for its equal share of the outputs ----
+  //      k slots in order for its equal share of the outputs.  The arrival
+  //      counter only grows (this launch's target: gridDim * (epoch + 1)),
+  //      so no CTA has to reset it: the last CTA to arrive clears the
+  //      segment counters (no CTA reads them any more) and bumps the epoch
+  //      for the next launch, and every CTA leaves right after its share ----
   __syncthreads();
   if (tid == 0) {
-    asm volatile("red.release.gpu.global.add.s32 [%0], 1;" ::"l"(a.sync + 3) : "memory");
-    fused_wait_geq(a.sync + 3, (int)gridDim.x, a.wait);
+    const unsigned target = (unsigned)gridDim.x * (unsigned)(bc[6] + 1);
+    int old;
+    asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], 1;" : "=r"(old) : "l"(a.sync + 3) : "memory");
+    if ((unsigned)old + 1u == target) {
+      for (int i = 0; i < a.max_seg; ++i) done1[i] = 0;
+      *reinterpret_cast<volatile int*>(a.sync) = bc[6] + 1;
+    } else {
+      fused_wait_geq(a.sync + 3, (int)target, a.wait);
+    }
   }
   __syncthreads();
   {
@@ -930,29 +945,11 @@ __global__ void __launch_bounds__(kFusedMaxWarps * 32, 1) fused_decode_kernel(co
         s4.w = fmaf(wr, __uint_as_float(uu.w), s4.w);
       }
       const size_t o = (size_t)t * a.H + m;
-      if (BF16) {
-        store_d<QMOE_BF16>(a.out, o, s4.x); store_d<QMOE_BF16>(a.out, o + 1, s4.y);
-        store_d<QMOE_BF16>(a.out, o + 2, s4.z); store_d<QMOE_BF16>(a.out, o + 3, s4.w);
-      } else {
-        store_d<QMOE_F16>(a.out, o, s4.x); store_d<QMOE_F16>(a.out, o + 1, s4.y);
-        store_d<QMOE_F16>(a.out, o + 2, s4.z); store_d<QMOE_F16>(a.out, o + 3, s4.w);
-      }
+      if (BF16) store_d4<QMOE_BF16>(a.out, o, s4);
+      else store_d4<QMOE_F16>(a.out, o, s4);
     }
   }
 
-  // ---- the last CTA out clears the counters for the next launch ----
-  __syncthreads();
-  if (tid == 0) {
-    int old;
-    asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], 1;" : "=r"(old) : "l"(a.sync + 1) : "memory");
-    bc[5] = old == (int)gridDim.x - 1 ? 1 : 0;
-  }
-  __syncthreads();
-  if (bc[5]) {
-    const int nsync = kSyncHeader + a.max_seg;
-    for (int i = tid; i < nsync; i += NT) a.sync[i] = 0;
-    __threadfence();
-  }
 }
 
 // Launch of one instantiated width pair (explicitly instantiated in
